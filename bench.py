@@ -1,0 +1,419 @@
+#!/usr/bin/env python3
+"""Benchmark of the GQA AV decode reduction on GB300.
+
+One step = one call of gqa_av_decode on one batch of the Llama-style decode
+workload (B=1, Cmax=8192, Hq=32, Hkv=8, D=128, bf16 V, full-length context)
+unless --workload names another. Metric: achieved HBM GB/s over the
+compulsory bytes (every in-range V row once, every in-range attn weight once,
+out once, seq_lens), with µs/call as ms_per_step.
+
+Device timing: the K calls are captured in CUDA graphs (one call per node,
+cycling through rotating input sets whose total exceeds 3x the L2 size, so
+every call reads cold inputs) and replayed between CUDA events on the
+launching stream. e2e: the same calls through the public API with the inputs
+copied from pinned host memory and out copied back, inside the timed region.
+
+`--impl reference` times the fp64 CPU oracle (the only reference this method
+has) on the host cores, on a bounded sample of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from gqa_attention_weighted_gb300 import workloads as W  # noqa: E402
+
+METRIC = "GQA AV decode achieved HBM GB/s over compulsory bytes (V read once), µs/call"
+UNIT = "GB/s"
+DEFAULT_WORKLOAD = "llama"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["gqa_attention_weighted_gb300/csrc/gqa_av_kernel.cuh",
+                  "gqa_attention_weighted_gb300/csrc/gqa_av_instances.cuh",
+                  "gqa_attention_weighted_gb300/csrc/gqa_av_api.cu"]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def committed_traffic(workload: str, mode: int):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source for this workload and mode."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            entries = json.load(f)
+    except (OSError, ValueError):
+        return None
+    for e in entries:
+        if (e.get("kernel_hash") == kernel_hash() and e.get("workload") == workload
+                and e.get("mode") == mode):
+            return e.get("traffic_bytes_per_launch")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        if shutil.which("nvidia-smi"):
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.flush()
+        with open(self.file.name) as f:
+            rows = [r.strip().split(",") for r in f if r.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl != "reference" else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda") if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args, rank, world, local):
+    import gqa_attention_weighted_gb300 as gq
+
+    w = W.get(args.workload)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    mode = {"auto": gq.MODE_AUTO, "gqa": gq.MODE_GQA, "per_head": gq.MODE_PER_HEAD}[args.mode]
+    x = W.generate(w, dev, pad="zero")
+    lens = x["seq_lens"].cpu().tolist()
+    cbytes = W.compulsory_bytes(w, lens)
+    flops = W.flops(w, lens)
+
+    # Rotating input sets: total > 3x L2 so every call reads its inputs from HBM.
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    set_bytes = x["v"].numel() * 2 + x["attn"].numel() * 4 + w.B * w.Hq * w.D * 4
+    n_sets = max(1, math.ceil(3 * l2 / set_bytes)) if set_bytes < 3 * l2 else 1
+    sets = [x] + [{k: t.clone() for k, t in x.items()} for _ in range(n_sets - 1)]
+    outs = [torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device=dev) for _ in range(n_sets)]
+
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            s = sets[i % n_sets]
+            gq.gqa_av_decode(s["attn"], s["v"], s["seq_lens"], outs[i % n_sets], mode=mode)
+        stream.synchronize()
+        gq.gqa_av_device_status(stream)
+
+        chunk = min(args.steps, args.graph_len)
+        reps, rem = divmod(args.steps, chunk)
+
+        def capture(n):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    s = sets[i % n_sets]
+                    gq.gqa_av_decode(s["attn"], s["v"], s["seq_lens"], outs[i % n_sets],
+                                     mode=mode)
+            return g
+
+        g_main = capture(chunk)
+        g_rem = capture(rem) if rem else None
+        g_main.replay()  # graph warm-up (untimed)
+        stream.synchronize()
+
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        with ClockSampler(local) as clk:
+            start.record(stream)
+            for _ in range(reps):
+                g_main.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            end.record(stream)
+            end.synchronize()
+        torch.cuda.synchronize()
+        barrier(world)
+        elapsed_ms = start.elapsed_time(end)
+        gq.gqa_av_device_status(stream)
+
+    elapsed_ms = max_over_ranks(elapsed_ms, world)
+    ms_per_step = elapsed_ms / args.steps
+    value = cbytes * args.steps * world / (elapsed_ms * 1e-3) / 1e9
+    per_launch_s = ms_per_step * 1e-3
+    achieved = cbytes / per_launch_s / 1e9
+    peak, peak_kind = measured_peak()
+
+    e2e = run_e2e(gq, w, x, mode, dev, args, world)
+    plan = gq.gqa_av_plan(w.B, w.Cmax, w.Hq, w.Hkv, w.D, gq.native.v_dtype_code(x["v"].dtype), mode)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_baseline(w, x, args.cpu_seconds)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "us_per_call": ms_per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {**w.describe(), "mode": args.mode, "resolved_mode": plan["mode"],
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "compulsory_bytes_per_call": cbytes, "flops_per_call": flops,
+                   "l2": f"rotating {n_sets} input sets, {n_sets * set_bytes / 1e6:.0f} MB "
+                         f"(L2 {l2 / 1e6:.0f} MB)",
+                   "timing": f"CUDA graphs of {chunk} calls x {reps}"
+                             + (f" + {rem}" if rem else "") + ", events on the launch stream",
+                   "plan": plan},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_kind": f"{peak_kind} hbm_gbs (copy)",
+                     "frac_of_8tbs_nominal": round(achieved / 8000.0, 4),
+                     "traffic": committed_traffic(w.name, plan["mode"]),
+                     "kernel": "gqa_av_kernel", "kernel_hash": kernel_hash()},
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(gq, w, x, mode, dev, args, world):
+    """Same call with host inputs: pinned H2D copies, the call, D2H of out."""
+    host = {k: t.cpu().pin_memory() for k, t in x.items()}
+    out_host = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32).pin_memory()
+    dbuf = {k: torch.empty_like(t) for k, t in x.items()}
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * 4
+    steps = max(1, min(args.e2e_steps, args.steps))
+
+    def step():
+        for k in host:
+            dbuf[k].copy_(host[k], non_blocking=True)
+        gq.gqa_av_decode(dbuf["attn"], dbuf["v"], dbuf["seq_lens"], out, mode=mode)
+        out_host.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+        stream.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        start.record(stream)
+        for _ in range(steps):
+            step()
+        end.record(stream)
+        end.synchronize()
+        barrier(world)
+    ms = max_over_ranks(start.elapsed_time(end), world) / steps
+    cbytes = W.compulsory_bytes(w, x["seq_lens"].cpu().tolist())
+    return {"value": round(cbytes * world / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
+            "ms_per_step": ms, "steps": steps, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+# --------------------------------------------------------- oracle timings
+def oracle_inputs(w, x, rows):
+    """The workload cut to its first `rows` context positions (a bounded sample)."""
+    import numpy as np
+    attn = x["attn"][:, :rows].contiguous().cpu().numpy()
+    vb = x["v"][:, :rows].contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+    lens = x["seq_lens"].cpu().clamp(max=rows).numpy().astype(np.int32)
+    return attn, vb, lens
+
+
+def oracle_baseline(w, x, seconds):
+    """The fp64 oracle, as it stands, on the host cores: repeated passes over a
+    context prefix of the workload for about `seconds` seconds."""
+    import oracle
+    cores = oracle.host_cores()
+    rows = w.Cmax
+    attn, vb, lens = oracle_inputs(w, x, rows)
+    t0 = time.perf_counter()
+    oracle.gqa_av(attn, vb, w.v_dtype, lens, nthreads=cores)
+    t1 = time.perf_counter() - t0
+    if t1 > seconds:  # shrink the sample so one pass fits the budget
+        rows = max(1, int(rows * seconds / t1 / 2))
+        attn, vb, lens = oracle_inputs(w, x, rows)
+    sample_bytes = W.compulsory_bytes(w, lens.tolist())
+    n, t_total = 0, 0.0
+    while t_total < seconds or n < 1:
+        t0 = time.perf_counter()
+        oracle.gqa_av(attn, vb, w.v_dtype, lens, nthreads=cores)
+        t_total += time.perf_counter() - t0
+        n += 1
+    return {"value": round(sample_bytes * n / t_total / 1e9, 4), "unit": UNIT, "cores": cores,
+            "kind": "oracle",
+            "sample": f"{n} passes over context positions [0, {rows}) of {w.name} "
+                      f"({sample_bytes} compulsory bytes per pass), fp64, {t_total:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the oracle timed per step on a bounded sample."""
+    if rank != 0:
+        return
+    import oracle
+    w = W.get(args.workload)
+    x = W.generate(w, "cpu", pad="zero")
+    cores = oracle.host_cores()
+    budget = 90.0  # seconds for warm-up plus timed steps together
+    rows = w.Cmax
+    attn, vb, lens = oracle_inputs(w, x, rows)
+    t0 = time.perf_counter()
+    oracle.gqa_av(attn, vb, w.v_dtype, lens, nthreads=cores)
+    t1 = max(time.perf_counter() - t0, 1e-6)
+    per_step = budget / max(1, args.steps + args.warmup)
+    if t1 > per_step:
+        rows = max(1, int(rows * per_step / t1))
+        attn, vb, lens = oracle_inputs(w, x, rows)
+    sample_bytes = W.compulsory_bytes(w, lens.tolist())
+    for _ in range(args.warmup):
+        oracle.gqa_av(attn, vb, w.v_dtype, lens, nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gqa_av(attn, vb, w.v_dtype, lens, nthreads=cores)
+    elapsed = time.perf_counter() - t0
+    value = sample_bytes * args.steps / elapsed / 1e9
+    sample = (f"context positions [0, {rows}) of {w.name} per step "
+              f"({sample_bytes} compulsory bytes), fp64 oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": elapsed * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {**w.describe(), "sample_rows": rows},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    help="one of: " + ", ".join(W.ALIASES))
+    ap.add_argument("--mode", choices=["auto", "gqa", "per_head"], default="auto")
+    ap.add_argument("--graph-len", type=int, default=500)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.steps < 1 or args.warmup < 0:
+        ap.error("--steps must be >= 1 and --warmup >= 0")
+
+    rank, world, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            if not torch.cuda.is_available():
+                raise SystemExit("bench.py: the GB300 arm needs a CUDA GPU")
+            run_gpu(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

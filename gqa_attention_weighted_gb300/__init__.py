@@ -1,0 +1,21 @@
+"""GB300-native grouped-query-attention AV decode reduction.
+
+    out[b, q_h, d] = sum_{c < L_b} attn[b, c, q_h] * V[b, c, q_h // G, d]
+
+computed by hand-written sm_103a kernels behind a C ABI (include/gqa_av.h).
+``workloads`` (seeded inputs) imports without the CUDA library; the binding
+functions below need the built library and raise ImportError without it.
+"""
+from . import workloads  # noqa: F401
+
+_BINDING = ("gqa_av_decode", "gqa_av_decode_per_head", "gqa_av_decode_tuned", "gqa_av_plan",
+            "gqa_av_workspace_bytes", "gqa_av_set_workspace", "gqa_av_device_status",
+            "gqa_av_status_string", "gqa_av_last_error", "GqaAvError", "MODE_AUTO",
+            "MODE_PER_HEAD", "MODE_GQA", "GQA_AV_BF16", "GQA_AV_FP16")
+
+
+def __getattr__(name):
+    if name in _BINDING or name == "native":
+        from . import _native
+        return _native if name == "native" else getattr(_native, name)
+    raise AttributeError(name)

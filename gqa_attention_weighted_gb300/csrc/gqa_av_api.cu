@@ -1,0 +1,518 @@
+// Host side of the C ABI declared in include/gqa_av.h: argument checks, mode
+// resolution (the override knob on the page "pytorch/executorch pull 21063",
+// bullet on `gqa_override`), launch planning, the per-device workspace, TMA
+// tensor-map encoding and dispatch to the kernel instantiations.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+
+#include "gqa_av.h"
+#include "gqa_av_kernel.cuh"
+
+namespace gqa_av {
+
+// Explicit instantiations live in gqa_av_bf16.cu / gqa_av_fp16.cu.
+#define GQA_AV_DECLARE(TAG, GC)                                                          \
+  extern template cudaError_t launch<TAG, GC>(const Params&, int, int, cudaStream_t);    \
+  extern template cudaError_t occupancy<TAG, GC>(int, int, int*);
+#define GQA_AV_DECLARE_ALL(TAG)                                                              \
+  GQA_AV_DECLARE(TAG, 1) GQA_AV_DECLARE(TAG, 2) GQA_AV_DECLARE(TAG, 3) GQA_AV_DECLARE(TAG, 4) \
+  GQA_AV_DECLARE(TAG, 5) GQA_AV_DECLARE(TAG, 6) GQA_AV_DECLARE(TAG, 7) GQA_AV_DECLARE(TAG, 8) \
+  GQA_AV_DECLARE(TAG, 12) GQA_AV_DECLARE(TAG, 16)
+GQA_AV_DECLARE_ALL(Bf16Tag)
+GQA_AV_DECLARE_ALL(Fp16Tag)
+
+namespace {
+
+constexpr int kHeadChunks[] = {16, 12, 8, 7, 6, 5, 4, 3, 2, 1};
+constexpr size_t kStatusBytes = 256;               // device status word + padding
+constexpr int kMaxTicketTiles = 65536;             // tiles that can share a split combine
+constexpr size_t kTicketBytes = kMaxTicketTiles * sizeof(unsigned);
+constexpr size_t kHeaderBytes = kStatusBytes + kTicketBytes;
+constexpr long long kWaitTimeoutNs = 2000000000LL; // 2 s bound on every mbarrier wait
+
+thread_local std::string g_last_error;
+
+int fail(int status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return status;
+}
+
+int fail_cuda(cudaError_t e, const char* what) {
+  return fail(GQA_AV_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ----------------------------------------------------------------- dispatch
+using LaunchFn = cudaError_t (*)(const Params&, int, int, cudaStream_t);
+using OccFn = cudaError_t (*)(int, int, int*);
+
+template <typename Tag>
+bool pick(int gc, LaunchFn* l, OccFn* o) {
+  switch (gc) {
+#define GQA_AV_CASE(GC)          \
+  case GC:                       \
+    *l = launch<Tag, GC>;        \
+    *o = occupancy<Tag, GC>;     \
+    return true;
+    GQA_AV_CASE(1) GQA_AV_CASE(2) GQA_AV_CASE(3) GQA_AV_CASE(4) GQA_AV_CASE(5)
+    GQA_AV_CASE(6) GQA_AV_CASE(7) GQA_AV_CASE(8) GQA_AV_CASE(12) GQA_AV_CASE(16)
+#undef GQA_AV_CASE
+    default:
+      return false;
+  }
+}
+
+bool pick_kernel(int v_dtype, int gc, LaunchFn* l, OccFn* o) {
+  return v_dtype == GQA_AV_BF16 ? pick<Bf16Tag>(gc, l, o) : pick<Fp16Tag>(gc, l, o);
+}
+
+// ------------------------------------------------------------- device info
+struct DeviceInfo {
+  int sms = 0;
+  int smem_optin = 0;
+  bool ok = false;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceInfo> g_devices;
+std::map<std::tuple<int, int, int, int>, int> g_occupancy;  // (dev, dtype, gc, smem) -> ctas/SM
+
+int device_info(int dev, DeviceInfo* out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_devices.find(dev);
+  if (it != g_devices.end()) {
+    *out = it->second;
+    return GQA_AV_OK;
+  }
+  DeviceInfo di;
+  cudaError_t e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
+  di.ok = true;
+  g_devices[dev] = di;
+  *out = di;
+  return GQA_AV_OK;
+}
+
+int ctas_per_sm(int dev, int smem_limit, int v_dtype, int gc, int smem, int* n) {
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_occupancy.find(std::make_tuple(dev, v_dtype, gc, smem));
+    if (it != g_occupancy.end()) {
+      *n = it->second;
+      return GQA_AV_OK;
+    }
+  }
+  LaunchFn l;
+  OccFn o;
+  if (!pick_kernel(v_dtype, gc, &l, &o)) return fail(GQA_AV_ERR_UNSUPPORTED, "no kernel for GC=%d", gc);
+  int k = 0;
+  cudaError_t e = o(smem_limit, smem, &k);
+  if (e != cudaSuccess) return fail_cuda(e, "occupancy query");
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_occupancy[std::make_tuple(dev, v_dtype, gc, smem)] = k;
+  *n = k;
+  return GQA_AV_OK;
+}
+
+// ------------------------------------------------------------------- plan
+struct Plan {
+  int mode, heads, gc, nc, dt, ndt, ct, row_par, R, stages, nsplit, rows_per_split;
+  int hgroups, tiles, ap, avec, smem, occ;
+  uint32_t v_stage_bytes, a_off, bar_off;
+  size_t ws_bytes;  // partials only
+};
+
+int check_shape(int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode) {
+  if (B <= 0 || Cmax <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0)
+    return fail(GQA_AV_ERR_INVALID, "sizes must be positive (B=%d Cmax=%d Hq=%d Hkv=%d D=%d)", B,
+                Cmax, Hq, Hkv, D);
+  if (Hq % Hkv != 0)
+    return fail(GQA_AV_ERR_INVALID, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+  if (v_dtype != GQA_AV_BF16 && v_dtype != GQA_AV_FP16)
+    return fail(GQA_AV_ERR_INVALID, "unknown v_dtype %d", v_dtype);
+  if (mode != GQA_AV_MODE_AUTO && mode != GQA_AV_MODE_PER_HEAD && mode != GQA_AV_MODE_GQA)
+    return fail(GQA_AV_ERR_INVALID, "unknown mode %d", mode);
+  if (D % 8 != 0) return fail(GQA_AV_ERR_UNSUPPORTED, "D=%d is not a multiple of 8", D);
+  return GQA_AV_OK;
+}
+
+// Shared memory of a plan: [V ring | reduction buffer] [attn ring] [mbarriers] [flag].
+void layout(Plan* p) {
+  p->v_stage_bytes = static_cast<uint32_t>(p->R) * p->dt * 2;
+  const size_t vring = static_cast<size_t>(p->stages) * p->v_stage_bytes;
+  const size_t red = static_cast<size_t>(p->row_par) * p->heads * p->dt * 4;
+  p->a_off = static_cast<uint32_t>(align_up(std::max(vring, red), 128));
+  const size_t aring = static_cast<size_t>(p->stages) * p->R * p->ap * 4;
+  p->bar_off = static_cast<uint32_t>(align_up(p->a_off + aring, 16));
+  p->smem = static_cast<int>(p->bar_off + 2 * kMaxStages * 8 + 16);
+}
+
+int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode,
+              const gqa_av_tuning* t, Plan* p) {
+  int rc = check_shape(B, Cmax, Hq, Hkv, D, v_dtype, mode);
+  if (rc) return rc;
+  DeviceInfo di;
+  if ((rc = device_info(dev, &di))) return rc;
+
+  const int G = Hq / Hkv;
+  p->mode = mode == GQA_AV_MODE_AUTO ? (G > 1 ? GQA_AV_MODE_GQA : GQA_AV_MODE_PER_HEAD) : mode;
+  p->heads = p->mode == GQA_AV_MODE_GQA ? G : 1;
+  p->hgroups = Hq / p->heads;
+  p->gc = 1;
+  for (int c : kHeadChunks)
+    if (p->heads % c == 0) { p->gc = c; break; }
+  p->nc = p->heads / p->gc;
+
+  // Output columns per CTA: a multiple of 8 dividing D, at most 256 (one TMA box).
+  const int want_dt = (t && t->dtile > 0) ? t->dtile : 128;
+  if (t && t->dtile > 0 && (t->dtile % 8 || D % t->dtile || t->dtile > 256))
+    return fail(GQA_AV_ERR_INVALID, "dtile=%d must be a multiple of 8 dividing D=%d, <= 256",
+                t->dtile, D);
+  p->dt = 0;
+  for (int dt = std::min(want_dt, std::min(D, 256)); dt >= 8; dt -= 8)
+    if (D % dt == 0 && (dt / 8) * p->nc <= kConsumerThreads) { p->dt = dt; break; }
+  if (!p->dt)
+    return fail(GQA_AV_ERR_UNSUPPORTED, "no column tile fits G=%d heads per CTA", p->heads);
+  p->ndt = D / p->dt;
+  p->ct = p->dt / 8;
+  p->row_par = kConsumerThreads / (p->ct * p->nc);
+
+  // Rows per stage: about 8 KiB of V per stage, a multiple of 8 rows.
+  if (t && t->rows_per_stage > 0) {
+    if (t->rows_per_stage % 8 || t->rows_per_stage > 256)
+      return fail(GQA_AV_ERR_INVALID, "rows_per_stage=%d must be a multiple of 8, <= 256",
+                  t->rows_per_stage);
+    p->R = t->rows_per_stage;
+  } else {
+    p->R = std::max(8, std::min(256, 8192 / (2 * p->dt)));
+    p->R = std::min(p->R, static_cast<int>(align_up(Cmax, 8)));
+    p->R = std::max(8, p->R / 8 * 8);
+  }
+  if (t && t->stages > 0) {
+    if (t->stages < 2 || t->stages > kMaxStages)
+      return fail(GQA_AV_ERR_INVALID, "stages=%d must be in [2, %d]", t->stages, kMaxStages);
+    p->stages = t->stages;
+  } else {
+    p->stages = 6;
+  }
+  p->ap = static_cast<int>(align_up(p->heads, 4));
+  layout(p);
+  while (p->smem > di.smem_optin && p->stages > 2 && !(t && t->stages > 0)) {
+    --p->stages;
+    layout(p);
+  }
+  if (p->smem > di.smem_optin)
+    return fail(GQA_AV_ERR_UNSUPPORTED, "plan needs %d B of shared memory (limit %d)", p->smem,
+                di.smem_optin);
+
+  p->avec = 1;
+  if (Hq % 4 == 0 && p->heads % 4 == 0) p->avec = 4;
+  else if (Hq % 2 == 0 && p->heads % 2 == 0) p->avec = 2;
+
+  if ((rc = ctas_per_sm(dev, di.smem_optin, v_dtype, p->gc, p->smem, &p->occ))) return rc;
+  if (p->occ < 1) return fail(GQA_AV_ERR_UNSUPPORTED, "kernel does not fit on an SM");
+
+  // Context splits: enough CTAs to fill every SM, with at least 4 stages of rows each.
+  p->tiles = p->hgroups * B * p->ndt;
+  const int max_split = std::max(1, (Cmax + 4 * p->R - 1) / (4 * p->R));
+  int nsplit;
+  if (t && t->nsplit > 0) {
+    nsplit = std::min(t->nsplit, (Cmax + p->R - 1) / p->R);
+  } else {
+    const long long wave = static_cast<long long>(di.sms) * p->occ;
+    const double v_bytes = static_cast<double>(B) * Cmax * (p->heads == 1 ? Hq : Hkv) * D * 2;
+    const int waves = v_bytes > 256e6 ? 4 : 1;
+    nsplit = static_cast<int>(std::min<long long>(
+        max_split, std::max<long long>(1, (wave * waves + p->tiles - 1) / p->tiles)));
+  }
+  if (p->tiles > kMaxTicketTiles) nsplit = 1;
+  nsplit = std::max(1, nsplit);
+  p->rows_per_split = static_cast<int>(align_up((Cmax + nsplit - 1) / nsplit, p->R));
+  p->nsplit = (Cmax + p->rows_per_split - 1) / p->rows_per_split;
+  if (static_cast<long long>(p->tiles) * p->nsplit > 0x7fffffffLL)
+    return fail(GQA_AV_ERR_UNSUPPORTED, "grid too large");
+  p->ws_bytes = p->nsplit > 1
+                    ? static_cast<size_t>(p->tiles) * p->nsplit * p->heads * p->dt * sizeof(float)
+                    : 0;
+  return GQA_AV_OK;
+}
+
+// -------------------------------------------------------------- workspace
+struct Workspace {
+  void* base = nullptr;
+  size_t bytes = 0;
+  bool user = false;
+};
+std::map<int, Workspace> g_ws;
+
+// Returns the workspace of `dev` with at least `need` bytes; grows outside capture.
+int workspace(int dev, size_t need, cudaStream_t stream, Workspace* out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  Workspace& w = g_ws[dev];
+  if (w.base && w.bytes >= need) {
+    *out = w;
+    return GQA_AV_OK;
+  }
+  if (w.user)
+    return fail(GQA_AV_ERR_NOMEM, "caller workspace has %zu B, call needs %zu B", w.bytes, need);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaStreamIsCapturing");
+  if (cs != cudaStreamCaptureStatusNone)
+    return fail(GQA_AV_ERR_NOMEM,
+                "workspace must grow to %zu B but the stream is capturing; make one call with "
+                "the largest shape before capture",
+                need);
+  const size_t bytes = std::max(need, w.bytes + w.bytes / 2);
+  if (w.base) {
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
+    cudaFree(w.base);
+    w.base = nullptr;
+    w.bytes = 0;
+  }
+  void* p = nullptr;
+  e = cudaMalloc(&p, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(GQA_AV_ERR_NOMEM, "cudaMalloc(%zu) failed: %s", bytes, cudaGetErrorString(e));
+  }
+  e = cudaMemset(p, 0, kHeaderBytes);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaFree(p);
+    return fail_cuda(e, "zeroing the workspace header");
+  }
+  w.base = p;
+  w.bytes = bytes;
+  *out = w;
+  return GQA_AV_OK;
+}
+
+// ------------------------------------------------------------ tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int encode_fn(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e =
+        cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !f)
+      return fail(GQA_AV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  *fn = g_encode;
+  return GQA_AV_OK;
+}
+
+// V viewed as 4-D {D, Hkv, Cmax, B} (innermost first); box {dt, 1, R, 1}.
+int encode_v_map(CUtensorMap* m, const void* v, int B, int Cmax, int Hkv, int D, int dt, int R) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  int rc = encode_fn(&enc);
+  if (rc) return rc;
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)Cmax, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2,
+                                 (cuuint64_t)Cmax * Hkv * D * 2};
+  const cuuint32_t box[4] = {(cuuint32_t)dt, 1, (cuuint32_t)R, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(v), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(GQA_AV_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return GQA_AV_OK;
+}
+
+int current_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  return e == cudaSuccess ? GQA_AV_OK : fail_cuda(e, "cudaGetDevice");
+}
+
+int run(const float* attn, const void* v, const int32_t* seq_lens, float* out, int B, int Cmax,
+        int Hq, int Hkv, int D, int v_dtype, int mode, const gqa_av_tuning* tuning,
+        cudaStream_t stream) {
+  g_last_error.clear();
+  int rc = check_shape(B, Cmax, Hq, Hkv, D, v_dtype, mode);
+  if (rc) return rc;
+  if (!attn || !v || !out) return fail(GQA_AV_ERR_INVALID, "attn, v_cache and out must be non-NULL");
+  if ((reinterpret_cast<uintptr_t>(attn) | reinterpret_cast<uintptr_t>(v) |
+       reinterpret_cast<uintptr_t>(out)) & 15)
+    return fail(GQA_AV_ERR_UNSUPPORTED, "attn, v_cache and out must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(seq_lens) & 3)
+    return fail(GQA_AV_ERR_INVALID, "seq_lens must be 4-byte aligned");
+  int dev;
+  if ((rc = current_device(&dev))) return rc;
+  Plan pl;
+  if ((rc = make_plan(dev, B, Cmax, Hq, Hkv, D, v_dtype, mode, tuning, &pl))) return rc;
+  Workspace ws;
+  if ((rc = workspace(dev, kHeaderBytes + pl.ws_bytes, stream, &ws))) return rc;
+
+  Params p;
+  memset(&p, 0, sizeof p);
+  if ((rc = encode_v_map(&p.v_map, v, B, Cmax, Hkv, D, pl.dt, pl.R))) return rc;
+  p.attn = attn;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.status = static_cast<unsigned*>(ws.base);
+  p.tickets = reinterpret_cast<unsigned*>(static_cast<char*>(ws.base) + kStatusBytes);
+  p.ws = reinterpret_cast<float*>(static_cast<char*>(ws.base) + kHeaderBytes);
+  p.B = B; p.Cmax = Cmax; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.G = Hq / Hkv;
+  p.heads = pl.heads; p.hgroups = pl.hgroups; p.dt = pl.dt; p.ndt = pl.ndt; p.ct = pl.ct;
+  p.nc = pl.nc; p.row_par = pl.row_par; p.R = pl.R; p.stages = pl.stages;
+  p.rows_per_split = pl.rows_per_split; p.nsplit = pl.nsplit; p.ap = pl.ap; p.avec = pl.avec;
+  p.v_stage_bytes = pl.v_stage_bytes; p.a_off = pl.a_off; p.bar_off = pl.bar_off;
+  p.timeout_ns = kWaitTimeoutNs;
+  if (pl.avec > 1 && (reinterpret_cast<uintptr_t>(attn) & (4 * pl.avec - 1))) p.avec = 1;
+
+  LaunchFn l;
+  OccFn o;
+  if (!pick_kernel(v_dtype, pl.gc, &l, &o)) return fail(GQA_AV_ERR_UNSUPPORTED, "no kernel");
+  cudaError_t e = l(p, pl.tiles * pl.nsplit, pl.smem, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
+  return GQA_AV_OK;
+}
+
+}  // namespace
+}  // namespace gqa_av
+
+using namespace gqa_av;
+
+extern "C" {
+
+int gqa_av_decode(const float* attn, const void* v_cache, const int32_t* seq_lens, float* out,
+                  int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode, void* stream) {
+  return run(attn, v_cache, seq_lens, out, B, Cmax, Hq, Hkv, D, v_dtype, mode, nullptr,
+             static_cast<cudaStream_t>(stream));
+}
+
+int gqa_av_decode_per_head(const float* attn, const void* v_cache, const int32_t* seq_lens,
+                           float* out, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype,
+                           void* stream) {
+  return run(attn, v_cache, seq_lens, out, B, Cmax, Hq, Hkv, D, v_dtype, GQA_AV_MODE_PER_HEAD,
+             nullptr, static_cast<cudaStream_t>(stream));
+}
+
+int gqa_av_decode_tuned(const float* attn, const void* v_cache, const int32_t* seq_lens,
+                        float* out, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode,
+                        const gqa_av_tuning* tuning, void* stream) {
+  return run(attn, v_cache, seq_lens, out, B, Cmax, Hq, Hkv, D, v_dtype, mode, tuning,
+             static_cast<cudaStream_t>(stream));
+}
+
+int gqa_av_plan(int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode,
+                const gqa_av_tuning* tuning, gqa_av_plan_info* info) {
+  g_last_error.clear();
+  if (!info) return fail(GQA_AV_ERR_INVALID, "info must be non-NULL");
+  int dev, rc;
+  if ((rc = current_device(&dev))) return rc;
+  Plan p;
+  if ((rc = make_plan(dev, B, Cmax, Hq, Hkv, D, v_dtype, mode, tuning, &p))) return rc;
+  info->mode = p.mode;
+  info->heads_per_cta = p.heads;
+  info->head_chunk = p.gc;
+  info->dtile = p.dt;
+  info->rows_per_stage = p.R;
+  info->stages = p.stages;
+  info->nsplit = p.nsplit;
+  info->rows_per_split = p.rows_per_split;
+  info->tiles = p.tiles;
+  info->ctas = p.tiles * p.nsplit;
+  info->threads_per_cta = kThreads;
+  info->smem_bytes = p.smem;
+  info->ctas_per_sm = p.occ;
+  info->workspace_bytes = kHeaderBytes + p.ws_bytes;
+  return GQA_AV_OK;
+}
+
+size_t gqa_av_workspace_bytes(int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode) {
+  gqa_av_plan_info info;
+  if (gqa_av_plan(B, Cmax, Hq, Hkv, D, v_dtype, mode, nullptr, &info) != GQA_AV_OK) return 0;
+  return info.workspace_bytes;
+}
+
+int gqa_av_set_workspace(void* ptr, size_t bytes) {
+  g_last_error.clear();
+  int dev, rc;
+  if ((rc = current_device(&dev))) return rc;
+  if (ptr && bytes < kHeaderBytes)
+    return fail(GQA_AV_ERR_INVALID, "workspace must hold at least %zu B", kHeaderBytes);
+  if (ptr && (reinterpret_cast<uintptr_t>(ptr) & 255))
+    return fail(GQA_AV_ERR_INVALID, "workspace must be 256-byte aligned");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
+  std::lock_guard<std::mutex> lk(g_mu);
+  Workspace& w = g_ws[dev];
+  if (w.base && !w.user) cudaFree(w.base);
+  w = Workspace();
+  if (ptr) {
+    e = cudaMemset(ptr, 0, kHeaderBytes);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda(e, "zeroing the workspace header");
+    w.base = ptr;
+    w.bytes = bytes;
+    w.user = true;
+  }
+  return GQA_AV_OK;
+}
+
+int gqa_av_device_status(void* stream, int clear) {
+  g_last_error.clear();
+  int dev, rc;
+  if ((rc = current_device(&dev))) return rc;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
+  Workspace w;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    w = g_ws[dev];
+  }
+  if (!w.base) return GQA_AV_OK;
+  unsigned word = 0;
+  e = cudaMemcpy(&word, w.base, sizeof word, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda(e, "reading the device status word");
+  if (clear && word) {
+    e = cudaMemset(w.base, 0, kHeaderBytes);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda(e, "clearing the device status word");
+  }
+  if (word)
+    return fail(GQA_AV_ERR_DEVICE_TIMEOUT, "a bounded wait ran out on the device (status 0x%x)", word);
+  return GQA_AV_OK;
+}
+
+const char* gqa_av_status_string(int status) {
+  switch (status) {
+    case GQA_AV_OK: return "GQA_AV_OK";
+    case GQA_AV_ERR_INVALID: return "GQA_AV_ERR_INVALID";
+    case GQA_AV_ERR_UNSUPPORTED: return "GQA_AV_ERR_UNSUPPORTED";
+    case GQA_AV_ERR_CUDA: return "GQA_AV_ERR_CUDA";
+    case GQA_AV_ERR_NOMEM: return "GQA_AV_ERR_NOMEM";
+    case GQA_AV_ERR_DEVICE_TIMEOUT: return "GQA_AV_ERR_DEVICE_TIMEOUT";
+    default: return "GQA_AV_ERR_UNKNOWN";
+  }
+}
+
+const char* gqa_av_last_error(void) { return g_last_error.c_str(); }
+
+int gqa_av_version(void) { return 1; }
+
+}  // extern "C"

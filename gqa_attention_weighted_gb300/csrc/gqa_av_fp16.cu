@@ -1,0 +1,5 @@
+// fp16 V-cache instantiations of the AV kernel.
+#include "gqa_av_instances.cuh"
+namespace gqa_av {
+GQA_AV_INSTANTIATE_ALL(Fp16Tag)
+}  // namespace gqa_av

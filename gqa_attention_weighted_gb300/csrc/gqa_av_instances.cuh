@@ -1,0 +1,42 @@
+// Explicit instantiations of the AV kernel for one V element type.
+// Included by gqa_av_bf16.cu / gqa_av_fp16.cu with GQA_AV_TAG defined, so the
+// two element types compile as separate translation units in parallel.
+#pragma once
+#include "gqa_av_kernel.cuh"
+
+namespace gqa_av {
+
+template <typename Tag, int GC>
+cudaError_t launch(const Params& p, int grid, int smem_bytes, cudaStream_t stream) {
+  gqa_av_kernel<Tag, GC><<<grid, kThreads, smem_bytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// Raises the kernel's dynamic shared-memory limit to `smem_limit` (the device's
+// opt-in maximum, so every plan can launch) and reports CTAs per SM at `smem_bytes`.
+template <typename Tag, int GC>
+cudaError_t occupancy(int smem_limit, int smem_bytes, int* ctas_per_sm) {
+  cudaError_t e = cudaFuncSetAttribute(gqa_av_kernel<Tag, GC>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_limit);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, gqa_av_kernel<Tag, GC>,
+                                                       kThreads, smem_bytes);
+}
+
+#define GQA_AV_INSTANTIATE(TAG, GC)                                                      \
+  template cudaError_t launch<TAG, GC>(const Params&, int, int, cudaStream_t);           \
+  template cudaError_t occupancy<TAG, GC>(int, int, int*);
+
+#define GQA_AV_INSTANTIATE_ALL(TAG) \
+  GQA_AV_INSTANTIATE(TAG, 1)        \
+  GQA_AV_INSTANTIATE(TAG, 2)        \
+  GQA_AV_INSTANTIATE(TAG, 3)        \
+  GQA_AV_INSTANTIATE(TAG, 4)        \
+  GQA_AV_INSTANTIATE(TAG, 5)        \
+  GQA_AV_INSTANTIATE(TAG, 6)        \
+  GQA_AV_INSTANTIATE(TAG, 7)        \
+  GQA_AV_INSTANTIATE(TAG, 8)        \
+  GQA_AV_INSTANTIATE(TAG, 12)       \
+  GQA_AV_INSTANTIATE(TAG, 16)
+
+}  // namespace gqa_av

@@ -1,0 +1,157 @@
+/*
+ * gqa_av.h -- C ABI of the GB300 (sm_103a) grouped-query-attention AV decode
+ * reduction.
+ *
+ * Operation (page "pytorch/executorch pull 21063", summary paragraph): in
+ * grouped-query attention Hq = G * Hkv query heads share each KV head, and the
+ * decode-step output of query head q_h is
+ *
+ *     out[b, q_h, d] = sum_{c < L_b} attn[b, c, q_h] * V[b, c, kv_h, d],
+ *     kv_h = q_h / G,   G = Hq / Hkv,   L_b = clamp(seq_lens[b], 0, Cmax).
+ *
+ * The GQA-reuse variant (same page, paragraph on the GQA-reuse AV variant)
+ * reads each V-cache row once and reuses it for all G query heads of its
+ * group; the per-head variant reads it once per query head (G times). Both
+ * compute the same sums. The mode switch follows the page's test-only override
+ * knob (bullet on `gqa_override`): -1 auto-select, 0 force per-head,
+ * 1 force GQA-reuse, so both kernels can be measured on one shape.
+ *
+ * Layouts (all contiguous, row-major, caller-owned DEVICE memory):
+ *     attn      [B, Cmax, Hq]       float32
+ *     v_cache   [B, Cmax, Hkv, D]   bf16 (GQA_AV_BF16) or fp16 (GQA_AV_FP16)
+ *     seq_lens  [B]                 int32, or NULL meaning every L_b = Cmax
+ *     out       [B, Hq, D]          float32, fully overwritten (never accumulated)
+ * Entries at c >= L_b are never used. Values outside [0, Cmax] in seq_lens
+ * are clamped to that range on the device.
+ *
+ * Numerics: products and sums in fp32 (bf16/fp16 -> fp32 widening is exact),
+ * context splits combined in a fixed order, so repeated calls with the same
+ * shape give bitwise-identical out.
+ *
+ * Execution: every call is asynchronous on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream) and performs no host synchronisation. Calls
+ * share one per-device workspace, so calls that may overlap on the GPU (on
+ * different streams) must not be issued concurrently; calls on one stream are
+ * always safe. The workspace grows on demand with cudaMalloc; during stream
+ * capture it cannot grow, so make one call with the largest shape first (or
+ * supply a workspace with gqa_av_set_workspace).
+ *
+ * Errors: every entry point returns a status code. On any error nothing is
+ * launched and gqa_av_last_error() holds a message for the calling thread.
+ */
+#ifndef GQA_AV_H
+#define GQA_AV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define GQA_AV_OK                  0
+#define GQA_AV_ERR_INVALID         1 /* NULL pointer, size <= 0, Hq % Hkv != 0, bad mode or dtype */
+#define GQA_AV_ERR_UNSUPPORTED     2 /* D % 8 != 0, pointer not 16-byte aligned, shape too large */
+#define GQA_AV_ERR_CUDA            3 /* a CUDA runtime/driver call or a launch failed */
+#define GQA_AV_ERR_NOMEM           4 /* workspace could not be allocated (or not during capture) */
+#define GQA_AV_ERR_DEVICE_TIMEOUT  5 /* a bounded wait inside a kernel ran out (device status word) */
+
+/* V-cache element types. */
+#define GQA_AV_BF16 0
+#define GQA_AV_FP16 1
+
+/* Modes (the page's gqa_override knob). */
+#define GQA_AV_MODE_AUTO     (-1) /* GQA-reuse when G > 1, per-head when G == 1 (MHA) */
+#define GQA_AV_MODE_PER_HEAD   0  /* one CTA per (b, q_h, d-tile, split): V read G times */
+#define GQA_AV_MODE_GQA        1  /* one CTA per (b, kv_h, d-tile, split): V read once */
+
+/*
+ * The reduction. Arguments as in the layouts above; B, Cmax, Hq, Hkv, D > 0,
+ * Hq % Hkv == 0, D % 8 == 0; attn, v_cache and out 16-byte aligned.
+ * Forcing a mode on a shape it cannot run is an error (never a silent
+ * fallback): with Hq % Hkv != 0 every mode returns GQA_AV_ERR_INVALID.
+ */
+int gqa_av_decode(const float *attn, const void *v_cache, const int32_t *seq_lens,
+                  float *out, int B, int Cmax, int Hq, int Hkv, int D,
+                  int v_dtype, int mode, void *stream);
+
+/* Per-head baseline: identical to gqa_av_decode(..., GQA_AV_MODE_PER_HEAD, stream). */
+int gqa_av_decode_per_head(const float *attn, const void *v_cache, const int32_t *seq_lens,
+                           float *out, int B, int Cmax, int Hq, int Hkv, int D,
+                           int v_dtype, void *stream);
+
+/*
+ * Launch-shape overrides for sweeps and tests. A field <= 0 keeps the
+ * library's choice. nsplit: context splits per tile; dtile: output columns
+ * per CTA (a multiple of 8 dividing D, <= 256); rows_per_stage: V rows per
+ * pipeline stage (8..256); stages: pipeline depth (2..8). Results stay within
+ * the stated tolerance for every choice, and are bitwise reproducible for a
+ * fixed choice.
+ */
+typedef struct gqa_av_tuning {
+    int nsplit;
+    int dtile;
+    int rows_per_stage;
+    int stages;
+} gqa_av_tuning;
+
+int gqa_av_decode_tuned(const float *attn, const void *v_cache, const int32_t *seq_lens,
+                        float *out, int B, int Cmax, int Hq, int Hkv, int D,
+                        int v_dtype, int mode, const gqa_av_tuning *tuning, void *stream);
+
+/* The launch shape a call with these arguments would use (no launch, no allocation). */
+typedef struct gqa_av_plan_info {
+    int mode;            /* resolved mode: 0 per-head, 1 GQA-reuse */
+    int heads_per_cta;   /* query heads each CTA accumulates (G or 1) */
+    int head_chunk;      /* query heads per thread (a divisor of heads_per_cta) */
+    int dtile;           /* output columns per CTA */
+    int rows_per_stage;
+    int stages;
+    int nsplit;          /* context splits per tile */
+    int rows_per_split;
+    int tiles;           /* (head groups) x B x (D / dtile) */
+    int ctas;            /* tiles x nsplit */
+    int threads_per_cta;
+    int smem_bytes;
+    int ctas_per_sm;     /* occupancy of this kernel at this shared-memory size */
+    size_t workspace_bytes;
+} gqa_av_plan_info;
+
+int gqa_av_plan(int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode,
+                const gqa_av_tuning *tuning, gqa_av_plan_info *info);
+
+/* Device workspace bytes a call with these arguments needs (0 when none). */
+size_t gqa_av_workspace_bytes(int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode);
+
+/*
+ * Hand the library a caller-owned device workspace for the current device
+ * (at least gqa_av_workspace_bytes of the largest call, plus 4 KiB). The
+ * library zeroes it here (synchronously) and never frees it. ptr == NULL
+ * returns to a library-owned workspace. The caller keeps the memory alive
+ * until it calls gqa_av_set_workspace(NULL, 0) or the process ends.
+ */
+int gqa_av_set_workspace(void *ptr, size_t bytes);
+
+/*
+ * Synchronise `stream`, then read the current device's status word, which
+ * kernels set when a bounded wait runs out. Returns GQA_AV_OK or
+ * GQA_AV_ERR_DEVICE_TIMEOUT; with clear != 0 the word and the workspace's
+ * split counters are reset so later calls start clean.
+ */
+int gqa_av_device_status(void *stream, int clear);
+
+/* Name of a status code; never NULL. */
+const char *gqa_av_status_string(int status);
+
+/* Message of the calling thread's last error ("" if none). */
+const char *gqa_av_last_error(void);
+
+/* Library version, for the Python binding's load check. */
+int gqa_av_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_AV_H */

@@ -1,0 +1,73 @@
+"""The C-ABI library loads and exports every entry point its header declares;
+host-side argument checks reject bad calls before any CUDA call (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gqa_av.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(gqa_av_\w+)\s*\(", text, re.M)))
+
+
+@pytest.fixture(scope="module")
+def native():
+    from gqa_attention_weighted_gb300 import build
+    build.build()
+    from gqa_attention_weighted_gb300 import _native
+    return _native
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for f in ("gqa_av_decode", "gqa_av_decode_per_head", "gqa_av_status_string",
+              "gqa_av_workspace_bytes"):
+        assert f in names
+
+
+def test_library_exports_every_declared_symbol(native):
+    lib = ctypes.CDLL(native.LIBRARY)
+    missing = [f for f in declared_functions() if not hasattr(lib, f)]
+    assert not missing, f"declared but not exported: {missing}"
+
+
+def test_status_strings(native):
+    assert native.gqa_av_status_string(0) == "GQA_AV_OK"
+    assert native.gqa_av_status_string(1) == "GQA_AV_ERR_INVALID"
+    assert native.gqa_av_status_string(5) == "GQA_AV_ERR_DEVICE_TIMEOUT"
+    assert native.gqa_av_status_string(99) == "GQA_AV_ERR_UNKNOWN"
+    assert native.lib.gqa_av_version() == 1
+
+
+# (attn, v, out) as fake non-NULL 16-byte-aligned addresses: every case below
+# is rejected by the host checks before any pointer is touched or CUDA called.
+FAKE = 1 << 20
+
+
+@pytest.mark.parametrize("args,status", [
+    ((FAKE, FAKE, None, FAKE, 1, 8, 6, 4, 8, 0, -1), 1),   # Hq % Hkv != 0
+    ((FAKE, FAKE, None, FAKE, 0, 8, 4, 4, 8, 0, -1), 1),   # B == 0
+    ((FAKE, FAKE, None, FAKE, 1, -3, 4, 4, 8, 0, -1), 1),  # Cmax < 0
+    ((FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 8, 2, -1), 1),   # unknown dtype
+    ((FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 8, 0, 3), 1),    # unknown mode
+    ((None, FAKE, None, FAKE, 1, 8, 4, 4, 8, 0, -1), 1),   # NULL attn
+    ((FAKE, FAKE, None, None, 1, 8, 4, 4, 8, 0, 1), 1),    # NULL out
+    ((FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 12, 0, 1), 2),   # D % 8 != 0
+    ((FAKE + 4, FAKE, None, FAKE, 1, 8, 4, 4, 8, 0, 0), 2),  # misaligned attn
+    ((FAKE, FAKE, FAKE + 2, FAKE, 1, 8, 4, 4, 8, 0, 0), 1),  # misaligned seq_lens
+])
+def test_host_checks_reject_before_launch(native, args, status):
+    rc = native.lib.gqa_av_decode(*args, None)
+    assert rc == status, native.gqa_av_last_error()
+    assert native.gqa_av_last_error() != ""
+
+
+def test_per_head_entry_checks(native):
+    rc = native.lib.gqa_av_decode_per_head(FAKE, FAKE, None, FAKE, 1, 8, 6, 4, 8, 0, None)
+    assert rc == 1 and "multiple" in native.gqa_av_last_error()

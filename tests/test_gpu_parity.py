@@ -1,0 +1,232 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Gate (per case): max|gpu - oracle| <= 1e-4 * max(1, max|oracle|), with fp32
+out compared to fp64 oracle values on identical seeded inputs. Padding rows
+(c >= L_b) hold NaN, so a kernel that uses an out-of-range row fails.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import bits, decoded, load_golden, rand_case
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def gq():
+    from gqa_attention_weighted_gb300 import build
+    build.build()
+    import gqa_attention_weighted_gb300 as pkg
+    return pkg
+
+
+def run_gpu(gq, attn, v, seq_lens, mode=-1, tuning=None, out_fill=float("nan")):
+    dev = torch.device("cuda")
+    a, vv = attn.to(dev), v.to(dev)
+    sl = None if seq_lens is None else seq_lens.to(dev)
+    B, C, Hq = attn.shape
+    D = v.shape[3]
+    out = torch.full((B, Hq, D), out_fill, dtype=torch.float32, device=dev)
+    if tuning is None:
+        gq.gqa_av_decode(a, vv, sl, out, mode=mode)
+    else:
+        gq.gqa_av_decode_tuned(a, vv, sl, out, mode=mode, tuning=tuning)
+    gq.gqa_av_device_status()
+    return out.cpu().double().numpy()
+
+
+def run_oracle(attn, v, seq_lens, vd):
+    return oracle.gqa_av(attn.numpy(), bits(v), vd,
+                         None if seq_lens is None else seq_lens.numpy(),
+                         nthreads=oracle.host_cores())
+
+
+def assert_close(got, ref, what=""):
+    tol = TOL * max(1.0, float(np.abs(ref).max()) if ref.size else 1.0)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = float(np.abs(got - ref).max()) if ref.size else 0.0
+    assert err <= tol, f"{what}: max|gpu-oracle| = {err:.3e} > {tol:.3e}"
+    return err
+
+
+# ---------------------------------------------------------------- exactness
+@pytest.mark.parametrize("vd", ["bf16", "fp16"])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_hand_worked_fixture_exact(gq, vd, mode):
+    g = load_golden("hand_worked_b2_c3_hq4_hkv2_d2.json", vd)
+    # D=2 is below the kernel's D % 8 granularity: embed the fixture in D=8
+    # columns (the extra columns are zero) and compare the first two exactly.
+    v = torch.zeros((2, 3, 2, 8), dtype=g["v"].dtype)
+    v[..., :2] = g["v"]
+    out = run_gpu(gq, g["attn"], v, g["seq_lens"], mode)
+    assert np.array_equal(out[..., :2], g["out"]), out[..., :2]
+    assert np.array_equal(out[..., 2:], np.zeros((2, 4, 6)))
+
+
+@pytest.mark.parametrize("vd", ["bf16", "fp16"])
+def test_one_hot_returns_the_row_exactly(gq, vd):
+    rng = np.random.default_rng(21)
+    B, C, Hq, Hkv, D = 2, 700, 12, 3, 128
+    _, v, sl = rand_case(rng, B, C, Hq, Hkv, D, vd, [700, 333])
+    vv = decoded(v)
+    for c0 in (0, 255, 332):
+        a = torch.zeros((B, C, Hq), dtype=torch.float32)
+        a[:, c0, :] = 1.0
+        for mode in (0, 1):
+            out = run_gpu(gq, a, v, sl, mode)
+            for b in range(B):
+                for q in range(Hq):
+                    assert np.array_equal(out[b, q], vv[b, c0, q // 4]), (c0, mode, b, q)
+
+
+# ------------------------------------------------------------ shape sweep
+SWEEP = []
+for G in (1, 2, 3, 4, 5, 7, 8, 12, 16, 32):
+    for D in (64, 128, 256):
+        SWEEP.append((G, D))
+SWEEP += [(4, 8), (6, 24), (3, 80), (9, 96), (10, 128), (14, 64), (20, 64), (11, 40)]
+
+
+@pytest.mark.parametrize("G,D", SWEEP, ids=[f"G{g}-D{d}" for g, d in SWEEP])
+def test_shape_sweep(gq, G, D):
+    rng = np.random.default_rng(1000 * G + D)
+    Hkv = 2 if G <= 16 else 1
+    B, C = 3, 517
+    lens = [517, 1, 200]
+    for vd in ("bf16", "fp16"):
+        attn, v, sl = rand_case(rng, B, C, G * Hkv, Hkv, D, vd, lens)
+        ref = run_oracle(attn, v, sl, vd)
+        for mode in (0, 1):
+            assert_close(run_gpu(gq, attn, v, sl, mode), ref, f"G={G} D={D} {vd} mode={mode}")
+
+
+@pytest.mark.parametrize("L", [0, 1, 2, 7, 8, 9, 31, 32, 33, 63, 64, 65, 255, 256, 257, 1000])
+def test_lengths_and_ragged_tails(gq, L):
+    rng = np.random.default_rng(L + 7)
+    B, C, Hq, Hkv, D = 2, 1024, 8, 2, 64
+    attn, v, sl = rand_case(rng, B, C, Hq, Hkv, D, "bf16", [L, max(0, 1024 - L)])
+    ref = run_oracle(attn, v, sl, "bf16")
+    for mode in (0, 1):
+        out = run_gpu(gq, attn, v, sl, mode)
+        assert_close(out, ref, f"L={L} mode={mode}")
+        if L == 0:
+            assert np.array_equal(out[0], np.zeros_like(out[0]))
+
+
+def test_lengths_are_clamped_and_null_means_full(gq):
+    rng = np.random.default_rng(5)
+    B, C, Hq, Hkv, D = 3, 300, 8, 2, 64
+    attn, v, _ = rand_case(rng, B, C, Hq, Hkv, D, "bf16", [300, 300, 300], pad_nan=False)
+    full = run_oracle(attn, v, None, "bf16")
+    assert_close(run_gpu(gq, attn, v, None), full, "seq_lens=NULL")
+    sl = torch.tensor([300, 301, 1 << 30], dtype=torch.int32)
+    assert_close(run_gpu(gq, attn, v, sl), full, "lengths above Cmax")
+    neg = run_gpu(gq, attn, v, torch.tensor([-5, 0, -(1 << 30)], dtype=torch.int32))
+    assert np.array_equal(neg, np.zeros_like(neg))
+
+
+# ------------------------------------------------------ launch-shape sweep
+TUNINGS = [dict(nsplit=1), dict(nsplit=2), dict(nsplit=7), dict(nsplit=1000),
+           dict(dtile=64), dict(dtile=32, rows_per_stage=8), dict(stages=2),
+           dict(stages=8, rows_per_stage=64), dict(rows_per_stage=256, stages=3),
+           dict(nsplit=5, dtile=8, rows_per_stage=16, stages=4)]
+
+
+@pytest.mark.parametrize("tuning", TUNINGS, ids=[str(t) for t in TUNINGS])
+def test_tunings_agree_and_are_deterministic(gq, tuning):
+    rng = np.random.default_rng(99)
+    B, C, Hq, Hkv, D = 2, 1500, 24, 8, 128
+    for vd in ("bf16", "fp16"):
+        attn, v, sl = rand_case(rng, B, C, Hq, Hkv, D, vd, [1500, 777])
+        ref = run_oracle(attn, v, sl, vd)
+        for mode in (0, 1):
+            a = run_gpu(gq, attn, v, sl, mode, tuning)
+            b = run_gpu(gq, attn, v, sl, mode, tuning)
+            assert_close(a, ref, f"{tuning} {vd} mode={mode}")
+            assert np.array_equal(a, b), "repeated call differs bitwise"
+
+
+def test_modes_agree_and_identical_weights_give_identical_heads(gq):
+    rng = np.random.default_rng(3)
+    B, C, Hq, Hkv, D = 2, 2048, 16, 2, 128
+    attn, v, sl = rand_case(rng, B, C, Hq, Hkv, D, "bf16", [2048, 1111])
+    G = Hq // Hkv
+    for k in range(Hkv):
+        for g in range(1, G):
+            attn[:, :, k * G + g] = attn[:, :, k * G]
+    gqa = run_gpu(gq, attn, v, sl, 1)
+    per = run_gpu(gq, attn, v, sl, 0)
+    assert_close(gqa, per, "mode 1 vs mode 0")
+    for k in range(Hkv):
+        for g in range(1, G):
+            assert np.array_equal(gqa[:, k * G + g], gqa[:, k * G])
+            assert np.array_equal(per[:, k * G + g], per[:, k * G])
+
+
+# --------------------------------------------------- guards and error paths
+def test_output_guard_regions_untouched(gq):
+    rng = np.random.default_rng(4)
+    B, C, Hq, Hkv, D = 2, 640, 12, 4, 64
+    attn, v, sl = rand_case(rng, B, C, Hq, Hkv, D, "fp16", [640, 17])
+    ref = run_oracle(attn, v, sl, "fp16")
+    dev = torch.device("cuda")
+    n = B * Hq * D
+    guard = 4096
+    buf = torch.full((guard + n + guard,), 12345.0, dtype=torch.float32, device=dev)
+    out = buf[guard:guard + n].view(B, Hq, D)
+    for mode in (0, 1):
+        gq.gqa_av_decode(attn.to(dev), v.to(dev), sl.to(dev), out, mode=mode)
+        gq.gqa_av_device_status()
+        assert_close(out.cpu().double().numpy(), ref, f"mode {mode}")
+        assert torch.all(buf[:guard] == 12345.0) and torch.all(buf[guard + n:] == 12345.0)
+
+
+def test_invalid_calls_launch_nothing(gq):
+    dev = torch.device("cuda")
+    attn = torch.zeros((1, 16, 6), device=dev)
+    v = torch.zeros((1, 16, 4, 8), dtype=torch.bfloat16, device=dev)
+    out = torch.full((1, 6, 8), 7.0, device=dev)
+    with pytest.raises(gq.GqaAvError) as e:
+        gq.gqa_av_decode(attn, v, None, out, mode=1)
+    assert e.value.status == 1
+    v12 = torch.zeros((1, 16, 2, 12), dtype=torch.bfloat16, device=dev)
+    out12 = torch.full((1, 6, 12), 7.0, device=dev)
+    with pytest.raises(gq.GqaAvError) as e:
+        gq.gqa_av_decode(attn, v12, None, out12)
+    assert e.value.status == 2
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0) and torch.all(out12 == 7.0)
+
+
+def test_caller_supplied_workspace(gq):
+    rng = np.random.default_rng(6)
+    B, C, Hq, Hkv, D = 1, 4096, 32, 8, 128
+    attn, v, sl = rand_case(rng, B, C, Hq, Hkv, D, "bf16", [4096])
+    ref = run_oracle(attn, v, sl, "bf16")
+    need = gq.gqa_av_workspace_bytes(B, C, Hq, Hkv, D, 0, 1)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    gq.gqa_av_set_workspace(ws)
+    try:
+        assert_close(run_gpu(gq, attn, v, sl, 1), ref, "caller workspace")
+        small = torch.empty(300 * 1024, dtype=torch.uint8, device="cuda")
+        gq.gqa_av_set_workspace(small)
+        with pytest.raises(gq.GqaAvError) as e:
+            run_gpu(gq, attn, v, sl, 1, dict(nsplit=16))
+        assert e.value.status == 4
+    finally:
+        gq.gqa_av_set_workspace(None)
+    assert_close(run_gpu(gq, attn, v, sl, 1), ref, "library workspace again")
+
+
+def test_plan_reports_the_launch(gq):
+    p = gq.gqa_av_plan(1, 8192, 32, 8, 128, 0, -1)
+    assert p["mode"] == 1 and p["heads_per_cta"] == 4 and p["tiles"] == 8
+    assert p["ctas"] == p["tiles"] * p["nsplit"] and p["ctas_per_sm"] >= 1
+    q = gq.gqa_av_plan(1, 8192, 32, 32, 128, 0, -1)
+    assert q["mode"] == 0 and q["heads_per_cta"] == 1
+    r = gq.gqa_av_plan(8, 32768, 16, 1, 256, 1, -1)
+    assert r["heads_per_cta"] == 16 and r["head_chunk"] == 16
