@@ -61,6 +61,7 @@ def _load() -> ctypes.CDLL:
     lib.gqa_av_decode.argtypes = [P, P, P, P, *sizes, I, I, P]
     lib.gqa_av_decode_per_head.argtypes = [P, P, P, P, *sizes, I, P]
     lib.gqa_av_decode_tuned.argtypes = [P, P, P, P, *sizes, I, I, ctypes.POINTER(Tuning), P]
+    lib.gqa_av_decode_noalloc.argtypes = [P, P, P, P, *sizes, I, I, P]
     lib.gqa_av_plan.argtypes = [*sizes, I, I, ctypes.POINTER(Tuning), ctypes.POINTER(PlanInfo)]
     lib.gqa_av_workspace_bytes.argtypes = [*sizes, I, I]
     lib.gqa_av_workspace_bytes.restype = S
@@ -71,7 +72,8 @@ def _load() -> ctypes.CDLL:
     lib.gqa_av_last_error.argtypes = []
     lib.gqa_av_last_error.restype = ctypes.c_char_p
     lib.gqa_av_version.argtypes = []
-    for f in ("gqa_av_decode", "gqa_av_decode_per_head", "gqa_av_decode_tuned", "gqa_av_plan",
+    for f in ("gqa_av_decode", "gqa_av_decode_per_head", "gqa_av_decode_tuned",
+              "gqa_av_decode_noalloc", "gqa_av_plan",
               "gqa_av_set_workspace", "gqa_av_device_status", "gqa_av_version"):
         getattr(lib, f).restype = I
     return lib
@@ -133,6 +135,17 @@ def gqa_av_decode_per_head(attn, v_cache, seq_lens, out, stream=None) -> torch.T
     B, C, Hq, Hkv, D, vd = _shapes(attn, v_cache, seq_lens, out)
     _check(lib.gqa_av_decode_per_head(_ptr(attn), _ptr(v_cache), _ptr(seq_lens), _ptr(out),
                                       B, C, Hq, Hkv, D, vd, _stream_handle(stream)))
+    return out
+
+
+def gqa_av_decode_noalloc(attn, v_cache, seq_lens, out, mode: int = MODE_AUTO,
+                          stream=None) -> torch.Tensor:
+    """gqa_av_decode for callers that may not allocate device memory: the
+    library's fixed scratch array is used and no call allocates. The first call
+    on a device looks up that array's address; make it before any capture."""
+    B, C, Hq, Hkv, D, vd = _shapes(attn, v_cache, seq_lens, out)
+    _check(lib.gqa_av_decode_noalloc(_ptr(attn), _ptr(v_cache), _ptr(seq_lens), _ptr(out),
+                                     B, C, Hq, Hkv, D, vd, int(mode), _stream_handle(stream)))
     return out
 
 

@@ -516,3 +516,74 @@ const char* gqa_av_last_error(void) { return g_last_error.c_str(); }
 int gqa_av_version(void) { return 1; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Support for the no-allocation entry point (gqa_av_noalloc.cu). These two
+// functions are used only by that entry point and leave the paths above as
+// they are.
+// ---------------------------------------------------------------------------
+namespace gqa_av {
+
+int record_error(int status, const char* msg) { return fail(status, "%s", msg); }
+
+// One call of the reduction in the default launch shape, with the status
+// word, split tickets and split partials placed in caller-given device scratch
+// laid out as [status_bytes][ticket_bytes][partials]. Clears the status word
+// and the tickets it uses on `stream` before the launch; allocates nothing.
+int run_in_scratch(const float* attn, const void* v, const int32_t* seq_lens, float* out, int B,
+                   int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode, cudaStream_t stream,
+                   void* scratch, size_t status_bytes, size_t ticket_bytes, size_t scratch_bytes) {
+  g_last_error.clear();
+  int rc = check_shape(B, Cmax, Hq, Hkv, D, v_dtype, mode);
+  if (rc) return rc;
+  if (!attn || !v || !out) return fail(GQA_AV_ERR_INVALID, "attn, v_cache and out must be non-NULL");
+  if ((reinterpret_cast<uintptr_t>(attn) | reinterpret_cast<uintptr_t>(v) |
+       reinterpret_cast<uintptr_t>(out)) & 15)
+    return fail(GQA_AV_ERR_UNSUPPORTED, "attn, v_cache and out must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(seq_lens) & 3)
+    return fail(GQA_AV_ERR_INVALID, "seq_lens must be 4-byte aligned");
+  int dev;
+  if ((rc = current_device(&dev))) return rc;
+  Plan pl;
+  if ((rc = make_plan(dev, B, Cmax, Hq, Hkv, D, v_dtype, mode, nullptr, &pl))) return rc;
+  const size_t partial_cap = scratch_bytes - status_bytes - ticket_bytes;
+  if (pl.nsplit > 1 && static_cast<size_t>(pl.tiles) * sizeof(unsigned) > ticket_bytes)
+    return fail(GQA_AV_ERR_UNSUPPORTED,
+                "no-allocation call: %d tiles need split tickets, the fixed scratch has room for %zu",
+                pl.tiles, ticket_bytes / sizeof(unsigned));
+  if (pl.ws_bytes > partial_cap)
+    return fail(GQA_AV_ERR_UNSUPPORTED,
+                "no-allocation call: this shape needs %zu B of split partials, the fixed scratch "
+                "holds %zu B (use gqa_av_decode)",
+                pl.ws_bytes, partial_cap);
+  char* base = static_cast<char*>(scratch);
+  const size_t clear = status_bytes + (pl.nsplit > 1 ? pl.tiles * sizeof(unsigned) : 0);
+  cudaError_t e = cudaMemsetAsync(base, 0, clear, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "clearing the no-allocation scratch");
+
+  Params p;
+  memset(&p, 0, sizeof p);
+  if ((rc = encode_v_map(&p.v_map, v, B, Cmax, Hkv, D, pl.dt, pl.R))) return rc;
+  p.attn = attn;
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.status = reinterpret_cast<unsigned*>(base);
+  p.tickets = reinterpret_cast<unsigned*>(base + status_bytes);
+  p.ws = reinterpret_cast<float*>(base + status_bytes + ticket_bytes);
+  p.B = B; p.Cmax = Cmax; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.G = Hq / Hkv;
+  p.heads = pl.heads; p.hgroups = pl.hgroups; p.dt = pl.dt; p.ndt = pl.ndt; p.ct = pl.ct;
+  p.nc = pl.nc; p.row_par = pl.row_par; p.R = pl.R; p.stages = pl.stages;
+  p.rows_per_split = pl.rows_per_split; p.nsplit = pl.nsplit; p.ap = pl.ap; p.avec = pl.avec;
+  p.v_stage_bytes = pl.v_stage_bytes; p.a_off = pl.a_off; p.bar_off = pl.bar_off;
+  p.timeout_ns = kWaitTimeoutNs;
+  if (pl.avec > 1 && (reinterpret_cast<uintptr_t>(attn) & (4 * pl.avec - 1))) p.avec = 1;
+
+  LaunchFn l;
+  OccFn o;
+  if (!pick_kernel(v_dtype, pl.gc, &l, &o)) return fail(GQA_AV_ERR_UNSUPPORTED, "no kernel");
+  e = l(p, pl.tiles * pl.nsplit, pl.smem, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
+  return GQA_AV_OK;
+}
+
+}  // namespace gqa_av

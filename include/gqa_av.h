@@ -141,6 +141,34 @@ int gqa_av_set_workspace(void *ptr, size_t bytes);
  */
 int gqa_av_device_status(void *stream, int clear);
 
+/*
+ * No-allocation variant of gqa_av_decode. The source pages have no
+ * counterpart to it; it exists for callers that may not allocate device memory when they run the
+ * reduction: engine plug-ins whose host owns all device memory, latency-
+ * critical loops that must not risk the implicit synchronisation of
+ * cudaMalloc/cudaFree, processes with a fixed up-front memory budget.
+ *
+ * Same arguments, layouts, launch shape and results as gqa_av_decode, but the
+ * scratch it needs (status word, split tickets, split partials) lives in one
+ * fixed array of GQA_AV_NOALLOC_SCRATCH_BYTES in this library's device
+ * globals, held on every GPU that loads the library until the process exits.
+ * No call allocates or frees memory. Set-up: the first call on each device
+ * looks up that array's device address (cudaGetSymbolAddress), so make that
+ * first call before any stream capture. A shape whose split partials need more
+ * than the array holds, or more than GQA_AV_NOALLOC_MAX_TILES split tiles, is
+ * rejected with GQA_AV_ERR_UNSUPPORTED and a message; gqa_av_decode handles it.
+ * All calls on a device share the array, which keeps the last call's
+ * contents: each call clears, on its stream, the status word and tickets it
+ * uses. Calls that may overlap on the GPU (unordered streams) race on the
+ * array and must not be issued.
+ */
+#define GQA_AV_NOALLOC_SCRATCH_BYTES (8u << 20) /* 8 MiB */
+#define GQA_AV_NOALLOC_MAX_TILES     4096
+
+int gqa_av_decode_noalloc(const float *attn, const void *v_cache, const int32_t *seq_lens,
+                          float *out, int B, int Cmax, int Hq, int Hkv, int D,
+                          int v_dtype, int mode, void *stream);
+
 /* Name of a status code; never NULL. */
 const char *gqa_av_status_string(int status);
 
