@@ -43,7 +43,8 @@ class Tuning(ctypes.Structure):
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "mode", "heads_per_cta", "head_chunk", "dtile", "rows_per_stage", "stages", "nsplit",
-        "rows_per_split", "tiles", "ctas", "threads_per_cta", "smem_bytes", "ctas_per_sm")] + [
+        "combine_ctas", "rows_per_split", "tiles", "ctas", "threads_per_cta", "smem_bytes",
+        "ctas_per_sm")] + [
         ("workspace_bytes", ctypes.c_size_t)]
 
     def as_dict(self):

@@ -16,6 +16,7 @@
 #include <tuple>
 
 #include "gqa_av.h"
+#define GQA_AV_COMBINE_KERNEL  // the split combine kernel lives in this translation unit
 #include "gqa_av_kernel.cuh"
 
 namespace gqa_av {
@@ -27,17 +28,15 @@ namespace gqa_av {
 #define GQA_AV_DECLARE_ALL(TAG)                                                              \
   GQA_AV_DECLARE(TAG, 1) GQA_AV_DECLARE(TAG, 2) GQA_AV_DECLARE(TAG, 3) GQA_AV_DECLARE(TAG, 4) \
   GQA_AV_DECLARE(TAG, 5) GQA_AV_DECLARE(TAG, 6) GQA_AV_DECLARE(TAG, 7) GQA_AV_DECLARE(TAG, 8) \
-  GQA_AV_DECLARE(TAG, 12) GQA_AV_DECLARE(TAG, 16)
+  GQA_AV_DECLARE(TAG, 12)
 GQA_AV_DECLARE_ALL(Bf16Tag)
 GQA_AV_DECLARE_ALL(Fp16Tag)
 
 namespace {
 
-constexpr int kHeadChunks[] = {16, 12, 8, 7, 6, 5, 4, 3, 2, 1};
-constexpr size_t kStatusBytes = 256;               // device status word + padding
-constexpr int kMaxTicketTiles = 65536;             // tiles that can share a split combine
-constexpr size_t kTicketBytes = kMaxTicketTiles * sizeof(unsigned);
-constexpr size_t kHeaderBytes = kStatusBytes + kTicketBytes;
+// Heads per thread; 16 would exceed the registers a 9-warp CTA can give a thread.
+constexpr int kHeadChunks[] = {12, 8, 7, 6, 5, 4, 3, 2, 1};
+constexpr size_t kHeaderBytes = 256;               // device status word + padding
 constexpr long long kWaitTimeoutNs = 2000000000LL; // 2 s bound on every mbarrier wait
 
 thread_local std::string g_last_error;
@@ -61,25 +60,28 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // ----------------------------------------------------------------- dispatch
 using LaunchFn = cudaError_t (*)(const Params&, int, int, cudaStream_t);
 using OccFn = cudaError_t (*)(int, int, int*);
+struct Kernel {
+  LaunchFn launch;
+  OccFn occupancy;
+};
 
 template <typename Tag>
-bool pick(int gc, LaunchFn* l, OccFn* o) {
+bool pick(int gc, Kernel* k) {
   switch (gc) {
-#define GQA_AV_CASE(GC)          \
-  case GC:                       \
-    *l = launch<Tag, GC>;        \
-    *o = occupancy<Tag, GC>;     \
+#define GQA_AV_CASE(GC)                          \
+  case GC:                                       \
+    *k = {launch<Tag, GC>, occupancy<Tag, GC>};  \
     return true;
     GQA_AV_CASE(1) GQA_AV_CASE(2) GQA_AV_CASE(3) GQA_AV_CASE(4) GQA_AV_CASE(5)
-    GQA_AV_CASE(6) GQA_AV_CASE(7) GQA_AV_CASE(8) GQA_AV_CASE(12) GQA_AV_CASE(16)
+    GQA_AV_CASE(6) GQA_AV_CASE(7) GQA_AV_CASE(8) GQA_AV_CASE(12)
 #undef GQA_AV_CASE
     default:
       return false;
   }
 }
 
-bool pick_kernel(int v_dtype, int gc, LaunchFn* l, OccFn* o) {
-  return v_dtype == GQA_AV_BF16 ? pick<Bf16Tag>(gc, l, o) : pick<Fp16Tag>(gc, l, o);
+bool pick_kernel(int v_dtype, int gc, Kernel* k) {
+  return v_dtype == GQA_AV_BF16 ? pick<Bf16Tag>(gc, k) : pick<Fp16Tag>(gc, k);
 }
 
 // ------------------------------------------------------------- device info
@@ -120,11 +122,10 @@ int ctas_per_sm(int dev, int smem_limit, int v_dtype, int gc, int smem, int* n) 
       return GQA_AV_OK;
     }
   }
-  LaunchFn l;
-  OccFn o;
-  if (!pick_kernel(v_dtype, gc, &l, &o)) return fail(GQA_AV_ERR_UNSUPPORTED, "no kernel for GC=%d", gc);
+  Kernel kern;
+  if (!pick_kernel(v_dtype, gc, &kern)) return fail(GQA_AV_ERR_UNSUPPORTED, "no kernel for GC=%d", gc);
   int k = 0;
-  cudaError_t e = o(smem_limit, smem, &k);
+  cudaError_t e = kern.occupancy(smem_limit, smem, &k);
   if (e != cudaSuccess) return fail_cuda(e, "occupancy query");
   std::lock_guard<std::mutex> lk(g_mu);
   g_occupancy[std::make_tuple(dev, v_dtype, gc, smem)] = k;
@@ -136,6 +137,7 @@ int ctas_per_sm(int dev, int smem_limit, int v_dtype, int gc, int smem, int* n) 
 struct Plan {
   int mode, heads, gc, nc, dt, ndt, ct, row_par, R, stages, nsplit, rows_per_split;
   int hgroups, tiles, ap, avec, smem, occ;
+  int parts, cols_per_cta, ctas_per_tile;  // split combine launch (nsplit > 1)
   uint32_t v_stage_bytes, a_off, bar_off;
   size_t ws_bytes;  // partials only
 };
@@ -202,7 +204,14 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
                   t->rows_per_stage);
     p->R = t->rows_per_stage;
   } else {
-    p->R = std::max(8, std::min(256, 8192 / (2 * p->dt)));
+    // About 32 KiB of V per stage (large TMA boxes stream faster per SM), but
+    // short enough that a short context still splits across every SM.
+    p->R = std::max(8, std::min(256, 32768 / (2 * p->dt)));
+    const long long tiles = static_cast<long long>(Hq / p->heads) * B * (D / p->dt);
+    if (tiles < di.sms) {
+      const long long want = (di.sms + tiles - 1) / tiles;  // splits that reach every SM
+      p->R = static_cast<int>(std::min<long long>(p->R, std::max<long long>(8, Cmax / (2 * want))));
+    }
     p->R = std::min(p->R, static_cast<int>(align_up(Cmax, 8)));
     p->R = std::max(8, p->R / 8 * 8);
   }
@@ -211,7 +220,7 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
       return fail(GQA_AV_ERR_INVALID, "stages=%d must be in [2, %d]", t->stages, kMaxStages);
     p->stages = t->stages;
   } else {
-    p->stages = 6;
+    p->stages = 3;
   }
   p->ap = static_cast<int>(align_up(p->heads, 4));
   layout(p);
@@ -230,20 +239,23 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
   if ((rc = ctas_per_sm(dev, di.smem_optin, v_dtype, p->gc, p->smem, &p->occ))) return rc;
   if (p->occ < 1) return fail(GQA_AV_ERR_UNSUPPORTED, "kernel does not fit on an SM");
 
-  // Context splits: enough CTAs to fill every SM, with at least 4 stages of rows each.
+  // Context splits: with fewer tiles than SMs the grid is one wave whose
+  // splits cover every SM; with many tiles it runs in waves (a split with no
+  // context exits at once) and splits only balance ragged lengths.
   p->tiles = p->hgroups * B * p->ndt;
-  const int max_split = std::max(1, (Cmax + 4 * p->R - 1) / (4 * p->R));
+  const int max_split = std::max(1, Cmax / (2 * p->R));  // at least two stages of rows
+  const long long wave = static_cast<long long>(di.sms) * p->occ;
   int nsplit;
   if (t && t->nsplit > 0) {
     nsplit = std::min(t->nsplit, (Cmax + p->R - 1) / p->R);
+  } else if (p->tiles < di.sms) {
+    nsplit = static_cast<int>(std::min<long long>(max_split, di.sms / p->tiles));
   } else {
-    const long long wave = static_cast<long long>(di.sms) * p->occ;
     const double v_bytes = static_cast<double>(B) * Cmax * (p->heads == 1 ? Hq : Hkv) * D * 2;
     const int waves = v_bytes > 256e6 ? 4 : 1;
     nsplit = static_cast<int>(std::min<long long>(
         max_split, std::max<long long>(1, (wave * waves + p->tiles - 1) / p->tiles)));
   }
-  if (p->tiles > kMaxTicketTiles) nsplit = 1;
   nsplit = std::max(1, nsplit);
   p->rows_per_split = static_cast<int>(align_up((Cmax + nsplit - 1) / nsplit, p->R));
   p->nsplit = (Cmax + p->rows_per_split - 1) / p->rows_per_split;
@@ -252,8 +264,51 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
   p->ws_bytes = p->nsplit > 1
                     ? static_cast<size_t>(p->tiles) * p->nsplit * p->heads * p->dt * sizeof(float)
                     : 0;
+  // Split combine: `parts` threads per float4 column, a power of two <= 16.
+  p->parts = 1;
+  while (p->parts < 16 && p->parts < p->nsplit) p->parts *= 2;
+  p->cols_per_cta = kCombineThreads / p->parts;
+  const int ncol4 = p->heads * p->dt / 4;
+  p->ctas_per_tile = (ncol4 + p->cols_per_cta - 1) / p->cols_per_cta;
   return GQA_AV_OK;
 }
+
+// Kernel parameters of one call of plan `pl` (everything but the tensor map).
+void fill_params(Params* p, const Plan& pl, const float* attn, const int32_t* seq_lens,
+                 float* out, void* status, void* partials, int B, int Cmax, int Hq, int Hkv,
+                 int D) {
+  p->attn = attn;
+  p->seq_lens = seq_lens;
+  p->out = out;
+  p->status = static_cast<unsigned*>(status);
+  p->ws = static_cast<float*>(partials);
+  p->B = B; p->Cmax = Cmax; p->Hq = Hq; p->Hkv = Hkv; p->D = D; p->G = Hq / Hkv;
+  p->heads = pl.heads; p->hgroups = pl.hgroups; p->dt = pl.dt; p->ndt = pl.ndt; p->ct = pl.ct;
+  p->nc = pl.nc; p->row_par = pl.row_par; p->R = pl.R; p->stages = pl.stages;
+  p->rows_per_split = pl.rows_per_split; p->nsplit = pl.nsplit;
+  p->ap = pl.ap; p->avec = pl.avec;
+  p->v_stage_bytes = pl.v_stage_bytes; p->a_off = pl.a_off; p->bar_off = pl.bar_off;
+  p->timeout_ns = kWaitTimeoutNs;
+  if (pl.avec > 1 && (reinterpret_cast<uintptr_t>(attn) & (4 * pl.avec - 1))) p->avec = 1;
+}
+
+// Launches the main kernel and, when the tile has several splits, the split
+// combine right after it on the same stream.
+cudaError_t launch_call(const Kernel& kern, const Plan& pl, const Params& p, cudaStream_t stream) {
+  cudaError_t e = kern.launch(p, pl.tiles * pl.nsplit, pl.smem, stream);
+  if (e != cudaSuccess || pl.nsplit == 1) return e;
+  CombineParams c;
+  c.ws = p.ws;
+  c.seq_lens = p.seq_lens;
+  c.out = p.out;
+  c.B = p.B; c.Cmax = p.Cmax; c.Hq = p.Hq; c.D = p.D;
+  c.heads = pl.heads; c.dt = pl.dt; c.ndt = pl.ndt;
+  c.rows_per_split = pl.rows_per_split; c.nsplit = pl.nsplit;
+  c.tile_elems = pl.heads * pl.dt;
+  c.parts = pl.parts; c.cols_per_cta = pl.cols_per_cta; c.ctas_per_tile = pl.ctas_per_tile;
+  return launch_combine(c, pl.tiles * pl.ctas_per_tile, stream);
+}
+
 
 // -------------------------------------------------------------- workspace
 struct Workspace {
@@ -369,29 +424,36 @@ int run(const float* attn, const void* v, const int32_t* seq_lens, float* out, i
   Params p;
   memset(&p, 0, sizeof p);
   if ((rc = encode_v_map(&p.v_map, v, B, Cmax, Hkv, D, pl.dt, pl.R))) return rc;
-  p.attn = attn;
-  p.seq_lens = seq_lens;
-  p.out = out;
-  p.status = static_cast<unsigned*>(ws.base);
-  p.tickets = reinterpret_cast<unsigned*>(static_cast<char*>(ws.base) + kStatusBytes);
-  p.ws = reinterpret_cast<float*>(static_cast<char*>(ws.base) + kHeaderBytes);
-  p.B = B; p.Cmax = Cmax; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.G = Hq / Hkv;
-  p.heads = pl.heads; p.hgroups = pl.hgroups; p.dt = pl.dt; p.ndt = pl.ndt; p.ct = pl.ct;
-  p.nc = pl.nc; p.row_par = pl.row_par; p.R = pl.R; p.stages = pl.stages;
-  p.rows_per_split = pl.rows_per_split; p.nsplit = pl.nsplit; p.ap = pl.ap; p.avec = pl.avec;
-  p.v_stage_bytes = pl.v_stage_bytes; p.a_off = pl.a_off; p.bar_off = pl.bar_off;
-  p.timeout_ns = kWaitTimeoutNs;
-  if (pl.avec > 1 && (reinterpret_cast<uintptr_t>(attn) & (4 * pl.avec - 1))) p.avec = 1;
+  char* wsb = static_cast<char*>(ws.base);
+  fill_params(&p, pl, attn, seq_lens, out, wsb, wsb + kHeaderBytes, B, Cmax, Hq, Hkv, D);
 
-  LaunchFn l;
-  OccFn o;
-  if (!pick_kernel(v_dtype, pl.gc, &l, &o)) return fail(GQA_AV_ERR_UNSUPPORTED, "no kernel");
-  cudaError_t e = l(p, pl.tiles * pl.nsplit, pl.smem, stream);
+  Kernel kern;
+  if (!pick_kernel(v_dtype, pl.gc, &kern)) return fail(GQA_AV_ERR_UNSUPPORTED, "no kernel");
+  cudaError_t e = launch_call(kern, pl, p, stream);
   if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
   return GQA_AV_OK;
 }
 
 }  // namespace
+
+// Programmatic dependent launch, like the main kernel: the combine starts its
+// prologue while the main kernel drains and reads the partials only after
+// griddepcontrol.wait.
+cudaError_t launch_combine(const CombineParams& p, int grid, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gqa_av_combine_kernel, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 }  // namespace gqa_av
 
 using namespace gqa_av;
@@ -433,6 +495,7 @@ int gqa_av_plan(int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode,
   info->rows_per_stage = p.R;
   info->stages = p.stages;
   info->nsplit = p.nsplit;
+  info->combine_ctas = p.nsplit > 1 ? p.tiles * p.ctas_per_tile : 0;
   info->rows_per_split = p.rows_per_split;
   info->tiles = p.tiles;
   info->ctas = p.tiles * p.nsplit;
@@ -527,12 +590,12 @@ namespace gqa_av {
 int record_error(int status, const char* msg) { return fail(status, "%s", msg); }
 
 // One call of the reduction in the default launch shape, with the status
-// word, split tickets and split partials placed in caller-given device scratch
-// laid out as [status_bytes][ticket_bytes][partials]. Clears the status word
-// and the tickets it uses on `stream` before the launch; allocates nothing.
+// word and split partials placed in caller-given device scratch laid out as
+// [status_bytes][partials]. Clears the status word on `stream` before the
+// launch; allocates nothing.
 int run_in_scratch(const float* attn, const void* v, const int32_t* seq_lens, float* out, int B,
                    int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode, cudaStream_t stream,
-                   void* scratch, size_t status_bytes, size_t ticket_bytes, size_t scratch_bytes) {
+                   void* scratch, size_t status_bytes, size_t scratch_bytes) {
   g_last_error.clear();
   int rc = check_shape(B, Cmax, Hq, Hkv, D, v_dtype, mode);
   if (rc) return rc;
@@ -546,42 +609,24 @@ int run_in_scratch(const float* attn, const void* v, const int32_t* seq_lens, fl
   if ((rc = current_device(&dev))) return rc;
   Plan pl;
   if ((rc = make_plan(dev, B, Cmax, Hq, Hkv, D, v_dtype, mode, nullptr, &pl))) return rc;
-  const size_t partial_cap = scratch_bytes - status_bytes - ticket_bytes;
-  if (pl.nsplit > 1 && static_cast<size_t>(pl.tiles) * sizeof(unsigned) > ticket_bytes)
-    return fail(GQA_AV_ERR_UNSUPPORTED,
-                "no-allocation call: %d tiles need split tickets, the fixed scratch has room for %zu",
-                pl.tiles, ticket_bytes / sizeof(unsigned));
+  const size_t partial_cap = scratch_bytes - status_bytes;
   if (pl.ws_bytes > partial_cap)
     return fail(GQA_AV_ERR_UNSUPPORTED,
                 "no-allocation call: this shape needs %zu B of split partials, the fixed scratch "
                 "holds %zu B (use gqa_av_decode)",
                 pl.ws_bytes, partial_cap);
   char* base = static_cast<char*>(scratch);
-  const size_t clear = status_bytes + (pl.nsplit > 1 ? pl.tiles * sizeof(unsigned) : 0);
-  cudaError_t e = cudaMemsetAsync(base, 0, clear, stream);
+  cudaError_t e = cudaMemsetAsync(base, 0, status_bytes, stream);
   if (e != cudaSuccess) return fail_cuda(e, "clearing the no-allocation scratch");
 
   Params p;
   memset(&p, 0, sizeof p);
   if ((rc = encode_v_map(&p.v_map, v, B, Cmax, Hkv, D, pl.dt, pl.R))) return rc;
-  p.attn = attn;
-  p.seq_lens = seq_lens;
-  p.out = out;
-  p.status = reinterpret_cast<unsigned*>(base);
-  p.tickets = reinterpret_cast<unsigned*>(base + status_bytes);
-  p.ws = reinterpret_cast<float*>(base + status_bytes + ticket_bytes);
-  p.B = B; p.Cmax = Cmax; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.G = Hq / Hkv;
-  p.heads = pl.heads; p.hgroups = pl.hgroups; p.dt = pl.dt; p.ndt = pl.ndt; p.ct = pl.ct;
-  p.nc = pl.nc; p.row_par = pl.row_par; p.R = pl.R; p.stages = pl.stages;
-  p.rows_per_split = pl.rows_per_split; p.nsplit = pl.nsplit; p.ap = pl.ap; p.avec = pl.avec;
-  p.v_stage_bytes = pl.v_stage_bytes; p.a_off = pl.a_off; p.bar_off = pl.bar_off;
-  p.timeout_ns = kWaitTimeoutNs;
-  if (pl.avec > 1 && (reinterpret_cast<uintptr_t>(attn) & (4 * pl.avec - 1))) p.avec = 1;
+  fill_params(&p, pl, attn, seq_lens, out, base, base + status_bytes, B, Cmax, Hq, Hkv, D);
 
-  LaunchFn l;
-  OccFn o;
-  if (!pick_kernel(v_dtype, pl.gc, &l, &o)) return fail(GQA_AV_ERR_UNSUPPORTED, "no kernel");
-  e = l(p, pl.tiles * pl.nsplit, pl.smem, stream);
+  Kernel kern;
+  if (!pick_kernel(v_dtype, pl.gc, &kern)) return fail(GQA_AV_ERR_UNSUPPORTED, "no kernel");
+  e = launch_call(kern, pl, p, stream);
   if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
   return GQA_AV_OK;
 }

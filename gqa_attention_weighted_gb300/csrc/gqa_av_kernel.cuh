@@ -1,30 +1,35 @@
-// GQA AV decode reduction kernel for sm_103a (GB300).
+// GQA AV decode reduction kernels for sm_103a (GB300).
 //
 // Operation (page "pytorch/executorch pull 21063", summary paragraph):
 //   out[b, q_h, d] = sum_{c < L_b} attn[b, c, q_h] * V[b, c, q_h / G, d].
 //
-// One CTA owns a tile (head group, b, d-tile) and one context split of it.
-// In GQA-reuse mode a head group is the G query heads of one KV head, so each
-// V row is fetched from HBM once and used for all G heads (the GQA-reuse
-// paragraph on the same page); in per-head mode a head group is one query
-// head and V rows are fetched once per query head.
+// gqa_av_kernel: one CTA owns a tile (head group, b, d-tile) and one context
+// split of it. In GQA-reuse mode a head group is the G query heads of one KV
+// head, so each V row is fetched from HBM once and used for all G heads (the
+// GQA-reuse paragraph on the same page); in per-head mode a head group is one
+// query head and V rows are fetched once per query head.
 //
 // Warp roles:
-//   * warp kConsumerWarps (the producer): lane 0 streams V rows with 4-D TMA
+//   * producer (warp kConsumerWarps): lane 0 streams V rows with 4-D TMA
 //     tensor loads into a multi-stage shared-memory ring; all 32 lanes copy the
 //     matching attn weights with cp.async. Both signal one "full" mbarrier per
-//     stage.
-//   * warps 0..kConsumerWarps-1 (consumers): thread t owns 8 adjacent output
+//     stage; a slot is refilled once every consumer warp has released it
+//     ("empty" mbarrier). Stage 0 is issued before the sequence length is read.
+//   * consumers (warps 0..kConsumerWarps-1): thread t owns 8 adjacent output
 //     columns of one head chunk and a row slot; for every V row of its slot it
-//     widens 8 bf16/fp16 values to fp32 and does GC x 8 FMAs into registers,
-//     then releases the stage through an "empty" mbarrier.
-// After the context loop the row slots are summed in shared memory in a fixed
-// order. A split that is alone writes `out` directly; otherwise it writes its
-// partial to the workspace and takes a ticket; the last CTA of the tile sums
-// all partials in split order and writes `out`, so results are bitwise
-// reproducible and independent of CTA arrival order. Every mbarrier wait is
-// bounded by a %globaltimer deadline; on expiry the CTA sets the device status
-// word, lets its own copies in flight land, and returns.
+//     widens 8 bf16/fp16 values to fp32 and does GC x 8 FMAs (packed f32x2,
+//     each lane rounded like fmaf) into registers.
+// After the context loop the row slots are summed through shared memory in
+// slot order. A tile whose context fits one split writes `out`; otherwise
+// each split writes its partial to the workspace and gqa_av_combine_kernel,
+// launched next on the same stream, sums the partials of every (tile, column)
+// in split order. Results are bitwise reproducible.
+//
+// Both kernels use programmatic dependent launch: each starts its prologue
+// while the previous kernel in the stream drains, and touches data of earlier
+// kernels only after griddepcontrol.wait. Every mbarrier wait is bounded by a
+// %globaltimer deadline; on expiry the CTA sets the device status word, lets
+// its own copies in flight land, and returns.
 #pragma once
 
 #include <cuda.h>
@@ -37,8 +42,9 @@ namespace gqa_av {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;
+constexpr int kThreads = kConsumerThreads + 32;  // + the producer warp
 constexpr int kMaxStages = 8;
+constexpr int kCombineThreads = 256;
 
 // Device status word bits.
 constexpr unsigned kErrFullWait = 1u;
@@ -50,8 +56,7 @@ struct alignas(64) Params {
   const float* attn;            // [B, Cmax, Hq]
   const int32_t* seq_lens;      // [B] or null
   float* out;                   // [B, Hq, D]
-  float* ws;                    // [tiles][nsplit][heads * dt] partials
-  unsigned int* tickets;        // [tiles], zero between calls
+  float* ws;                    // [tiles][nsplit][heads * dt] split partials
   unsigned int* status;         // device status word
   int B, Cmax, Hq, Hkv, D, G;
   int heads;                    // query heads per CTA
@@ -64,13 +69,28 @@ struct alignas(64) Params {
   int R;                        // rows per stage
   int stages;
   int rows_per_split;
-  int nsplit;
+  int nsplit;                   // context splits per tile
   int ap;                       // floats per attn row in shared memory
   int avec;                     // floats per attn cp.async (1, 2 or 4)
   uint32_t v_stage_bytes;       // R * dt * 2
   uint32_t a_off;               // shared-memory offset of the attn ring
   uint32_t bar_off;             // shared-memory offset of the mbarriers
   long long timeout_ns;         // bound on every mbarrier wait
+};
+
+// The split combine: out[tile column] = sum over the tile's splits with
+// context, ws[tile][s][column], in split order.
+struct CombineParams {
+  const float* ws;              // [tiles][nsplit][tile_elems]
+  const int32_t* seq_lens;      // [B] or null
+  float* out;                   // [B, Hq, D]
+  int B, Cmax, Hq, D;
+  int heads, dt, ndt;
+  int rows_per_split, nsplit;
+  int tile_elems;               // heads * dt
+  int parts;                    // threads per column (fixed chunks of splits)
+  int cols_per_cta;             // float4 columns per CTA (kCombineThreads / parts)
+  int ctas_per_tile;
 };
 
 // ---------------------------------------------------------------------------
@@ -90,28 +110,39 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// One potentially blocking test of the phase of `parity`: the thread is
+// suspended until the phase completes or about `hint_ns` pass, so a waiting
+// warp takes no issue slots from the warps that do the work.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
 
 // Waits for the phase of `parity` to complete; false if `timeout_ns` passed.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long timeout_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait(bar, parity, 100000u)) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity, 100000u)) return true;
     if (static_cast<long long>(global_timer_ns() - t0) > timeout_ns) return false;
   }
+}
+
+// Programmatic dependent launch: wait until the previous kernel in the stream
+// has completed and its memory is visible (a no-op without such a launch),
+// and allow the next kernel to start its own prologue.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -159,6 +190,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
+// Named barrier of the consumer warps only (the producer warp does not join).
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
 }
@@ -210,11 +242,46 @@ __device__ __forceinline__ void load_weights(const float* a, float (&w)[GC]) {
   }
 }
 
+__device__ __forceinline__ void add4(float4& s, const float4 x) {
+  s.x += x.x; s.y += x.y; s.z += x.z; s.w += x.w;
+}
+
+// s += src[lo * stride] + ... + src[(hi-1) * stride], added in index order;
+// the loads of each batch are issued together. kGlobal reads through L2 only.
+template <bool kGlobal>
+__device__ __forceinline__ void sum_strided(float4& s, const float4* src, size_t stride, int lo,
+                                            int hi) {
+  constexpr int kBatch = 8;
+  for (int i0 = lo; i0 < hi; i0 += kBatch) {
+    float4 x[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i)
+      if (i0 + i < hi) x[i] = kGlobal ? __ldcg(src + (i0 + i) * stride) : src[(i0 + i) * stride];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i)
+      if (i0 + i < hi) add4(s, x[i]);
+  }
+}
+
+// Two fp32 lanes in one 64-bit register pair, and the packed FMA on them:
+// acc.lo += w * v.lo, acc.hi += w * v.hi, each rounded like fmaf.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t x, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+}
+__device__ __forceinline__ void ffma2(uint64_t& acc, uint64_t w2, uint64_t v2) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(w2), "l"(v2));
+}
+
 // ---------------------------------------------------------------------------
-// The kernel. Tag selects the V element type, GC the heads per thread.
+// The main kernel. Tag selects the V element type, GC the heads per thread.
 // ---------------------------------------------------------------------------
 template <typename Tag, int GC>
-__global__ void __launch_bounds__(kThreads, (GC <= 8 ? 2 : 1))
+__global__ void __launch_bounds__(kThreads, 1)
 gqa_av_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t smem[];
 
@@ -233,14 +300,7 @@ gqa_av_kernel(const __grid_constant__ Params p) {
   const int h0 = hg * p.heads;            // first query head of the CTA
   const int kv_h = h0 / p.G;              // its KV head (all heads of the CTA share it)
   const int d0 = dti * p.dt;
-
-  int L = p.seq_lens ? p.seq_lens[b] : p.Cmax;
-  L = L < 0 ? 0 : (L > p.Cmax ? p.Cmax : L);
-  const int nsplit_b = L > 0 ? (L + p.rows_per_split - 1) / p.rows_per_split : 1;
-  if (split >= nsplit_b) return;          // whole CTA: no context left for it
-  const int c_begin = split * p.rows_per_split;
-  const int c_end = min(c_begin + p.rows_per_split, L);
-  const int n_iters = c_end > c_begin ? (c_end - c_begin + p.R - 1) / p.R : 0;
+  const int c_begin = split * p.rows_per_split;  // < Cmax for every launched split
   const int tile_elems = p.heads * p.dt;
 
   uint8_t* vring = smem;
@@ -258,15 +318,57 @@ gqa_av_kernel(const __grid_constant__ Params p) {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_flag = 0;
   }
+  if (warp == kConsumerWarps && lane == 0)  // a kernel parameter: fetch it during the wait
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.v_map)) : "memory");
   __syncthreads();
 
-  // ----------------------------------------------------------------- producer
+  // Nothing written by earlier kernels is touched before they are done.
+  grid_dependency_wait();
+  grid_launch_dependents();
+
   if (warp == kConsumerWarps) {
+    // ----------------------------------------------------------------- producer
     const uint64_t policy = evict_first_policy();
+    const float* attn_b = p.attn + (size_t)b * p.Cmax * p.Hq + h0;
     const int per_row = p.heads / p.avec;
-    int issued = 0;
+    // V rows [c0, c0 + R) by TMA; attn weights of the first `rows` of them by cp.async.
+    auto issue = [&](int stage, int c0, int rows) {
+      const uint32_t full = full0 + 8 * stage;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(full, p.v_stage_bytes);
+        tma_load_4d(smem_addr(vring + (size_t)stage * p.v_stage_bytes), &p.v_map, d0, kv_h, c0, b,
+                    full, policy);
+      }
+      const float* src = attn_b + (size_t)c0 * p.Hq;
+      const uint32_t dst = smem_addr(aring + (size_t)stage * p.R * p.ap);
+      const int n = rows * per_row;
+      for (int i = lane; i < n; i += 32) {
+        const int r = i / per_row, k = (i - r * per_row) * p.avec;
+        const uint32_t d = dst + 4u * (r * p.ap + k);
+        const float* sp = src + (size_t)r * p.Hq + k;
+        if (p.avec == 4) cp_async<16>(d, sp);
+        else if (p.avec == 2) cp_async<8>(d, sp);
+        else cp_async<4>(d, sp);
+      }
+      cp_async_arrive_noinc(full);
+    };
+    // Stage 0 goes out before the sequence length is known; its rows lie
+    // inside [0, Cmax) whatever the length is.
+    issue(0, c_begin, min(p.R, p.Cmax - c_begin));
+
+    int L = p.seq_lens ? p.seq_lens[b] : p.Cmax;
+    L = L < 0 ? 0 : (L > p.Cmax ? p.Cmax : L);
+    const int nsplit_b = L > 0 ? (L + p.rows_per_split - 1) / p.rows_per_split : 1;
+    if (split >= nsplit_b) {
+      // No context for this split: let the early stage land, then leave.
+      if (!mbar_wait(full0, 0, p.timeout_ns) && lane == 0) atomicOr(p.status, kErrDrain);
+      return;
+    }
+    const int c_end = min(c_begin + p.rows_per_split, L);
+    const int n_iters = c_end > c_begin ? (c_end - c_begin + p.R - 1) / p.R : 0;
+    int issued = 1;
     bool ok = true;
-    for (int it = 0; it < n_iters; ++it) {
+    for (int it = 1; it < n_iters; ++it) {
       const int stage = it % p.stages;
       const uint32_t parity = ((it / p.stages) & 1) ^ 1;
       if (!mbar_wait(empty0 + 8 * stage, parity, p.timeout_ns)) {
@@ -275,64 +377,43 @@ gqa_av_kernel(const __grid_constant__ Params p) {
         break;
       }
       const int c0 = c_begin + it * p.R;
-      const int rows = min(p.R, c_end - c0);
-      const uint32_t full = full0 + 8 * stage;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(full, p.v_stage_bytes);
-        tma_load_4d(smem_addr(vring + (size_t)stage * p.v_stage_bytes), &p.v_map, d0, kv_h, c0, b,
-                    full, policy);
-      }
-      const float* src = p.attn + ((size_t)b * p.Cmax + c0) * p.Hq + h0;
-      const uint32_t dst = smem_addr(aring + (size_t)stage * p.R * p.ap);
-      const int n = rows * per_row;
-      if (p.avec == 4) {
-        for (int i = lane; i < n; i += 32) {
-          const int r = i / per_row, k = i - r * per_row;
-          cp_async<16>(dst + 4u * (r * p.ap + 4 * k), src + (size_t)r * p.Hq + 4 * k);
-        }
-      } else if (p.avec == 2) {
-        for (int i = lane; i < n; i += 32) {
-          const int r = i / per_row, k = i - r * per_row;
-          cp_async<8>(dst + 4u * (r * p.ap + 2 * k), src + (size_t)r * p.Hq + 2 * k);
-        }
-      } else {
-        for (int i = lane; i < n; i += 32) {
-          const int r = i / per_row, k = i - r * per_row;
-          cp_async<4>(dst + 4u * (r * p.ap + k), src + (size_t)r * p.Hq + k);
-        }
-      }
-      cp_async_arrive_noinc(full);
+      issue(stage, c0, min(p.R, c_end - c0));
       issued = it + 1;
     }
     cp_async_wait_all();
     if (!ok) {
-      // Let every TMA load this CTA issued land before the CTA can exit.
-      for (int it = 0; it < issued; ++it) {
-        const int stage = it % p.stages;
-        // Only the latest use of each stage can still be in flight.
-        if (it + p.stages < issued) continue;
-        if (!mbar_wait(full0 + 8 * stage, (it / p.stages) & 1, p.timeout_ns))
+      // Let every load this CTA issued land before the CTA can exit.
+      for (int it = max(0, issued - p.stages); it < issued; ++it)
+        if (!mbar_wait(full0 + 8 * (it % p.stages), (it / p.stages) & 1, p.timeout_ns))
           atomicOr(p.status, kErrDrain);
-      }
     }
     return;
   }
 
-  // ---------------------------------------------------------------- consumers
+  // ------------------------------------------------------------------ consumers
+  int L = p.seq_lens ? p.seq_lens[b] : p.Cmax;
+  L = L < 0 ? 0 : (L > p.Cmax ? p.Cmax : L);
+  const int nsplit_b = L > 0 ? (L + p.rows_per_split - 1) / p.rows_per_split : 1;
+  if (split >= nsplit_b) return;  // the producer waits for the early stage
+  const int c_end = min(c_begin + p.rows_per_split, L);
+  const int n_iters = c_end > c_begin ? (c_end - c_begin + p.R - 1) / p.R : 0;
+  const int n_stages = max(n_iters, 1);  // stages issued, counting the early one
+
   const int slots = p.ct * p.nc;
   const int my_col = tid % p.ct;
   const int my_chunk = (tid / p.ct) % p.nc;
   const int my_slot = tid / slots;
   const bool active = my_slot < p.row_par;
 
-  float acc[GC][8];
+  // acc[g][i] holds columns 2i and 2i+1 of head g of the chunk.
+  uint64_t acc[GC][4];
 #pragma unroll
   for (int g = 0; g < GC; ++g)
 #pragma unroll
-    for (int k = 0; k < 8; ++k) acc[g][k] = 0.f;
+    for (int i = 0; i < 4; ++i) acc[g][i] = 0ull;
 
   bool ok = true;
-  for (int it = 0; it < n_iters; ++it) {
+  for (int it = 0; it < n_stages; ++it) {
     const int stage = it % p.stages;
     if (!mbar_wait(full0 + 8 * stage, (it / p.stages) & 1, p.timeout_ns)) {
       atomicOr(p.status, kErrFullWait);
@@ -349,12 +430,17 @@ gqa_av_kernel(const __grid_constant__ Params p) {
         const uint4 raw = *reinterpret_cast<const uint4*>(vst + (size_t)r * p.dt);
         float v[8];
         widen8(Tag{}, raw, v);
+        uint64_t v2[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v2[i] = pack2(v[2 * i], v[2 * i + 1]);
         float w[GC];
         load_weights<GC>(ast + (size_t)r * p.ap, w);
 #pragma unroll
-        for (int g = 0; g < GC; ++g)
+        for (int g = 0; g < GC; ++g) {
+          const uint64_t w2 = pack2(w[g], w[g]);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) acc[g][k] = fmaf(w[g], v[k], acc[g][k]);
+          for (int i = 0; i < 4; ++i) ffma2(acc[g][i], w2, v2[i]);
+        }
       }
     }
     __syncwarp();
@@ -362,66 +448,102 @@ gqa_av_kernel(const __grid_constant__ Params p) {
   }
   if (!ok) s_flag = 1;
   consumer_sync();
-  if (s_flag) return;  // the producer drains in-flight copies before exiting
+  if (s_flag) return;  // the producer drains the loads it issued
 
-  // Row slots -> one partial per (head, column), summed in slot order.
+  // Row slots -> this CTA's partial: every slot writes its accumulators to its
+  // own row of shared memory, then each float4 column is summed over the rows
+  // in slot order.
   float* red = reinterpret_cast<float*>(smem);  // the V ring is free now
   if (active) {
     float* dst = red + (size_t)my_slot * tile_elems + (size_t)(my_chunk * GC) * p.dt + my_col * 8;
 #pragma unroll
     for (int g = 0; g < GC; ++g) {
+      float x[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) unpack2(acc[g][i], x[2 * i], x[2 * i + 1]);
       float4* q = reinterpret_cast<float4*>(dst + (size_t)g * p.dt);
-      q[0] = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
-      q[1] = make_float4(acc[g][4], acc[g][5], acc[g][6], acc[g][7]);
+      q[0] = make_float4(x[0], x[1], x[2], x[3]);
+      q[1] = make_float4(x[4], x[5], x[6], x[7]);
     }
   }
   consumer_sync();
 
-  const bool alone = nsplit_b == 1;
-  float* part = p.ws + ((size_t)tile * p.nsplit + split) * tile_elems;
-  for (int e = tid * 4; e < tile_elems; e += kConsumerThreads * 4) {
-    float4 s = *reinterpret_cast<const float4*>(red + e);
-    for (int r = 1; r < p.row_par; ++r) {
-      const float4 x = *reinterpret_cast<const float4*>(red + (size_t)r * tile_elems + e);
-      s.x += x.x; s.y += x.y; s.z += x.z; s.w += x.w;
-    }
-    if (alone) {
-      const int h = e / p.dt, dd = e - h * p.dt;
-      *reinterpret_cast<float4*>(p.out + ((size_t)b * p.Hq + h0 + h) * p.D + d0 + dd) = s;
+  const int ncol4 = tile_elems >> 2;
+  const float4* red4 = reinterpret_cast<const float4*>(red);
+  float4* part = reinterpret_cast<float4*>(p.ws + ((size_t)tile * p.nsplit + split) * tile_elems);
+  for (int col = tid; col < ncol4; col += kConsumerThreads) {
+    float4 sum = red4[col];
+    sum_strided<false>(sum, red4 + col, ncol4, 1, p.row_par);
+    if (nsplit_b == 1) {
+      const int e = col * 4, h = e / p.dt, dd = e - h * p.dt;
+      *reinterpret_cast<float4*>(p.out + ((size_t)b * p.Hq + h0 + h) * p.D + d0 + dd) = sum;
     } else {
-      __stcg(reinterpret_cast<float4*>(part + e), s);
+      __stcg(part + col, sum);
     }
   }
-  if (alone) return;
-
-  // Deterministic split combine: the last CTA of the tile sums in split order.
-  __threadfence();
-  consumer_sync();
-  if (tid == 0) {
-    const unsigned prev = atomicAdd(p.tickets + tile, 1u);
-    s_flag = (prev == static_cast<unsigned>(nsplit_b - 1)) ? 2 : 0;
-  }
-  consumer_sync();
-  if (s_flag != 2) return;
-  __threadfence();
-  const float* base = p.ws + (size_t)tile * p.nsplit * tile_elems;
-  for (int e = tid * 4; e < tile_elems; e += kConsumerThreads * 4) {
-    float4 s = __ldcg(reinterpret_cast<const float4*>(base + e));
-    for (int r = 1; r < nsplit_b; ++r) {
-      const float4 x = __ldcg(reinterpret_cast<const float4*>(base + (size_t)r * tile_elems + e));
-      s.x += x.x; s.y += x.y; s.z += x.z; s.w += x.w;
-    }
-    const int h = e / p.dt, dd = e - h * p.dt;
-    *reinterpret_cast<float4*>(p.out + ((size_t)b * p.Hq + h0 + h) * p.D + d0 + dd) = s;
-  }
-  if (tid == 0) p.tickets[tile] = 0u;
 }
 
-// Launch entry for one (element type, head chunk) instantiation.
+#ifdef GQA_AV_COMBINE_KERNEL  // defined in exactly one translation unit
+// ---------------------------------------------------------------------------
+// The split combine. CTA (tile, column block): `parts` threads per float4
+// column each sum a fixed chunk of the splits (their loads in flight
+// together), then the chunks are added in chunk order.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kCombineThreads)
+gqa_av_combine_kernel(const __grid_constant__ CombineParams p) {
+  __shared__ float4 chunk_sum[kCombineThreads];
+  const int tile = blockIdx.x / p.ctas_per_tile;
+  const int blk = blockIdx.x - tile * p.ctas_per_tile;
+  const int tiles_per_hg = p.B * p.ndt;
+  const int hg = tile / tiles_per_hg;
+  const int rem = tile - hg * tiles_per_hg;
+  const int b = rem / p.ndt;
+  const int dti = rem - b * p.ndt;
+
+  // seq_lens is read before the dependency wait: the main kernel, the only
+  // grid this one depends on, does not write it, and the main kernel started
+  // (and so could trigger this launch) only after everything before it was
+  // done.
+  int L = p.seq_lens ? p.seq_lens[b] : p.Cmax;
+  L = L < 0 ? 0 : (L > p.Cmax ? p.Cmax : L);
+  const int nunit = L > 0 ? (L + p.rows_per_split - 1) / p.rows_per_split : 1;
+  const int ncl = p.nsplit;
+  grid_dependency_wait();  // the partials of the main kernel are complete and visible
+  grid_launch_dependents();
+  if (nunit == 1) return;  // the main kernel wrote this tile's output
+
+  const int ncol4 = p.tile_elems >> 2;
+  const int t = threadIdx.x;
+  const int j = t / p.cols_per_cta;                     // chunk of splits
+  const int col = blk * p.cols_per_cta + (t - j * p.cols_per_cta);
+  const int chunk = (nunit + p.parts - 1) / p.parts;
+  const int lo = j * chunk, hi = min(lo + chunk, nunit);
+  const float4* base = reinterpret_cast<const float4*>(p.ws) + (size_t)tile * ncl * ncol4;
+  float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (col < ncol4 && lo < hi) {
+    sum = __ldcg(base + (size_t)lo * ncol4 + col);
+    sum_strided<true>(sum, base + col, ncol4, lo + 1, hi);
+  }
+  chunk_sum[t] = sum;
+  __syncthreads();
+  if (j == 0 && col < ncol4) {
+    for (int k = 1; k < p.parts && k * chunk < nunit; ++k) add4(sum, chunk_sum[k * p.cols_per_cta + t]);
+    const int e = col * 4, h = e / p.dt, dd = e - h * p.dt;
+    *reinterpret_cast<float4*>(p.out + ((size_t)b * p.Hq + hg * p.heads + h) * p.D +
+                               dti * p.dt + dd) = sum;
+  }
+}
+
+#endif  // GQA_AV_COMBINE_KERNEL
+
+// Launch entry points for one (element type, head chunk) instantiation.
 template <typename Tag, int GC>
 cudaError_t launch(const Params& p, int grid, int smem_bytes, cudaStream_t stream);
 
 template <typename Tag, int GC>
 cudaError_t occupancy(int smem_limit, int smem_bytes, int* ctas_per_sm);
+
+
+cudaError_t launch_combine(const CombineParams& p, int grid, cudaStream_t stream);
 
 }  // namespace gqa_av

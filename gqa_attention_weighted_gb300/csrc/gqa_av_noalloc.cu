@@ -10,17 +10,18 @@
 //   * processes that reserve their whole memory budget up front.
 // gqa_av_decode keeps a growable workspace and may allocate on a call that
 // needs more of it. This entry point instead keeps its scratch (status word,
-// split tickets, split partials) in the fixed file-scope array below, so no
-// call ever allocates.
+// split partials) in the fixed file-scope array below, so no call ever
+// allocates.
 //
 // The array holds GQA_AV_NOALLOC_SCRATCH_BYTES on every GPU that loads this
 // library, until the process exits. Its device address is looked up once per
 // device, by that device's first call, with cudaGetSymbolAddress. Host code
 // must not use the array's name as a device address: on the host that name
 // is a stand-in. All calls on a device share the array and it keeps the last
-// call's contents, so each call clears the status word and split tickets it
-// uses (on its stream) before its kernel starts, and calls that may overlap
-// on the GPU (different streams, no ordering between them) race on it.
+// call's contents, so each call clears the status word (on its stream) before
+// its kernels start; split partials are always written before they are read.
+// Calls that may overlap on the GPU (different streams, no ordering between
+// them) race on it.
 #include <cuda_runtime.h>
 
 #include <map>
@@ -32,16 +33,14 @@ namespace gqa_av {
 int record_error(int status, const char* msg);
 int run_in_scratch(const float* attn, const void* v, const int32_t* seq_lens, float* out, int B,
                    int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode, cudaStream_t stream,
-                   void* scratch, size_t status_bytes, size_t ticket_bytes, size_t scratch_bytes);
+                   void* scratch, size_t status_bytes, size_t scratch_bytes);
 }  // namespace gqa_av
 
 namespace {
 
 constexpr size_t kScratchBytes = GQA_AV_NOALLOC_SCRATCH_BYTES;
-constexpr size_t kStatusBytes = 256;                     // device status word + padding
-constexpr size_t kTicketBytes = GQA_AV_NOALLOC_MAX_TILES * sizeof(unsigned);
-static_assert(kTicketBytes % 256 == 0, "split partials must start 256-byte aligned");
-static_assert(kStatusBytes + kTicketBytes < kScratchBytes, "scratch too small");
+constexpr size_t kStatusBytes = 256;  // device status word + padding; partials follow
+static_assert(kStatusBytes < kScratchBytes, "scratch too small");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
@@ -79,5 +78,5 @@ extern "C" int gqa_av_decode_noalloc(const float* attn, const void* v_cache,
   if (rc) return rc;
   return gqa_av::run_in_scratch(attn, v_cache, seq_lens, out, B, Cmax, Hq, Hkv, D, v_dtype, mode,
                                 static_cast<cudaStream_t>(stream), scratch, kStatusBytes,
-                                kTicketBytes, kScratchBytes);
+                                kScratchBytes);
 }

@@ -109,6 +109,7 @@ typedef struct gqa_av_plan_info {
     int rows_per_stage;
     int stages;
     int nsplit;          /* context splits per tile */
+    int combine_ctas;    /* CTAs of the split-combine kernel (0: not launched) */
     int rows_per_split;
     int tiles;           /* (head groups) x B x (D / dtile) */
     int ctas;            /* tiles x nsplit */
@@ -126,8 +127,9 @@ size_t gqa_av_workspace_bytes(int B, int Cmax, int Hq, int Hkv, int D, int v_dty
 
 /*
  * Hand the library a caller-owned device workspace for the current device
- * (at least gqa_av_workspace_bytes of the largest call, plus 4 KiB). The
- * library zeroes it here (synchronously) and never frees it. ptr == NULL
+ * (at least gqa_av_workspace_bytes of the largest call, 256-byte aligned).
+ * The library zeroes its status word here (synchronously) and never frees it.
+ * ptr == NULL
  * returns to a library-owned workspace. The caller keeps the memory alive
  * until it calls gqa_av_set_workspace(NULL, 0) or the process ends.
  */
@@ -136,8 +138,7 @@ int gqa_av_set_workspace(void *ptr, size_t bytes);
 /*
  * Synchronise `stream`, then read the current device's status word, which
  * kernels set when a bounded wait runs out. Returns GQA_AV_OK or
- * GQA_AV_ERR_DEVICE_TIMEOUT; with clear != 0 the word and the workspace's
- * split counters are reset so later calls start clean.
+ * GQA_AV_ERR_DEVICE_TIMEOUT; with clear != 0 the word is reset.
  */
 int gqa_av_device_status(void *stream, int clear);
 
@@ -149,21 +150,20 @@ int gqa_av_device_status(void *stream, int clear);
  * cudaMalloc/cudaFree, processes with a fixed up-front memory budget.
  *
  * Same arguments, layouts, launch shape and results as gqa_av_decode, but the
- * scratch it needs (status word, split tickets, split partials) lives in one
+ * scratch it needs (status word, split partials) lives in one
  * fixed array of GQA_AV_NOALLOC_SCRATCH_BYTES in this library's device
  * globals, held on every GPU that loads the library until the process exits.
  * No call allocates or frees memory. Set-up: the first call on each device
  * looks up that array's device address (cudaGetSymbolAddress), so make that
  * first call before any stream capture. A shape whose split partials need more
- * than the array holds, or more than GQA_AV_NOALLOC_MAX_TILES split tiles, is
- * rejected with GQA_AV_ERR_UNSUPPORTED and a message; gqa_av_decode handles it.
- * All calls on a device share the array, which keeps the last call's
- * contents: each call clears, on its stream, the status word and tickets it
- * uses. Calls that may overlap on the GPU (unordered streams) race on the
- * array and must not be issued.
+ * than the array holds (8 MiB less its 256-byte status word) is rejected with
+ * GQA_AV_ERR_UNSUPPORTED and a message; gqa_av_decode handles it. All calls on
+ * a device share the array, which keeps the last call's contents: each call
+ * clears the status word on its stream, and every partial is written before
+ * it is read. Calls that may overlap on the GPU (unordered streams) race on
+ * the array and must not be issued.
  */
 #define GQA_AV_NOALLOC_SCRATCH_BYTES (8u << 20) /* 8 MiB */
-#define GQA_AV_NOALLOC_MAX_TILES     4096
 
 int gqa_av_decode_noalloc(const float *attn, const void *v_cache, const int32_t *seq_lens,
                           float *out, int B, int Cmax, int Hq, int Hkv, int D,

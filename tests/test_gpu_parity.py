@@ -133,7 +133,11 @@ def test_lengths_are_clamped_and_null_means_full(gq):
 TUNINGS = [dict(nsplit=1), dict(nsplit=2), dict(nsplit=7), dict(nsplit=1000),
            dict(dtile=64), dict(dtile=32, rows_per_stage=8), dict(stages=2),
            dict(stages=8, rows_per_stage=64), dict(rows_per_stage=256, stages=3),
-           dict(nsplit=5, dtile=8, rows_per_stage=16, stages=4)]
+           dict(nsplit=5, dtile=8, rows_per_stage=16, stages=4),
+           dict(nsplit=16), dict(nsplit=12, dtile=32), dict(nsplit=33, rows_per_stage=32),
+           dict(nsplit=10, dtile=64, rows_per_stage=16),
+           dict(nsplit=3, stages=2, rows_per_stage=128),
+           dict(nsplit=14, dtile=32, stages=4, rows_per_stage=24)]
 
 
 @pytest.mark.parametrize("tuning", TUNINGS, ids=[str(t) for t in TUNINGS])
@@ -212,7 +216,7 @@ def test_caller_supplied_workspace(gq):
     gq.gqa_av_set_workspace(ws)
     try:
         assert_close(run_gpu(gq, attn, v, sl, 1), ref, "caller workspace")
-        small = torch.empty(300 * 1024, dtype=torch.uint8, device="cuda")
+        small = torch.empty(64 * 1024, dtype=torch.uint8, device="cuda")
         gq.gqa_av_set_workspace(small)
         with pytest.raises(gq.GqaAvError) as e:
             run_gpu(gq, attn, v, sl, 1, dict(nsplit=16))
@@ -229,4 +233,4 @@ def test_plan_reports_the_launch(gq):
     q = gq.gqa_av_plan(1, 8192, 32, 32, 128, 0, -1)
     assert q["mode"] == 0 and q["heads_per_cta"] == 1
     r = gq.gqa_av_plan(8, 32768, 16, 1, 256, 1, -1)
-    assert r["heads_per_cta"] == 16 and r["head_chunk"] == 16
+    assert r["heads_per_cta"] == 16 and r["head_chunk"] == 8
