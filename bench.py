@@ -258,9 +258,12 @@ def run_gpu(args, rank, world, local):
                      "peak_kind": f"{peak_kind} hbm_gbs (copy)",
                      "frac_of_8tbs_nominal": round(achieved / 8000.0, 4),
                      "traffic": committed_traffic(w.name, plan["mode"]),
-                     "kernel": "gqa_av_kernel", "kernel_hash": kernel_hash()},
+                     "kernel": "gqa_av_kernel", "kernel_hash": kernel_hash(),
+                     "duration": "average time of one whole call (main kernel and, when the "
+                                 "context is split, the split-combine kernel) over the timed "
+                                 "region; the main kernel alone is shorter"},
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if plan["combine_ctas"] else 1),
         "clocks": clk.summary(),
     }
     if cpu is not None:
