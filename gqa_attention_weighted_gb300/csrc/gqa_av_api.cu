@@ -88,6 +88,7 @@ bool pick_kernel(int v_dtype, int gc, Kernel* k) {
 struct DeviceInfo {
   int sms = 0;
   int smem_optin = 0;
+  int smem_per_sm = 0;
   bool ok = false;
 };
 
@@ -106,6 +107,8 @@ int device_info(int dev, DeviceInfo* out) {
   cudaError_t e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess)
     e = cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&di.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
   if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
   di.ok = true;
   g_devices[dev] = di;
@@ -138,6 +141,9 @@ struct Plan {
   int mode, heads, gc, nc, dt, ndt, ct, row_par, R, stages, nsplit, rows_per_split;
   int hgroups, tiles, ap, avec, smem, occ;
   int parts, cols_per_cta, ctas_per_tile;  // split combine launch (nsplit > 1)
+  int one_per_sm;                          // shared memory padded so one CTA fits per SM
+  int early;                               // stages issued before the length is read
+  int attn_tma;                            // attn weights by TMA (rows of Hq % 4 == 0 floats)
   uint32_t v_stage_bytes, a_off, bar_off;
   size_t ws_bytes;  // partials only
 };
@@ -157,14 +163,14 @@ int check_shape(int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode) 
 }
 
 // Shared memory of a plan: [V ring | reduction buffer] [attn ring] [mbarriers] [flag].
-void layout(Plan* p) {
+void layout(Plan* p, int min_smem = 0) {
   p->v_stage_bytes = static_cast<uint32_t>(p->R) * p->dt * 2;
   const size_t vring = static_cast<size_t>(p->stages) * p->v_stage_bytes;
   const size_t red = static_cast<size_t>(p->row_par) * p->heads * p->dt * 4;
   p->a_off = static_cast<uint32_t>(align_up(std::max(vring, red), 128));
   const size_t aring = static_cast<size_t>(p->stages) * p->R * p->ap * 4;
   p->bar_off = static_cast<uint32_t>(align_up(p->a_off + aring, 16));
-  p->smem = static_cast<int>(p->bar_off + 2 * kMaxStages * 8 + 16);
+  p->smem = std::max(static_cast<int>(p->bar_off + 2 * kMaxStages * 8 + 16), min_smem);
 }
 
 int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode,
@@ -190,77 +196,95 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
                 t->dtile, D);
   p->dt = 0;
   for (int dt = std::min(want_dt, std::min(D, 256)); dt >= 8; dt -= 8)
-    if (D % dt == 0 && (dt / 8) * p->nc <= kConsumerThreads) { p->dt = dt; break; }
+    if (D % dt == 0 && (dt / 8) * p->nc <= 32 * consumer_warps(p->gc)) { p->dt = dt; break; }
   if (!p->dt)
     return fail(GQA_AV_ERR_UNSUPPORTED, "no column tile fits G=%d heads per CTA", p->heads);
   p->ndt = D / p->dt;
   p->ct = p->dt / 8;
-  p->row_par = kConsumerThreads / (p->ct * p->nc);
+  p->row_par = 32 * consumer_warps(p->gc) / (p->ct * p->nc);
 
-  // Rows per stage: about 8 KiB of V per stage, a multiple of 8 rows.
+  // Context splits. With fewer tiles than SMs the grid is one wave of one CTA
+  // per SM (shared memory is padded to more than half an SM so no SM takes
+  // two); with many tiles it runs in waves (a split with no context exits at
+  // once) and splits only balance ragged lengths.
+  p->tiles = p->hgroups * B * p->ndt;
+  const bool one_wave = !(t && t->nsplit > 0) && p->tiles < di.sms;
+  long long want;
+  if (t && t->nsplit > 0) {
+    want = t->nsplit;
+  } else if (one_wave) {
+    want = di.sms / p->tiles;
+  } else {
+    const double v_bytes = static_cast<double>(B) * Cmax * (p->heads == 1 ? Hq : Hkv) * D * 2;
+    const int waves = v_bytes > 256e6 ? 4 : 1;
+    // Occupancy is not known yet: assume two CTAs per SM for the wave size.
+    want = (2LL * di.sms * waves + p->tiles - 1) / p->tiles;
+  }
+  want = std::max<long long>(1, std::min<long long>(want, (Cmax + 7) / 8));
+  const int rps0 = static_cast<int>((Cmax + want - 1) / want);
+
+  // Rows per stage: about 32 KiB of V per TMA box (large boxes stream faster
+  // per SM), a multiple of 8 rows, dividing the split into equal stages.
+  int iters;
   if (t && t->rows_per_stage > 0) {
     if (t->rows_per_stage % 8 || t->rows_per_stage > 256)
       return fail(GQA_AV_ERR_INVALID, "rows_per_stage=%d must be a multiple of 8, <= 256",
                   t->rows_per_stage);
     p->R = t->rows_per_stage;
+    iters = (rps0 + p->R - 1) / p->R;
   } else {
-    // About 32 KiB of V per stage (large TMA boxes stream faster per SM), but
-    // short enough that a short context still splits across every SM.
-    p->R = std::max(8, std::min(256, 32768 / (2 * p->dt)));
-    const long long tiles = static_cast<long long>(Hq / p->heads) * B * (D / p->dt);
-    if (tiles < di.sms) {
-      const long long want = (di.sms + tiles - 1) / tiles;  // splits that reach every SM
-      p->R = static_cast<int>(std::min<long long>(p->R, std::max<long long>(8, Cmax / (2 * want))));
-    }
-    p->R = std::min(p->R, static_cast<int>(align_up(Cmax, 8)));
-    p->R = std::max(8, p->R / 8 * 8);
+    const int rmax = std::max(8, std::min(256, 32768 / (2 * p->dt)) / 8 * 8);
+    iters = (rps0 + rmax - 1) / rmax;
+    p->R = static_cast<int>(align_up((rps0 + iters - 1) / iters, 8));
   }
+  p->rows_per_split = p->R * iters;
+  p->nsplit = (Cmax + p->rows_per_split - 1) / p->rows_per_split;
+  if (static_cast<long long>(p->tiles) * p->nsplit > 0x7fffffffLL)
+    return fail(GQA_AV_ERR_UNSUPPORTED, "grid too large");
+
   if (t && t->stages > 0) {
     if (t->stages < 2 || t->stages > kMaxStages)
       return fail(GQA_AV_ERR_INVALID, "stages=%d must be in [2, %d]", t->stages, kMaxStages);
     p->stages = t->stages;
   } else {
-    p->stages = 3;
+    p->stages = std::max(2, std::min(3, iters));
   }
-  p->ap = static_cast<int>(align_up(p->heads, 4));
-  layout(p);
+  // attn weights of a stage. By TMA when attn rows are 16-byte multiples
+  // (Hq % 4 == 0): the box starts at the 4-aligned head at or below the CTA's
+  // first head (a TMA box must start 16-byte aligned) and is wide enough for
+  // every CTA's heads; otherwise by cp.async, `avec` floats a copy.
+  const int max_off = p->heads % 4 == 0 ? 0 : (p->heads % 2 == 0 ? 2 : 3);
+  const int aw = static_cast<int>(align_up(p->heads + max_off, 4));
+  p->attn_tma = Hq % 4 == 0 && aw <= 256;
+  p->ap = p->attn_tma ? aw : static_cast<int>(align_up(p->heads, 4));
+  p->avec = 1;
+  if (Hq % 4 == 0 && p->heads % 4 == 0) p->avec = 4;
+  else if (Hq % 2 == 0 && p->heads % 2 == 0) p->avec = 2;
+  p->one_per_sm = one_wave && static_cast<long long>(p->tiles) * p->nsplit <= di.sms;
+  const int min_smem = p->one_per_sm ? di.smem_per_sm / 2 + 1024 : 0;
+  layout(p, min_smem);
   while (p->smem > di.smem_optin && p->stages > 2 && !(t && t->stages > 0)) {
     --p->stages;
-    layout(p);
+    layout(p, min_smem);
   }
   if (p->smem > di.smem_optin)
     return fail(GQA_AV_ERR_UNSUPPORTED, "plan needs %d B of shared memory (limit %d)", p->smem,
                 di.smem_optin);
-
-  p->avec = 1;
-  if (Hq % 4 == 0 && p->heads % 4 == 0) p->avec = 4;
-  else if (Hq % 2 == 0 && p->heads % 2 == 0) p->avec = 2;
+  // One stage goes out before the length is read: issuing the whole ring
+  // early delays the first stage behind the others (measured slower on a
+  // one-wave Llama-size grid), and a CTA past its length reads it for nothing.
+  if (t && t->early_stages > 0) {
+    if (t->early_stages > p->stages)
+      return fail(GQA_AV_ERR_INVALID, "early_stages=%d must be in [1, stages=%d]",
+                  t->early_stages, p->stages);
+    p->early = t->early_stages;
+  } else {
+    p->early = 1;
+  }
 
   if ((rc = ctas_per_sm(dev, di.smem_optin, v_dtype, p->gc, p->smem, &p->occ))) return rc;
   if (p->occ < 1) return fail(GQA_AV_ERR_UNSUPPORTED, "kernel does not fit on an SM");
 
-  // Context splits: with fewer tiles than SMs the grid is one wave whose
-  // splits cover every SM; with many tiles it runs in waves (a split with no
-  // context exits at once) and splits only balance ragged lengths.
-  p->tiles = p->hgroups * B * p->ndt;
-  const int max_split = std::max(1, Cmax / (2 * p->R));  // at least two stages of rows
-  const long long wave = static_cast<long long>(di.sms) * p->occ;
-  int nsplit;
-  if (t && t->nsplit > 0) {
-    nsplit = std::min(t->nsplit, (Cmax + p->R - 1) / p->R);
-  } else if (p->tiles < di.sms) {
-    nsplit = static_cast<int>(std::min<long long>(max_split, di.sms / p->tiles));
-  } else {
-    const double v_bytes = static_cast<double>(B) * Cmax * (p->heads == 1 ? Hq : Hkv) * D * 2;
-    const int waves = v_bytes > 256e6 ? 4 : 1;
-    nsplit = static_cast<int>(std::min<long long>(
-        max_split, std::max<long long>(1, (wave * waves + p->tiles - 1) / p->tiles)));
-  }
-  nsplit = std::max(1, nsplit);
-  p->rows_per_split = static_cast<int>(align_up((Cmax + nsplit - 1) / nsplit, p->R));
-  p->nsplit = (Cmax + p->rows_per_split - 1) / p->rows_per_split;
-  if (static_cast<long long>(p->tiles) * p->nsplit > 0x7fffffffLL)
-    return fail(GQA_AV_ERR_UNSUPPORTED, "grid too large");
   p->ws_bytes = p->nsplit > 1
                     ? static_cast<size_t>(p->tiles) * p->nsplit * p->heads * p->dt * sizeof(float)
                     : 0;
@@ -286,10 +310,13 @@ void fill_params(Params* p, const Plan& pl, const float* attn, const int32_t* se
   p->heads = pl.heads; p->hgroups = pl.hgroups; p->dt = pl.dt; p->ndt = pl.ndt; p->ct = pl.ct;
   p->nc = pl.nc; p->row_par = pl.row_par; p->R = pl.R; p->stages = pl.stages;
   p->rows_per_split = pl.rows_per_split; p->nsplit = pl.nsplit;
-  p->ap = pl.ap; p->avec = pl.avec;
+  p->early_stages = pl.early;
+  p->ap = pl.ap; p->avec = pl.avec; p->attn_tma = pl.attn_tma;
+  p->a_stage_bytes = static_cast<uint32_t>(pl.R) * pl.ap * 4;
   p->v_stage_bytes = pl.v_stage_bytes; p->a_off = pl.a_off; p->bar_off = pl.bar_off;
   p->timeout_ns = kWaitTimeoutNs;
-  if (pl.avec > 1 && (reinterpret_cast<uintptr_t>(attn) & (4 * pl.avec - 1))) p->avec = 1;
+  // attn is 16-byte aligned (checked before planning): a TMA source or a
+  // cp.async of up to 16 bytes can start at any 4-head boundary of it.
 }
 
 // Launches the main kernel and, when the tile has several splits, the split
@@ -397,6 +424,22 @@ int encode_v_map(CUtensorMap* m, const void* v, int B, int Cmax, int Hkv, int D,
   return GQA_AV_OK;
 }
 
+// attn viewed as 3-D {Hq, Cmax, B} (innermost first); box {width, R, 1}.
+int encode_attn_map(CUtensorMap* m, const float* attn, int B, int Cmax, int Hq, int width, int R) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  int rc = encode_fn(&enc);
+  if (rc) return rc;
+  const cuuint64_t dims[3] = {(cuuint64_t)Hq, (cuuint64_t)Cmax, (cuuint64_t)B};
+  const cuuint64_t strides[2] = {(cuuint64_t)Hq * 4, (cuuint64_t)Cmax * Hq * 4};
+  const cuuint32_t box[3] = {(cuuint32_t)width, (cuuint32_t)R, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(attn), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(GQA_AV_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled (attn) failed (%d)", (int)r);
+  return GQA_AV_OK;
+}
+
 int current_device(int* dev) {
   cudaError_t e = cudaGetDevice(dev);
   return e == cudaSuccess ? GQA_AV_OK : fail_cuda(e, "cudaGetDevice");
@@ -426,6 +469,7 @@ int run(const float* attn, const void* v, const int32_t* seq_lens, float* out, i
   if ((rc = encode_v_map(&p.v_map, v, B, Cmax, Hkv, D, pl.dt, pl.R))) return rc;
   char* wsb = static_cast<char*>(ws.base);
   fill_params(&p, pl, attn, seq_lens, out, wsb, wsb + kHeaderBytes, B, Cmax, Hq, Hkv, D);
+  if (p.attn_tma && (rc = encode_attn_map(&p.a_map, attn, B, Cmax, Hq, pl.ap, pl.R))) return rc;
 
   Kernel kern;
   if (!pick_kernel(v_dtype, pl.gc, &kern)) return fail(GQA_AV_ERR_UNSUPPORTED, "no kernel");
@@ -494,12 +538,13 @@ int gqa_av_plan(int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode,
   info->dtile = p.dt;
   info->rows_per_stage = p.R;
   info->stages = p.stages;
+  info->early_stages = p.early;
   info->nsplit = p.nsplit;
   info->combine_ctas = p.nsplit > 1 ? p.tiles * p.ctas_per_tile : 0;
   info->rows_per_split = p.rows_per_split;
   info->tiles = p.tiles;
   info->ctas = p.tiles * p.nsplit;
-  info->threads_per_cta = kThreads;
+  info->threads_per_cta = cta_threads(p.gc);
   info->smem_bytes = p.smem;
   info->ctas_per_sm = p.occ;
   info->workspace_bytes = kHeaderBytes + p.ws_bytes;
@@ -623,6 +668,7 @@ int run_in_scratch(const float* attn, const void* v, const int32_t* seq_lens, fl
   memset(&p, 0, sizeof p);
   if ((rc = encode_v_map(&p.v_map, v, B, Cmax, Hkv, D, pl.dt, pl.R))) return rc;
   fill_params(&p, pl, attn, seq_lens, out, base, base + status_bytes, B, Cmax, Hq, Hkv, D);
+  if (p.attn_tma && (rc = encode_attn_map(&p.a_map, attn, B, Cmax, Hq, pl.ap, pl.R))) return rc;
 
   Kernel kern;
   if (!pick_kernel(v_dtype, pl.gc, &kern)) return fail(GQA_AV_ERR_UNSUPPORTED, "no kernel");

@@ -13,7 +13,7 @@ template <typename Tag, int GC>
 cudaError_t launch(const Params& p, int grid, int smem_bytes, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(cta_threads(GC));
   cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -33,7 +33,7 @@ cudaError_t occupancy(int smem_limit, int smem_bytes, int* ctas_per_sm) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem_limit);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, gqa_av_kernel<Tag, GC>,
-                                                       kThreads, smem_bytes);
+                                                       cta_threads(GC), smem_bytes);
 }
 
 #define GQA_AV_INSTANTIATE(TAG, GC)                                                      \

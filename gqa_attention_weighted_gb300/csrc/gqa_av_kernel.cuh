@@ -11,10 +11,12 @@
 //
 // Warp roles:
 //   * producer (warp kConsumerWarps): lane 0 streams V rows with 4-D TMA
-//     tensor loads into a multi-stage shared-memory ring; all 32 lanes copy the
-//     matching attn weights with cp.async. Both signal one "full" mbarrier per
-//     stage; a slot is refilled once every consumer warp has released it
-//     ("empty" mbarrier). Stage 0 is issued before the sequence length is read.
+//     tensor loads into a multi-stage shared-memory ring, and their attn
+//     weights with a 3-D TMA box (head groups of a multiple of 4 heads) or,
+//     otherwise, by cp.async from all 32 lanes. Both signal one "full"
+//     mbarrier per stage; a slot is refilled once every consumer warp has
+//     released it ("empty" mbarrier). The first stage(s) are issued before the
+//     sequence length is read.
 //   * consumers (warps 0..kConsumerWarps-1): thread t owns 8 adjacent output
 //     columns of one head chunk and a row slot; for every V row of its slot it
 //     widens 8 bf16/fp16 values to fp32 and does GC x 8 FMAs (packed f32x2,
@@ -40,9 +42,13 @@
 
 namespace gqa_av {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kThreads = kConsumerThreads + 32;  // + the producer warp
+// Consumer warps per CTA. A sub-partition's register file is shared by its
+// warps: with the producer warp, 13 warps put 4 on one sub-partition and leave
+// 128 registers a thread (enough up to 8 heads a thread; 12 heads need the 168
+// that 9 warps leave). Measured on the Llama-size shape: 12 consumer warps
+// beat 8, 11 and 15.
+__host__ __device__ constexpr int consumer_warps(int gc) { return gc >= 12 ? 8 : 12; }
+__host__ __device__ constexpr int cta_threads(int gc) { return 32 * (consumer_warps(gc) + 1); }
 constexpr int kMaxStages = 8;
 constexpr int kCombineThreads = 256;
 
@@ -53,6 +59,7 @@ constexpr unsigned kErrDrain = 4u;
 
 struct alignas(64) Params {
   CUtensorMap v_map;            // V as 4-D {D, Hkv, Cmax, B}; box {dt, 1, R, 1}
+  CUtensorMap a_map;            // attn as 3-D {Hq, Cmax, B}; box {ap, R, 1} (when attn_tma)
   const float* attn;            // [B, Cmax, Hq]
   const int32_t* seq_lens;      // [B] or null
   float* out;                   // [B, Hq, D]
@@ -72,9 +79,12 @@ struct alignas(64) Params {
   int nsplit;                   // context splits per tile
   int ap;                       // floats per attn row in shared memory
   int avec;                     // floats per attn cp.async (1, 2 or 4)
+  int attn_tma;                 // attn weights by TMA (Hq % 4 == 0) instead of cp.async
+  uint32_t a_stage_bytes;       // R * ap * 4
   uint32_t v_stage_bytes;       // R * dt * 2
   uint32_t a_off;               // shared-memory offset of the attn ring
   uint32_t bar_off;             // shared-memory offset of the mbarriers
+  int early_stages;             // stages issued before the sequence length is read (>= 1)
   long long timeout_ns;         // bound on every mbarrier wait
 };
 
@@ -165,6 +175,16 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// 3-D tiled TMA load global -> shared, completion counted on `bar` in bytes.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x0, int x1,
+                                            int x2, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x0), "r"(x1), "r"(x2), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ uint64_t evict_first_policy() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -191,6 +211,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
 }
 
 // Named barrier of the consumer warps only (the producer warp does not join).
+template <int kConsumerThreads>
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
 }
@@ -281,8 +302,10 @@ __device__ __forceinline__ void ffma2(uint64_t& acc, uint64_t w2, uint64_t v2) {
 // The main kernel. Tag selects the V element type, GC the heads per thread.
 // ---------------------------------------------------------------------------
 template <typename Tag, int GC>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(cta_threads(GC), 1)
 gqa_av_kernel(const __grid_constant__ Params p) {
+  constexpr int kConsumerWarps = consumer_warps(GC);
+  constexpr int kConsumerThreads = kConsumerWarps * 32;
   extern __shared__ __align__(128) uint8_t smem[];
 
   const int tid = threadIdx.x;
@@ -302,6 +325,13 @@ gqa_av_kernel(const __grid_constant__ Params p) {
   const int d0 = dti * p.dt;
   const int c_begin = split * p.rows_per_split;  // < Cmax for every launched split
   const int tile_elems = p.heads * p.dt;
+  // A TMA attn box starts at the 4-aligned head at or below h0; the CTA's
+  // weights sit a_shift floats into each row of the stage.
+  const int a_shift = p.attn_tma ? (h0 & 3) : 0;
+  // Stages the producer issues before it knows the sequence length (>= 1,
+  // each in its own ring slot, all inside [0, Cmax)).
+  const int pre = min(min(min(p.early_stages, p.stages), p.rows_per_split / p.R),
+                      (p.Cmax - c_begin + p.R - 1) / p.R);
 
   uint8_t* vring = smem;
   float* aring = reinterpret_cast<float*>(smem + p.a_off);
@@ -312,14 +342,24 @@ gqa_av_kernel(const __grid_constant__ Params p) {
 
   if (tid == 0) {
     for (int s = 0; s < p.stages; ++s) {
-      mbar_init(full0 + 8 * s, 1 + 32);           // expect_tx arrival + 32 cp.async arrivals
+      // expect_tx arrival (+ 32 cp.async arrivals when attn is copied by lanes)
+      mbar_init(full0 + 8 * s, p.attn_tma ? 1 : 1 + 32);
       mbar_init(empty0 + 8 * s, kConsumerWarps);  // one arrival per consumer warp
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_flag = 0;
   }
-  if (warp == kConsumerWarps && lane == 0)  // a kernel parameter: fetch it during the wait
+  if (warp == kConsumerWarps && lane == 0) {  // kernel parameters: fetch them during the wait
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.v_map)) : "memory");
+    if (p.attn_tma)
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.a_map)) : "memory");
+  }
+  // Producer state that depends on kernel parameters only, ready before the wait.
+  const uint64_t policy = evict_first_policy();
+  const float* attn_b = p.attn + (size_t)b * p.Cmax * p.Hq + h0;
+  const int per_row = p.heads / p.avec;
+  const uint32_t vring_s = smem_addr(vring);
+  const uint32_t aring_s = smem_addr(aring);
   __syncthreads();
 
   // Nothing written by earlier kernels is touched before they are done.
@@ -328,19 +368,27 @@ gqa_av_kernel(const __grid_constant__ Params p) {
 
   if (warp == kConsumerWarps) {
     // ----------------------------------------------------------------- producer
-    const uint64_t policy = evict_first_policy();
-    const float* attn_b = p.attn + (size_t)b * p.Cmax * p.Hq + h0;
-    const int per_row = p.heads / p.avec;
-    // V rows [c0, c0 + R) by TMA; attn weights of the first `rows` of them by cp.async.
+    // V rows [c0, c0 + R) by TMA; their attn weights by a second TMA box, or
+    // (unaligned head groups) the weights of the first `rows` of them by cp.async.
     auto issue = [&](int stage, int c0, int rows) {
       const uint32_t full = full0 + 8 * stage;
+      if (p.attn_tma) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(full, p.v_stage_bytes + p.a_stage_bytes);
+          tma_load_4d(vring_s + (uint32_t)stage * p.v_stage_bytes, &p.v_map, d0, kv_h, c0, b, full,
+                      policy);
+          tma_load_3d(aring_s + (uint32_t)stage * p.a_stage_bytes, &p.a_map, h0 - a_shift, c0, b,
+                      full, policy);
+        }
+        return;
+      }
       if (lane == 0) {
         mbar_arrive_expect_tx(full, p.v_stage_bytes);
-        tma_load_4d(smem_addr(vring + (size_t)stage * p.v_stage_bytes), &p.v_map, d0, kv_h, c0, b,
-                    full, policy);
+        tma_load_4d(vring_s + (uint32_t)stage * p.v_stage_bytes, &p.v_map, d0, kv_h, c0, b, full,
+                    policy);
       }
       const float* src = attn_b + (size_t)c0 * p.Hq;
-      const uint32_t dst = smem_addr(aring + (size_t)stage * p.R * p.ap);
+      const uint32_t dst = aring_s + 4u * (uint32_t)(stage * p.R * p.ap);
       const int n = rows * per_row;
       for (int i = lane; i < n; i += 32) {
         const int r = i / per_row, k = (i - r * per_row) * p.avec;
@@ -352,23 +400,27 @@ gqa_av_kernel(const __grid_constant__ Params p) {
       }
       cp_async_arrive_noinc(full);
     };
-    // Stage 0 goes out before the sequence length is known; its rows lie
-    // inside [0, Cmax) whatever the length is.
-    issue(0, c_begin, min(p.R, p.Cmax - c_begin));
-
+    // The first `pre` stages go out before the sequence length is known
+    // (rows past the length are read for nothing, but they lie inside
+    // [0, Cmax)); the length load is issued before them and returns while
+    // they stream.
     int L = p.seq_lens ? p.seq_lens[b] : p.Cmax;
+    issue(0, c_begin, min(p.R, p.Cmax - c_begin));
+    for (int it = 1; it < pre; ++it) {
+      const int c0 = c_begin + it * p.R;
+      issue(it, c0, min(p.R, p.Cmax - c0));
+    }
     L = L < 0 ? 0 : (L > p.Cmax ? p.Cmax : L);
     const int nsplit_b = L > 0 ? (L + p.rows_per_split - 1) / p.rows_per_split : 1;
-    if (split >= nsplit_b) {
-      // No context for this split: let the early stage land, then leave.
-      if (!mbar_wait(full0, 0, p.timeout_ns) && lane == 0) atomicOr(p.status, kErrDrain);
-      return;
-    }
+    // Stages the consumers take: none for a split past the context (its
+    // consumers leave at once), else every stage holding context (at least
+    // one, as the first split of an empty context writes zeros).
     const int c_end = min(c_begin + p.rows_per_split, L);
-    const int n_iters = c_end > c_begin ? (c_end - c_begin + p.R - 1) / p.R : 0;
-    int issued = 1;
+    const int n_iters =
+        split < nsplit_b ? max((c_end - c_begin + p.R - 1) / p.R, 1) : 0;
+    int issued = pre;
     bool ok = true;
-    for (int it = 1; it < n_iters; ++it) {
+    for (int it = pre; it < n_iters; ++it) {
       const int stage = it % p.stages;
       const uint32_t parity = ((it / p.stages) & 1) ^ 1;
       if (!mbar_wait(empty0 + 8 * stage, parity, p.timeout_ns)) {
@@ -387,6 +439,9 @@ gqa_av_kernel(const __grid_constant__ Params p) {
         if (!mbar_wait(full0 + 8 * (it % p.stages), (it / p.stages) & 1, p.timeout_ns))
           atomicOr(p.status, kErrDrain);
     }
+    // Early stages the consumers do not take: let them land before leaving.
+    for (int it = n_iters; it < pre; ++it)
+      if (!mbar_wait(full0 + 8 * it, 0, p.timeout_ns) && lane == 0) atomicOr(p.status, kErrDrain);
     return;
   }
 
@@ -394,10 +449,10 @@ gqa_av_kernel(const __grid_constant__ Params p) {
   int L = p.seq_lens ? p.seq_lens[b] : p.Cmax;
   L = L < 0 ? 0 : (L > p.Cmax ? p.Cmax : L);
   const int nsplit_b = L > 0 ? (L + p.rows_per_split - 1) / p.rows_per_split : 1;
-  if (split >= nsplit_b) return;  // the producer waits for the early stage
+  if (split >= nsplit_b) return;  // the producer waits for the early stages
   const int c_end = min(c_begin + p.rows_per_split, L);
   const int n_iters = c_end > c_begin ? (c_end - c_begin + p.R - 1) / p.R : 0;
-  const int n_stages = max(n_iters, 1);  // stages issued, counting the early one
+  const int n_stages = max(n_iters, 1);  // stages taken, counting the first one
 
   const int slots = p.ct * p.nc;
   const int my_col = tid % p.ct;
@@ -423,9 +478,9 @@ gqa_av_kernel(const __grid_constant__ Params p) {
     const int rows = min(p.R, c_end - (c_begin + it * p.R));
     const uint16_t* vst =
         reinterpret_cast<const uint16_t*>(vring + (size_t)stage * p.v_stage_bytes) + my_col * 8;
-    const float* ast = aring + (size_t)stage * p.R * p.ap + my_chunk * GC;
+    const float* ast = aring + (size_t)stage * p.R * p.ap + a_shift + my_chunk * GC;
     if (active) {
-#pragma unroll 2
+#pragma unroll 4
       for (int r = my_slot; r < rows; r += p.row_par) {
         const uint4 raw = *reinterpret_cast<const uint4*>(vst + (size_t)r * p.dt);
         float v[8];
@@ -446,8 +501,14 @@ gqa_av_kernel(const __grid_constant__ Params p) {
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * stage);
   }
+  // The ring is reused below: early stages past the context must have landed.
+  for (int it = n_stages; it < pre && ok; ++it)
+    if (!mbar_wait(full0 + 8 * it, 0, p.timeout_ns)) {
+      atomicOr(p.status, kErrFullWait);
+      ok = false;
+    }
   if (!ok) s_flag = 1;
-  consumer_sync();
+  consumer_sync<kConsumerThreads>();
   if (s_flag) return;  // the producer drains the loads it issued
 
   // Row slots -> this CTA's partial: every slot writes its accumulators to its
@@ -466,7 +527,7 @@ gqa_av_kernel(const __grid_constant__ Params p) {
       q[1] = make_float4(x[4], x[5], x[6], x[7]);
     }
   }
-  consumer_sync();
+  consumer_sync<kConsumerThreads>();
 
   const int ncol4 = tile_elems >> 2;
   const float4* red4 = reinterpret_cast<const float4*>(red);

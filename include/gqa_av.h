@@ -85,15 +85,19 @@ int gqa_av_decode_per_head(const float *attn, const void *v_cache, const int32_t
  * Launch-shape overrides for sweeps and tests. A field <= 0 keeps the
  * library's choice. nsplit: context splits per tile; dtile: output columns
  * per CTA (a multiple of 8 dividing D, <= 256); rows_per_stage: V rows per
- * pipeline stage (8..256); stages: pipeline depth (2..8). Results stay within
- * the stated tolerance for every choice, and are bitwise reproducible for a
- * fixed choice.
+ * pipeline stage (8..256); stages: pipeline depth (2..8); early_stages:
+ * stages each CTA issues before it has read its sequence length (1..stages;
+ * the library issues one, since rows past a length are read for nothing and
+ * the first stage lands later behind the others). Results stay within the
+ * stated tolerance for every choice, and are bitwise reproducible for a fixed
+ * choice.
  */
 typedef struct gqa_av_tuning {
     int nsplit;
     int dtile;
     int rows_per_stage;
     int stages;
+    int early_stages;
 } gqa_av_tuning;
 
 int gqa_av_decode_tuned(const float *attn, const void *v_cache, const int32_t *seq_lens,
@@ -108,6 +112,7 @@ typedef struct gqa_av_plan_info {
     int dtile;           /* output columns per CTA */
     int rows_per_stage;
     int stages;
+    int early_stages;    /* stages issued before the sequence length is read */
     int nsplit;          /* context splits per tile */
     int combine_ctas;    /* CTAs of the split-combine kernel (0: not launched) */
     int rows_per_split;

@@ -137,7 +137,10 @@ TUNINGS = [dict(nsplit=1), dict(nsplit=2), dict(nsplit=7), dict(nsplit=1000),
            dict(nsplit=16), dict(nsplit=12, dtile=32), dict(nsplit=33, rows_per_stage=32),
            dict(nsplit=10, dtile=64, rows_per_stage=16),
            dict(nsplit=3, stages=2, rows_per_stage=128),
-           dict(nsplit=14, dtile=32, stages=4, rows_per_stage=24)]
+           dict(nsplit=14, dtile=32, stages=4, rows_per_stage=24),
+           dict(early_stages=1), dict(stages=3, early_stages=2),
+           dict(nsplit=7, stages=4, early_stages=4), dict(nsplit=16, early_stages=2),
+           dict(nsplit=2, rows_per_stage=64, stages=8, early_stages=8)]
 
 
 @pytest.mark.parametrize("tuning", TUNINGS, ids=[str(t) for t in TUNINGS])
@@ -189,6 +192,45 @@ def test_output_guard_regions_untouched(gq):
         assert torch.all(buf[:guard] == 12345.0) and torch.all(buf[guard + n:] == 12345.0)
 
 
+@pytest.mark.parametrize("G", [1, 2, 3, 5, 6, 7])
+def test_attn_boxes_for_unaligned_head_groups(gq, G):
+    # Hq a multiple of 4 with head groups of any size: the attn TMA box starts
+    # at the 4-aligned head below each group (shifts 0..3).
+    rng = np.random.default_rng(40 + G)
+    Hkv = 4
+    B, C, Hq, D = 2, 700, G * Hkv, 64
+    attn, v, sl = rand_case(rng, B, C, Hq, Hkv, D, "bf16", [700, 333])
+    ref = run_oracle(attn, v, sl, "bf16")
+    for mode in (0, 1):
+        assert_close(run_gpu(gq, attn, v, sl, mode), ref, f"G={G} mode={mode}")
+
+
+@pytest.mark.parametrize("shift", [1, 2, 4])
+def test_attn_pointer_alignment(gq, shift):
+    # attn starting `shift` floats into its allocation: a start that is not
+    # 16-byte aligned is rejected before any launch; a 16-byte one works.
+    rng = np.random.default_rng(50 + shift)
+    B, C, Hq, Hkv, D = 2, 500, 24, 8, 128
+    attn, v, sl = rand_case(rng, B, C, Hq, Hkv, D, "bf16", [500, 250])
+    ref = run_oracle(attn, v, sl, "bf16")
+    dev = torch.device("cuda")
+    store = torch.zeros(attn.numel() + 8, dtype=torch.float32, device=dev)
+    a = store[shift:shift + attn.numel()].view(attn.shape)
+    a.copy_(attn.to(dev))
+    for mode in (0, 1):
+        out = torch.full((B, Hq, D), 7.0, device=dev)
+        if shift % 4:
+            with pytest.raises(gq.GqaAvError) as e:
+                gq.gqa_av_decode(a, v.to(dev), sl.to(dev), out, mode=mode)
+            assert e.value.status == 2
+            torch.cuda.synchronize()
+            assert torch.all(out == 7.0)
+        else:
+            gq.gqa_av_decode(a, v.to(dev), sl.to(dev), out, mode=mode)
+            gq.gqa_av_device_status()
+            assert_close(out.cpu().double().numpy(), ref, f"shift={shift} mode={mode}")
+
+
 def test_invalid_calls_launch_nothing(gq):
     dev = torch.device("cuda")
     attn = torch.zeros((1, 16, 6), device=dev)
@@ -202,8 +244,16 @@ def test_invalid_calls_launch_nothing(gq):
     with pytest.raises(gq.GqaAvError) as e:
         gq.gqa_av_decode(attn, v12, None, out12)
     assert e.value.status == 2
+    attn8 = torch.zeros((1, 16, 8), device=dev)
+    v8 = torch.zeros((1, 16, 2, 64), dtype=torch.bfloat16, device=dev)
+    out8 = torch.full((1, 8, 64), 7.0, device=dev)
+    for bad in (dict(stages=9), dict(stages=1), dict(rows_per_stage=7), dict(dtile=12),
+                dict(stages=2, early_stages=3)):
+        with pytest.raises(gq.GqaAvError) as e:
+            gq.gqa_av_decode_tuned(attn8, v8, None, out8, mode=1, tuning=bad)
+        assert e.value.status == 1, bad
     torch.cuda.synchronize()
-    assert torch.all(out == 7.0) and torch.all(out12 == 7.0)
+    assert torch.all(out == 7.0) and torch.all(out12 == 7.0) and torch.all(out8 == 7.0)
 
 
 def test_caller_supplied_workspace(gq):
@@ -216,7 +266,8 @@ def test_caller_supplied_workspace(gq):
     gq.gqa_av_set_workspace(ws)
     try:
         assert_close(run_gpu(gq, attn, v, sl, 1), ref, "caller workspace")
-        small = torch.empty(64 * 1024, dtype=torch.uint8, device="cuda")
+        header = gq.gqa_av_workspace_bytes(1, 8, 4, 4, 8, 0, 0)  # a call with no splits
+        small = torch.empty(header + 64 * 1024, dtype=torch.uint8, device="cuda")
         gq.gqa_av_set_workspace(small)
         with pytest.raises(gq.GqaAvError) as e:
             run_gpu(gq, attn, v, sl, 1, dict(nsplit=16))
@@ -234,3 +285,6 @@ def test_plan_reports_the_launch(gq):
     assert q["mode"] == 0 and q["heads_per_cta"] == 1
     r = gq.gqa_av_plan(8, 32768, 16, 1, 256, 1, -1)
     assert r["heads_per_cta"] == 16 and r["head_chunk"] == 8
+    assert p["early_stages"] == 1
+    e = gq.gqa_av_plan(1, 8192, 32, 8, 128, 0, -1, dict(stages=3, early_stages=3))
+    assert e["stages"] == 3 and e["early_stages"] == 3
