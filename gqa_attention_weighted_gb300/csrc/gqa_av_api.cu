@@ -18,6 +18,7 @@
 #include "gqa_av.h"
 #define GQA_AV_COMBINE_KERNEL  // the split combine kernel lives in this translation unit
 #include "gqa_av_kernel.cuh"
+#include "gqa_av_mma.cuh"
 
 namespace gqa_av {
 
@@ -31,6 +32,13 @@ namespace gqa_av {
   GQA_AV_DECLARE(TAG, 12)
 GQA_AV_DECLARE_ALL(Bf16Tag)
 GQA_AV_DECLARE_ALL(Fp16Tag)
+#define GQA_AV_DECLARE_MMA(TAG, NB)                                                      \
+  extern template cudaError_t launch_mma<TAG, NB>(const Params&, int, int, cudaStream_t); \
+  extern template cudaError_t occupancy_mma<TAG, NB>(int, int, int*);
+#define GQA_AV_DECLARE_MMA_ALL(TAG) \
+  GQA_AV_DECLARE_MMA(TAG, 1) GQA_AV_DECLARE_MMA(TAG, 2) GQA_AV_DECLARE_MMA(TAG, 3) GQA_AV_DECLARE_MMA(TAG, 4)
+GQA_AV_DECLARE_MMA_ALL(Bf16Tag)
+GQA_AV_DECLARE_MMA_ALL(Fp16Tag)
 
 namespace {
 
@@ -65,6 +73,21 @@ struct Kernel {
   OccFn occupancy;
 };
 
+constexpr int kEngineFma = 1;     // CUDA-core packed-FMA kernel
+constexpr int kEngineTensor = 2;  // tcgen05 tensor-core kernel
+constexpr int kMaxMmaHeads = 64;  // N <= 64: B ring and tensor memory stay small
+
+template <typename Tag>
+bool pick_mma(int nb, Kernel* k) {
+  switch (nb) {
+    case 1: *k = {launch_mma<Tag, 1>, occupancy_mma<Tag, 1>}; return true;
+    case 2: *k = {launch_mma<Tag, 2>, occupancy_mma<Tag, 2>}; return true;
+    case 3: *k = {launch_mma<Tag, 3>, occupancy_mma<Tag, 3>}; return true;
+    case 4: *k = {launch_mma<Tag, 4>, occupancy_mma<Tag, 4>}; return true;
+    default: return false;
+  }
+}
+
 template <typename Tag>
 bool pick(int gc, Kernel* k) {
   switch (gc) {
@@ -80,8 +103,11 @@ bool pick(int gc, Kernel* k) {
   }
 }
 
-bool pick_kernel(int v_dtype, int gc, Kernel* k) {
-  return v_dtype == GQA_AV_BF16 ? pick<Bf16Tag>(gc, k) : pick<Fp16Tag>(gc, k);
+// `sel` is the head chunk (FMA kernel) or N / 16 (tensor-core kernel).
+bool pick_kernel(int v_dtype, int engine, int sel, Kernel* k) {
+  if (engine == kEngineTensor)
+    return v_dtype == GQA_AV_BF16 ? pick_mma<Bf16Tag>(sel, k) : pick_mma<Fp16Tag>(sel, k);
+  return v_dtype == GQA_AV_BF16 ? pick<Bf16Tag>(sel, k) : pick<Fp16Tag>(sel, k);
 }
 
 // ------------------------------------------------------------- device info
@@ -94,7 +120,7 @@ struct DeviceInfo {
 
 std::mutex g_mu;
 std::map<int, DeviceInfo> g_devices;
-std::map<std::tuple<int, int, int, int>, int> g_occupancy;  // (dev, dtype, gc, smem) -> ctas/SM
+std::map<std::tuple<int, int, int, int, int>, int> g_occupancy;  // (dev, dtype, engine, sel, smem)
 
 int device_info(int dev, DeviceInfo* out) {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -116,22 +142,23 @@ int device_info(int dev, DeviceInfo* out) {
   return GQA_AV_OK;
 }
 
-int ctas_per_sm(int dev, int smem_limit, int v_dtype, int gc, int smem, int* n) {
+int ctas_per_sm(int dev, int smem_limit, int v_dtype, int engine, int sel, int smem, int* n) {
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    auto it = g_occupancy.find(std::make_tuple(dev, v_dtype, gc, smem));
+    auto it = g_occupancy.find(std::make_tuple(dev, v_dtype, engine, sel, smem));
     if (it != g_occupancy.end()) {
       *n = it->second;
       return GQA_AV_OK;
     }
   }
   Kernel kern;
-  if (!pick_kernel(v_dtype, gc, &kern)) return fail(GQA_AV_ERR_UNSUPPORTED, "no kernel for GC=%d", gc);
+  if (!pick_kernel(v_dtype, engine, sel, &kern))
+    return fail(GQA_AV_ERR_UNSUPPORTED, "no kernel for engine %d / %d", engine, sel);
   int k = 0;
   cudaError_t e = kern.occupancy(smem_limit, smem, &k);
   if (e != cudaSuccess) return fail_cuda(e, "occupancy query");
   std::lock_guard<std::mutex> lk(g_mu);
-  g_occupancy[std::make_tuple(dev, v_dtype, gc, smem)] = k;
+  g_occupancy[std::make_tuple(dev, v_dtype, engine, sel, smem)] = k;
   *n = k;
   return GQA_AV_OK;
 }
@@ -143,6 +170,11 @@ struct Plan {
   int parts, cols_per_cta, ctas_per_tile;  // split combine launch (nsplit > 1)
   int one_per_sm;                          // shared memory padded so one CTA fits per SM
   int early;                               // stages issued before the length is read
+  int engine;                              // kEngineFma or kEngineTensor
+  int nmma;                                // tensor core: N (heads padded to 16)
+  int v_halves;                            // tensor core: 64-column V boxes per stage
+  int tmem_cols;                           // tensor core: tensor-memory columns
+  uint32_t b_off;                          // tensor core: B ring offset
   int attn_tma;                            // attn weights by TMA (rows of Hq % 4 == 0 floats)
   uint32_t v_stage_bytes, a_off, bar_off;
   size_t ws_bytes;  // partials only
@@ -160,6 +192,25 @@ int check_shape(int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode) 
     return fail(GQA_AV_ERR_INVALID, "unknown mode %d", mode);
   if (D % 8 != 0) return fail(GQA_AV_ERR_UNSUPPORTED, "D=%d is not a multiple of 8", D);
   return GQA_AV_OK;
+}
+
+// Kernel instantiation of a plan: head chunk (FMA) or N / 16 (tensor core).
+int kernel_sel(const Plan& p) { return p.engine == kEngineTensor ? p.nmma / 16 : p.gc; }
+
+// Shared memory of a tensor-core plan, from a 1024-byte-aligned base (1 KiB of
+// slack lets the kernel align the dynamic allocation): [V ring, stages x R x
+// 256 B] [attn ring] [B ring, stages x (hi, lo) x N x R x 2 B] [mbarriers,
+// tensor-memory address, flag].
+void layout_mma(Plan* p, int min_smem) {
+  p->v_stage_bytes = static_cast<uint32_t>(p->R) * 256;
+  const size_t vring = static_cast<size_t>(p->stages) * p->v_stage_bytes;
+  p->a_off = static_cast<uint32_t>(align_up(vring, 128));
+  const size_t aring = static_cast<size_t>(p->stages) * p->R * p->ap * 4;
+  p->b_off = static_cast<uint32_t>(align_up(p->a_off + aring, 128));
+  const size_t bring = static_cast<size_t>(p->stages) * 2 * p->nmma * p->R * 2;
+  p->bar_off = static_cast<uint32_t>(align_up(p->b_off + bring, 16));
+  const size_t bars = (3 * kMaxStages + 5) * 8 + 8;
+  p->smem = std::max(static_cast<int>(p->bar_off + bars + 1024), min_smem);
 }
 
 // Shared memory of a plan: [V ring | reduction buffer] [attn ring] [mbarriers] [flag].
@@ -189,19 +240,61 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
     if (p->heads % c == 0) { p->gc = c; break; }
   p->nc = p->heads / p->gc;
 
-  // Output columns per CTA: a multiple of 8 dividing D, at most 256 (one TMA box).
-  const int want_dt = (t && t->dtile > 0) ? t->dtile : 128;
-  if (t && t->dtile > 0 && (t->dtile % 8 || D % t->dtile || t->dtile > 256))
-    return fail(GQA_AV_ERR_INVALID, "dtile=%d must be a multiple of 8 dividing D=%d, <= 256",
-                t->dtile, D);
-  p->dt = 0;
-  for (int dt = std::min(want_dt, std::min(D, 256)); dt >= 8; dt -= 8)
-    if (D % dt == 0 && (dt / 8) * p->nc <= 32 * consumer_warps(p->gc)) { p->dt = dt; break; }
-  if (!p->dt)
-    return fail(GQA_AV_ERR_UNSUPPORTED, "no column tile fits G=%d heads per CTA", p->heads);
+  // Engine. The tensor-core kernel takes head groups of up to 64 heads and
+  // D >= 64 that splits into 128-column tiles (D <= 128 or D % 128 == 0);
+  // the packed-FMA kernel takes the rest, or any shape when asked for (a
+  // dtile override also selects it). Where both apply the library picks by
+  // what bounds the call (measured on GB300): 8 or more heads a CTA make the
+  // FMA kernel's arithmetic the bound, and so do long streams (the FMA issue
+  // rate falls behind HBM); short one-wave calls with few heads are bound by
+  // latency, where the FMA kernel's lighter pipeline is faster.
+  const bool mma_ok = p->heads <= kMaxMmaHeads && D >= 64 && (D <= kMmaM || D % kMmaM == 0);
+  const int want_engine = t ? t->engine : 0;
+  if (want_engine < 0 || want_engine > kEngineTensor)
+    return fail(GQA_AV_ERR_INVALID, "engine=%d must be 0 (auto), 1 (FMA) or 2 (tensor)",
+                want_engine);
+  if (want_engine == kEngineTensor && !mma_ok)
+    return fail(GQA_AV_ERR_UNSUPPORTED,
+                "the tensor-core engine needs <= %d heads per CTA and D >= 64 with D <= 128 or "
+                "D %% 128 == 0 (heads %d, D %d)",
+                kMaxMmaHeads, p->heads, D);
+  if (want_engine == kEngineTensor && t->dtile > 0 && t->dtile != std::min(D, kMmaM))
+    return fail(GQA_AV_ERR_INVALID, "the tensor-core engine uses dtile = %d", std::min(D, kMmaM));
+  const long long tile_rows =
+      static_cast<long long>(B) * p->hgroups * Cmax * ((D + kMmaM - 1) / kMmaM);
+  const bool prefer_tensor = p->heads >= 8 || tile_rows >= (1LL << 18);
+  if (want_engine)
+    p->engine = want_engine;
+  else
+    p->engine = mma_ok && !(t && t->dtile > 0) && prefer_tensor ? kEngineTensor : kEngineFma;
+  const bool tensor = p->engine == kEngineTensor;
+
+  if (tensor) {
+    // One MMA covers 128 output columns; D <= 64 leaves the second half idle.
+    p->dt = std::min(D, kMmaM);
+    p->nmma = static_cast<int>(align_up(p->heads, 16));
+    p->v_halves = p->dt > 64 ? 2 : 1;
+    p->tmem_cols = 32;  // two D buffers of 2N columns (hi and lo products)
+    while (p->tmem_cols < 4 * p->nmma) p->tmem_cols *= 2;
+    p->row_par = 1;
+  } else {
+    // Output columns per CTA: a multiple of 8 dividing D, at most 256 (one TMA box).
+    const int want_dt = (t && t->dtile > 0) ? t->dtile : 128;
+    if (t && t->dtile > 0 && (t->dtile % 8 || D % t->dtile || t->dtile > 256))
+      return fail(GQA_AV_ERR_INVALID, "dtile=%d must be a multiple of 8 dividing D=%d, <= 256",
+                  t->dtile, D);
+    p->dt = 0;
+    for (int dt = std::min(want_dt, std::min(D, 256)); dt >= 8; dt -= 8)
+      if (D % dt == 0 && (dt / 8) * p->nc <= 32 * consumer_warps(p->gc)) { p->dt = dt; break; }
+    if (!p->dt)
+      return fail(GQA_AV_ERR_UNSUPPORTED, "no column tile fits G=%d heads per CTA", p->heads);
+    p->nmma = 0;
+    p->v_halves = 0;
+    p->tmem_cols = 0;
+  }
   p->ndt = D / p->dt;
   p->ct = p->dt / 8;
-  p->row_par = 32 * consumer_warps(p->gc) / (p->ct * p->nc);
+  if (!tensor) p->row_par = 32 * consumer_warps(p->gc) / (p->ct * p->nc);
 
   // Context splits. With fewer tiles than SMs the grid is one wave of one CTA
   // per SM (shared memory is padded to more than half an SM so no SM takes
@@ -223,19 +316,25 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
   want = std::max<long long>(1, std::min<long long>(want, (Cmax + 7) / 8));
   const int rps0 = static_cast<int>((Cmax + want - 1) / want);
 
-  // Rows per stage: about 32 KiB of V per TMA box (large boxes stream faster
-  // per SM), a multiple of 8 rows, dividing the split into equal stages.
+  // Rows per stage: about 32 KiB of V per stage (large boxes stream faster
+  // per SM), a multiple of 8 rows (16, the MMA's K, for the tensor-core
+  // kernel), dividing the split into equal stages.
+  const int rq = tensor ? 16 : 8;
   int iters;
   if (t && t->rows_per_stage > 0) {
-    if (t->rows_per_stage % 8 || t->rows_per_stage > 256)
-      return fail(GQA_AV_ERR_INVALID, "rows_per_stage=%d must be a multiple of 8, <= 256",
-                  t->rows_per_stage);
+    if (t->rows_per_stage % rq || t->rows_per_stage > 256)
+      return fail(GQA_AV_ERR_INVALID, "rows_per_stage=%d must be a multiple of %d, <= 256",
+                  t->rows_per_stage, rq);
     p->R = t->rows_per_stage;
     iters = (rps0 + p->R - 1) / p->R;
   } else {
-    const int rmax = std::max(8, std::min(256, 32768 / (2 * p->dt)) / 8 * 8);
+    // The tensor-core kernel pays a fixed cost per stage (measured): about
+    // 48 KiB of V per stage there, 32 KiB for the FMA kernel.
+    const int row_bytes = tensor ? 256 : 2 * p->dt;
+    const int stage_bytes = tensor ? 49152 : 32768;
+    const int rmax = std::max(rq, std::min(256, stage_bytes / row_bytes) / rq * rq);
     iters = (rps0 + rmax - 1) / rmax;
-    p->R = static_cast<int>(align_up((rps0 + iters - 1) / iters, 8));
+    p->R = static_cast<int>(align_up((rps0 + iters - 1) / iters, rq));
   }
   p->rows_per_split = p->R * iters;
   p->nsplit = (Cmax + p->rows_per_split - 1) / p->rows_per_split;
@@ -262,10 +361,11 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
   else if (Hq % 2 == 0 && p->heads % 2 == 0) p->avec = 2;
   p->one_per_sm = one_wave && static_cast<long long>(p->tiles) * p->nsplit <= di.sms;
   const int min_smem = p->one_per_sm ? di.smem_per_sm / 2 + 1024 : 0;
-  layout(p, min_smem);
+  auto lay = [&] { if (tensor) layout_mma(p, min_smem); else layout(p, min_smem); };
+  lay();
   while (p->smem > di.smem_optin && p->stages > 2 && !(t && t->stages > 0)) {
     --p->stages;
-    layout(p, min_smem);
+    lay();
   }
   if (p->smem > di.smem_optin)
     return fail(GQA_AV_ERR_UNSUPPORTED, "plan needs %d B of shared memory (limit %d)", p->smem,
@@ -282,7 +382,9 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
     p->early = 1;
   }
 
-  if ((rc = ctas_per_sm(dev, di.smem_optin, v_dtype, p->gc, p->smem, &p->occ))) return rc;
+  if ((rc = ctas_per_sm(dev, di.smem_optin, v_dtype, p->engine, kernel_sel(*p), p->smem,
+                        &p->occ)))
+    return rc;
   if (p->occ < 1) return fail(GQA_AV_ERR_UNSUPPORTED, "kernel does not fit on an SM");
 
   p->ws_bytes = p->nsplit > 1
@@ -315,6 +417,7 @@ void fill_params(Params* p, const Plan& pl, const float* attn, const int32_t* se
   p->a_stage_bytes = static_cast<uint32_t>(pl.R) * pl.ap * 4;
   p->v_stage_bytes = pl.v_stage_bytes; p->a_off = pl.a_off; p->bar_off = pl.bar_off;
   p->timeout_ns = kWaitTimeoutNs;
+  p->v_halves = pl.v_halves; p->b_off = pl.b_off; p->tmem_cols = static_cast<uint32_t>(pl.tmem_cols);
   // attn is 16-byte aligned (checked before planning): a TMA source or a
   // cp.async of up to 16 bytes can start at any 4-head boundary of it.
 }
@@ -407,18 +510,22 @@ int encode_fn(PFN_cuTensorMapEncodeTiled_v12000* fn) {
   return GQA_AV_OK;
 }
 
-// V viewed as 4-D {D, Hkv, Cmax, B} (innermost first); box {dt, 1, R, 1}.
-int encode_v_map(CUtensorMap* m, const void* v, int B, int Cmax, int Hkv, int D, int dt, int R) {
+// V viewed as 4-D {D, Hkv, Cmax, B} (innermost first); box {dt, 1, R, 1}, or
+// for the tensor-core kernel {64, 1, R, 1} with the 128-byte swizzle its A
+// operand is read in.
+int encode_v_map(CUtensorMap* m, const void* v, int B, int Cmax, int Hkv, int D, int dt, int R,
+                 bool mma) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
   int rc = encode_fn(&enc);
   if (rc) return rc;
   const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)Cmax, (cuuint64_t)B};
   const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2,
                                  (cuuint64_t)Cmax * Hkv * D * 2};
-  const cuuint32_t box[4] = {(cuuint32_t)dt, 1, (cuuint32_t)R, 1};
+  const cuuint32_t box[4] = {(cuuint32_t)(mma ? 64 : dt), 1, (cuuint32_t)R, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(v), dims, strides, box,
-                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   mma ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(GQA_AV_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   return GQA_AV_OK;
@@ -466,13 +573,13 @@ int run(const float* attn, const void* v, const int32_t* seq_lens, float* out, i
 
   Params p;
   memset(&p, 0, sizeof p);
-  if ((rc = encode_v_map(&p.v_map, v, B, Cmax, Hkv, D, pl.dt, pl.R))) return rc;
+  if ((rc = encode_v_map(&p.v_map, v, B, Cmax, Hkv, D, pl.dt, pl.R, pl.engine == kEngineTensor))) return rc;
   char* wsb = static_cast<char*>(ws.base);
   fill_params(&p, pl, attn, seq_lens, out, wsb, wsb + kHeaderBytes, B, Cmax, Hq, Hkv, D);
   if (p.attn_tma && (rc = encode_attn_map(&p.a_map, attn, B, Cmax, Hq, pl.ap, pl.R))) return rc;
 
   Kernel kern;
-  if (!pick_kernel(v_dtype, pl.gc, &kern)) return fail(GQA_AV_ERR_UNSUPPORTED, "no kernel");
+  if (!pick_kernel(v_dtype, pl.engine, kernel_sel(pl), &kern)) return fail(GQA_AV_ERR_UNSUPPORTED, "no kernel");
   cudaError_t e = launch_call(kern, pl, p, stream);
   if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
   return GQA_AV_OK;
@@ -544,7 +651,8 @@ int gqa_av_plan(int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode,
   info->rows_per_split = p.rows_per_split;
   info->tiles = p.tiles;
   info->ctas = p.tiles * p.nsplit;
-  info->threads_per_cta = cta_threads(p.gc);
+  info->threads_per_cta = p.engine == kEngineTensor ? kMmaThreads : cta_threads(p.gc);
+  info->engine = p.engine;
   info->smem_bytes = p.smem;
   info->ctas_per_sm = p.occ;
   info->workspace_bytes = kHeaderBytes + p.ws_bytes;
@@ -666,12 +774,12 @@ int run_in_scratch(const float* attn, const void* v, const int32_t* seq_lens, fl
 
   Params p;
   memset(&p, 0, sizeof p);
-  if ((rc = encode_v_map(&p.v_map, v, B, Cmax, Hkv, D, pl.dt, pl.R))) return rc;
+  if ((rc = encode_v_map(&p.v_map, v, B, Cmax, Hkv, D, pl.dt, pl.R, pl.engine == kEngineTensor))) return rc;
   fill_params(&p, pl, attn, seq_lens, out, base, base + status_bytes, B, Cmax, Hq, Hkv, D);
   if (p.attn_tma && (rc = encode_attn_map(&p.a_map, attn, B, Cmax, Hq, pl.ap, pl.R))) return rc;
 
   Kernel kern;
-  if (!pick_kernel(v_dtype, pl.gc, &kern)) return fail(GQA_AV_ERR_UNSUPPORTED, "no kernel");
+  if (!pick_kernel(v_dtype, pl.engine, kernel_sel(pl), &kern)) return fail(GQA_AV_ERR_UNSUPPORTED, "no kernel");
   e = launch_call(kern, pl, p, stream);
   if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
   return GQA_AV_OK;

@@ -3,6 +3,7 @@
 // two element types compile as separate translation units in parallel.
 #pragma once
 #include "gqa_av_kernel.cuh"
+#include "gqa_av_mma.cuh"
 
 namespace gqa_av {
 
@@ -36,6 +37,36 @@ cudaError_t occupancy(int smem_limit, int smem_bytes, int* ctas_per_sm) {
                                                        cta_threads(GC), smem_bytes);
 }
 
+// The same for the tensor-core kernel, NB = N / 16 blocks of 16 heads.
+template <typename Tag, int NB>
+cudaError_t launch_mma(const Params& p, int grid, int smem_bytes, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kMmaThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gqa_av_mma_kernel<Tag, NB>, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <typename Tag, int NB>
+cudaError_t occupancy_mma(int smem_limit, int smem_bytes, int* ctas_per_sm) {
+  cudaError_t e = cudaFuncSetAttribute(gqa_av_mma_kernel<Tag, NB>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_limit);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, gqa_av_mma_kernel<Tag, NB>,
+                                                       kMmaThreads, smem_bytes);
+}
+
+#define GQA_AV_INSTANTIATE_MMA(TAG, NB)                                                  \
+  template cudaError_t launch_mma<TAG, NB>(const Params&, int, int, cudaStream_t);       \
+  template cudaError_t occupancy_mma<TAG, NB>(int, int, int*);
+
 #define GQA_AV_INSTANTIATE(TAG, GC)                                                      \
   template cudaError_t launch<TAG, GC>(const Params&, int, int, cudaStream_t);           \
   template cudaError_t occupancy<TAG, GC>(int, int, int*);
@@ -49,6 +80,10 @@ cudaError_t occupancy(int smem_limit, int smem_bytes, int* ctas_per_sm) {
   GQA_AV_INSTANTIATE(TAG, 6)        \
   GQA_AV_INSTANTIATE(TAG, 7)        \
   GQA_AV_INSTANTIATE(TAG, 8)        \
-  GQA_AV_INSTANTIATE(TAG, 12)
+  GQA_AV_INSTANTIATE(TAG, 12)       \
+  GQA_AV_INSTANTIATE_MMA(TAG, 1)    \
+  GQA_AV_INSTANTIATE_MMA(TAG, 2)    \
+  GQA_AV_INSTANTIATE_MMA(TAG, 3)    \
+  GQA_AV_INSTANTIATE_MMA(TAG, 4)
 
 }  // namespace gqa_av

@@ -86,6 +86,10 @@ struct alignas(64) Params {
   uint32_t bar_off;             // shared-memory offset of the mbarriers
   int early_stages;             // stages issued before the sequence length is read (>= 1)
   long long timeout_ns;         // bound on every mbarrier wait
+  // Tensor-core kernel only.
+  int v_halves;                 // 64-column V boxes per stage (1 or 2)
+  uint32_t b_off;               // shared-memory offset of the B (weights) ring
+  uint32_t tmem_cols;           // tensor-memory columns allocated (4 x N, power of 2 >= 32)
 };
 
 // The split combine: out[tile column] = sum over the tile's splits with
@@ -141,6 +145,32 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long lo
   const uint64_t t0 = global_timer_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity, 100000u)) return true;
+    if (static_cast<long long>(global_timer_ns() - t0) > timeout_ns) return false;
+  }
+}
+
+// The same test without a suspend hint: the thread polls, so it resumes within
+// a few tens of nanoseconds of the phase completing (for waits on the
+// critical path of a pipeline).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Polling wait for the phase of `parity`; false if `timeout_ns` passed.
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity, long long timeout_ns) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_test(bar, parity)) return true;
     if (static_cast<long long>(global_timer_ns() - t0) > timeout_ns) return false;
   }
 }

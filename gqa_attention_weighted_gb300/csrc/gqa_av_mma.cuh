@@ -1,0 +1,452 @@
+// GQA AV decode reduction on the 5th-generation tensor cores (tcgen05) for
+// sm_103a (GB300).
+//
+// Operation (page "pytorch/executorch pull 21063", summary paragraph):
+//   out[b, q_h, d] = sum_{c < L_b} attn[b, c, q_h] * V[b, c, q_h / G, d].
+//
+// One CTA owns the same tile as the FMA kernel (head group, b, d-tile of up to
+// 128 columns) and one context split of it, and reads each V row of its KV
+// head from HBM once for all heads of the group. Per pipeline stage of R
+// context rows it computes the stage's contribution
+//   D[m][n] = sum_k V[c0 + k][d0 + m] * attn[c0 + k][h0 + n]
+// as one tcgen05 matrix product with M = 128 (output columns), N = the group's
+// heads padded to a multiple of 16, K = R, accumulated in fp32 in tensor
+// memory:
+//   * A = V^T, read in place from the TMA-written stage: two 64-column halves
+//     of R rows x 128 B in the 128-byte-swizzled MN-major layout.
+//   * B = the weights, written by the converter warps as bf16 (fp16 for an
+//     fp16 cache) in the K-major core-matrix layout. The fp32 weight w is
+//     split as w = hi + lo with hi = round(w), lo = round(w - hi), and the
+//     hi and lo rows of all heads form one B of 2N rows, so one MMA pass over
+//     the stage's V gives both products: the weights keep about 16
+//     significant bits (V is exact in its own type, and bf16 x bf16 /
+//     fp16 x fp16 products are exact in fp32). fp16 weights are scaled by
+//     2^12 first (exact, undone in the epilogue) so small weights do not fall
+//     into fp16 subnormals.
+//   * The stage's D (double-buffered in tensor memory, 2N columns: hi then
+//     lo) is read back by the accumulator warps with tcgen05.ld and added
+//     into fp32 registers, so the tensor core accumulates at most R/16
+//     products into one value.
+// Rows of a stage past the context are zeroed in shared memory (V) and given
+// zero weight, so what lies there cannot reach the sum.
+//
+// Warp roles, each waiting only on its own inputs so the stages overlap:
+// warps 0-3 accumulate (warp w reads tensor-memory lanes 32w..32w+31 = output
+// columns), warps 4-7 write the weights of each stage as the B operand, warp 8
+// is the TMA producer, and warp 9 allocates tensor memory and one of its
+// threads issues the MMAs. Split partials and
+// the split combine are the FMA kernel's (same workspace layout). Every
+// mbarrier wait is bounded; on expiry the CTA sets the device status word,
+// lets its copies and MMAs in flight finish, frees its tensor memory and
+// returns.
+#pragma once
+
+#include <type_traits>
+
+#include "gqa_av_kernel.cuh"
+
+namespace gqa_av {
+
+constexpr int kMmaM = 128;         // output columns per MMA (D rows)
+constexpr int kMmaAccWarps = 4;    // warps 0-3: one per tensor-memory lane quarter
+constexpr int kMmaCvtWarps = 4;    // warps 4-7: weight conversion
+constexpr int kMmaProducerWarp = kMmaAccWarps + kMmaCvtWarps;
+constexpr int kMmaIssuerWarp = kMmaProducerWarp + 1;
+constexpr int kMmaThreads = 32 * (kMmaIssuerWarp + 1);
+constexpr unsigned kErrMmaWait = 8u;
+
+// tcgen05 shared-memory matrix descriptor: start address, leading- and
+// stride-dimension byte offsets (all >> 4), the sm_100 descriptor version
+// (bit 46) and the swizzle mode (bits 61-63: 0 none, 2 128-byte).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t swizzle) {
+  return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) |
+         (static_cast<uint64_t>(swizzle & 7u) << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 D, A and B of one 16-bit type
+// (bf16 or fp16, never mixed), A MN-major, B K-major, N x M = n x 128.
+template <typename Tag>
+__host__ __device__ constexpr uint32_t mma_idesc(int n) {
+  return (1u << 4) | (std::is_same<Tag, Bf16Tag>::value ? ((1u << 7) | (1u << 10)) : 0u) |
+         (1u << 15) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(kMmaM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation this thread issued has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Weights (a, b) split into 16-bit hi and lo pairs, each packed in a word
+// (a in the low half) for the B operand.
+__device__ __forceinline__ void split_weights(Bf16Tag, float a, float b, uint32_t& hi,
+                                              uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+__device__ __forceinline__ void split_weights(Fp16Tag, float a, float b, uint32_t& hi,
+                                              uint32_t& lo) {
+  const float x = a * 4096.0f, y = b * 4096.0f;
+  const __half2 h = __floats2half2_rn(x, y);
+  const float2 hf = __half22float2(h);
+  const __half2 l = __floats2half2_rn(x - hf.x, y - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+__host__ __device__ constexpr float weight_unscale(Bf16Tag) { return 1.0f; }
+__host__ __device__ constexpr float weight_unscale(Fp16Tag) { return 1.0f / 4096.0f; }
+
+// Named barrier of the accumulator warps and the MMA warp: the warps that
+// touch tensor memory.
+__device__ __forceinline__ void mma_team_sync() {
+  asm volatile("bar.sync 2, %0;" ::"n"(32 * (kMmaAccWarps + 1)) : "memory");
+}
+
+// Shared memory (offsets from a 1024-byte-aligned base):
+//   [V ring: stages x R x 256 B, two 64-column halves of R x 128 B per stage]
+//   [attn ring: stages x R x ap floats]
+//   [B ring: stages x 2N (hi rows, then lo rows) x R x 2 B]
+//   [mbarriers: full, empty, bready (kMaxStages each), dfull[2], dfree[2], drain]
+//   [tensor-memory address]
+template <typename Tag, int NB>
+__global__ void __launch_bounds__(kMmaThreads, 1) gqa_av_mma_kernel(const __grid_constant__ Params p) {
+  constexpr int N = 16 * NB;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = smem_addr(smem_raw);
+  const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base_s - raw_s);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  const int tiles_per_hg = p.B * p.ndt;
+  const int tile = blockIdx.x / p.nsplit;
+  const int split = blockIdx.x - tile * p.nsplit;
+  const int hg = tile / tiles_per_hg;
+  const int rem = tile - hg * tiles_per_hg;
+  const int b = rem / p.ndt;
+  const int dti = rem - b * p.ndt;
+  const int h0 = hg * p.heads;
+  const int kv_h = h0 / p.G;
+  const int d0 = dti * p.dt;
+  const int c_begin = split * p.rows_per_split;
+  const int a_shift = p.attn_tma ? (h0 & 3) : 0;
+  const int pre = min(min(min(p.early_stages, p.stages), p.rows_per_split / p.R),
+                      (p.Cmax - c_begin + p.R - 1) / p.R);
+
+  const uint32_t vring_s = base_s;
+  const uint32_t aring_s = base_s + p.a_off;
+  const uint32_t bring_s = base_s + p.b_off;
+  float* aring = reinterpret_cast<float*>(smem + p.a_off);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_off);
+  const uint32_t full0 = smem_addr(bars);
+  const uint32_t empty0 = smem_addr(bars + kMaxStages);
+  const uint32_t bready0 = smem_addr(bars + 2 * kMaxStages);
+  const uint32_t dfull0 = smem_addr(bars + 3 * kMaxStages);
+  const uint32_t dfree0 = smem_addr(bars + 3 * kMaxStages + 2);
+  const uint32_t drain = smem_addr(bars + 3 * kMaxStages + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kMaxStages + 5);
+
+  if (warp == kMmaIssuerWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "r"(p.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (tid == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(full0 + 8 * s, p.attn_tma ? 1 : 1 + 32);
+      mbar_init(empty0 + 8 * s, 1);                     // one tcgen05.commit per stage
+      mbar_init(bready0 + 8 * s, kMmaCvtWarps);         // one arrival per converter warp
+    }
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(dfull0 + 8 * j, 1);
+      mbar_init(dfree0 + 8 * j, kMmaAccWarps);
+    }
+    mbar_init(drain, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kMmaProducerWarp && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.v_map)) : "memory");
+    if (p.attn_tma)
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.a_map)) : "memory");
+  }
+  const uint64_t policy = evict_first_policy();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  grid_dependency_wait();
+  grid_launch_dependents();
+
+  if (warp == kMmaProducerWarp) {
+    // ----------------------------------------------------------------- producer
+    const float* attn_b = p.attn + (size_t)b * p.Cmax * p.Hq + h0;
+    const int per_row = p.heads / p.avec;
+    auto issue = [&](int stage, int c0, int rows) {
+      const uint32_t full = full0 + 8 * stage;
+      const uint32_t vdst = vring_s + (uint32_t)stage * p.v_stage_bytes;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(full, (uint32_t)p.v_halves * (p.v_stage_bytes / 2) +
+                                        (p.attn_tma ? p.a_stage_bytes : 0u));
+        for (int h = 0; h < p.v_halves; ++h)
+          tma_load_4d(vdst + (uint32_t)h * p.v_stage_bytes / 2, &p.v_map, d0 + 64 * h, kv_h, c0, b,
+                      full, policy);
+        if (p.attn_tma)
+          tma_load_3d(aring_s + (uint32_t)stage * p.a_stage_bytes, &p.a_map, h0 - a_shift, c0, b,
+                      full, policy);
+      }
+      if (p.attn_tma) return;
+      const float* src = attn_b + (size_t)c0 * p.Hq;
+      const uint32_t dst = aring_s + 4u * (uint32_t)(stage * p.R * p.ap);
+      const int n = rows * per_row;
+      for (int i = lane; i < n; i += 32) {
+        const int r = i / per_row, k = (i - r * per_row) * p.avec;
+        const uint32_t d = dst + 4u * (r * p.ap + k);
+        const float* sp = src + (size_t)r * p.Hq + k;
+        if (p.avec == 4) cp_async<16>(d, sp);
+        else if (p.avec == 2) cp_async<8>(d, sp);
+        else cp_async<4>(d, sp);
+      }
+      cp_async_arrive_noinc(full);
+    };
+    int L = p.seq_lens ? p.seq_lens[b] : p.Cmax;
+    issue(0, c_begin, min(p.R, p.Cmax - c_begin));
+    for (int it = 1; it < pre; ++it) {
+      const int c0 = c_begin + it * p.R;
+      issue(it, c0, min(p.R, p.Cmax - c0));
+    }
+    L = L < 0 ? 0 : (L > p.Cmax ? p.Cmax : L);
+    const int nsplit_b = L > 0 ? (L + p.rows_per_split - 1) / p.rows_per_split : 1;
+    const int c_end = min(c_begin + p.rows_per_split, L);
+    const int n_iters = split < nsplit_b ? max((c_end - c_begin + p.R - 1) / p.R, 1) : 0;
+    int issued = pre;
+    bool ok = true;
+    for (int it = pre; it < n_iters; ++it) {
+      const int stage = it % p.stages;
+      const uint32_t parity = ((it / p.stages) & 1) ^ 1;
+      if (!mbar_wait(empty0 + 8 * stage, parity, p.timeout_ns)) {
+        atomicOr(p.status, kErrEmptyWait);
+        ok = false;
+        break;
+      }
+      const int c0 = c_begin + it * p.R;
+      issue(stage, c0, min(p.R, c_end - c0));
+      issued = it + 1;
+    }
+    cp_async_wait_all();
+    if (!ok) {
+      for (int it = max(0, issued - p.stages); it < issued; ++it)
+        if (!mbar_wait(full0 + 8 * (it % p.stages), (it / p.stages) & 1, p.timeout_ns))
+          atomicOr(p.status, kErrDrain);
+    }
+    for (int it = n_iters; it < pre; ++it)
+      if (!mbar_wait(full0 + 8 * it, 0, p.timeout_ns) && lane == 0) atomicOr(p.status, kErrDrain);
+    return;
+  }
+
+  // Converters, accumulators and the MMA warp: the split's context.
+  int L = p.seq_lens ? p.seq_lens[b] : p.Cmax;
+  L = L < 0 ? 0 : (L > p.Cmax ? p.Cmax : L);
+  const int nsplit_b = L > 0 ? (L + p.rows_per_split - 1) / p.rows_per_split : 1;
+  const int c_end = min(c_begin + p.rows_per_split, L);
+  const int n_iters = split < nsplit_b ? max((c_end - c_begin + p.R - 1) / p.R, 1) : 0;
+  const uint32_t b_half = (uint32_t)N * p.R * 2;   // bytes of one of hi / lo
+
+  if (warp == kMmaIssuerWarp) {
+    // -------------------------------------------------------------- MMA issuer
+    bool ok = true;
+    if (lane == 0) {
+      const uint32_t idesc = mma_idesc<Tag>(2 * N);
+      const uint32_t a_lbo = (uint32_t)p.R * 128;      // second 64-column half
+      const uint32_t b_sbo = (uint32_t)(p.R / 8) * 128;  // next 8 rows of B
+      int issued = 0;
+      for (int it = 0; it < n_iters; ++it) {
+        const int stage = it % p.stages, j = it & 1;
+        if (!mbar_poll(bready0 + 8 * stage, (it / p.stages) & 1, p.timeout_ns) ||
+            (it >= 2 && !mbar_poll(dfree0 + 8 * j, ((it - 2) >> 1) & 1, p.timeout_ns))) {
+          atomicOr(p.status, kErrMmaWait);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + (uint32_t)(j * 2 * N);
+        const uint32_t a0 = vring_s + (uint32_t)stage * p.v_stage_bytes;
+        const uint32_t bb = bring_s + (uint32_t)stage * 2 * b_half;
+        // K step kk starts 16 rows on: 2048 B into each V half, two core
+        // matrices (256 B) into B. The start-address field holds address / 16
+        // in its low 14 bits, so the step is added to the descriptor itself.
+        const uint64_t ad0 = smem_desc(a0, a_lbo, 1024, 2);
+        const uint64_t bd0 = smem_desc(bb, 128, b_sbo, 0);
+        mma_f16(d_tmem, ad0, bd0, idesc, 0u);
+#pragma unroll 4
+        for (int kk = 1; kk < p.R / 16; ++kk)
+          mma_f16(d_tmem, ad0 + (uint64_t)(kk * (2048 >> 4)), bd0 + (uint64_t)(kk * (256 >> 4)),
+                  idesc, 1u);
+        mma_commit(empty0 + 8 * stage);  // V, attn and B slots free once these MMAs are done
+        mma_commit(dfull0 + 8 * j);
+        issued = it + 1;
+      }
+      if (issued > 0) {
+        mma_commit(drain);
+        if (!mbar_wait(drain, 0, p.timeout_ns)) atomicOr(p.status, kErrMmaWait);
+      }
+    }
+    __syncwarp();
+    (void)ok;
+    mma_team_sync();  // consumers are done with tensor memory
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(p.tmem_cols)
+                 : "memory");
+    return;
+  }
+
+  if (warp >= kMmaAccWarps) {
+    // --------------------------------------------------------------- converters
+    // Weights of each stage -> B hi / lo (K-major 8 x 16 B core matrices):
+    // element (n, k) at ((n / 8) * nkc + k / 8) * 128 + (n % 8) * 16 + (k % 8) * 2.
+    const int ctid = tid - 32 * kMmaAccWarps;
+    const int nkc = p.R / 8;
+    const int items = N * nkc;
+    for (int it = 0; it < n_iters; ++it) {
+      const int stage = it % p.stages;
+      if (!mbar_poll(full0 + 8 * stage, (it / p.stages) & 1, p.timeout_ns)) {
+        atomicOr(p.status, kErrFullWait);
+        break;
+      }
+      const int c0 = c_begin + it * p.R;
+      const int valid = min(p.R, c_end - c0);
+      const float* ast = aring + (size_t)stage * p.R * p.ap + a_shift;
+      uint8_t* bst = smem + p.b_off + (size_t)stage * 2 * b_half;
+      for (int t = ctid; t < items; t += kMmaCvtWarps * 32) {
+        const int n = t % N, kc = t / N;
+        float w[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int k = kc * 8 + e;
+          w[e] = (n < p.heads && k < valid) ? ast[(size_t)k * p.ap + n] : 0.0f;
+        }
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) split_weights(Tag{}, w[2 * q], w[2 * q + 1], hi[q], lo[q]);
+        const size_t off = (size_t)((n >> 3) * nkc + kc) * 128 + (n & 7) * 16;
+        *reinterpret_cast<uint4*>(bst + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(bst + b_half + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      // V rows past the context: zero (they may hold anything, NaN included).
+      if (valid < p.R) {
+        uint8_t* vst = smem + (size_t)stage * p.v_stage_bytes;
+        const int chunks = (p.R - valid) * 8;  // 16-byte chunks of one half
+        for (int t = ctid; t < chunks * p.v_halves; t += kMmaCvtWarps * 32) {
+          const int h = t / chunks, c = t - h * chunks;
+          const int k = valid + c / 8;
+          const size_t off = (size_t)h * (p.v_stage_bytes / 2) + (size_t)(k >> 3) * 1024 +
+                             (size_t)(k & 7) * 128 + (size_t)(c & 7) * 16;
+          *reinterpret_cast<uint4*>(vst + off) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bready0 + 8 * stage);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- accumulators
+  // Thread t owns output column m = t (tensor-memory lane t) of every head.
+  const int m = tid;
+  float acc[N];
+#pragma unroll
+  for (int n = 0; n < N; ++n) acc[n] = 0.0f;
+  bool ok = true;
+  for (int it = 0; it < n_iters; ++it) {   // add stage it's D into acc, free its buffer
+    const int j = it & 1;
+    if (!mbar_wait(dfull0 + 8 * j, (it >> 1) & 1, p.timeout_ns)) {
+      atomicOr(p.status, kErrMmaWait);
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(j * 2 * N);
+#pragma unroll
+    for (int q = 0; q < NB; ++q) {
+      float h[16], l[16];
+      tmem_ld16(taddr + 16u * q, h);
+      tmem_ld16(taddr + (uint32_t)N + 16u * q, l);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc[16 * q + i] += h[i] + l[i];
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(dfree0 + 8 * j);
+  }
+
+  if (ok && n_iters > 0) {
+    const float unscale = weight_unscale(Tag{});
+    const bool alone = nsplit_b == 1;
+    const int tile_elems = p.heads * p.dt;
+    float* part = p.ws + ((size_t)tile * p.nsplit + split) * tile_elems;
+    if (m < p.dt && d0 + m < p.D) {
+#pragma unroll
+      for (int n = 0; n < N; ++n) {
+        if (n < p.heads) {
+          const float v = acc[n] * unscale;
+          if (alone) p.out[((size_t)b * p.Hq + h0 + n) * p.D + d0 + m] = v;
+          else __stcg(part + (size_t)n * p.dt + m, v);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  mma_team_sync();
+}
+
+// Launch and occupancy of one instantiation (defined with the instantiations).
+template <typename Tag, int NB>
+cudaError_t launch_mma(const Params& p, int grid, int smem_bytes, cudaStream_t stream);
+template <typename Tag, int NB>
+cudaError_t occupancy_mma(int smem_limit, int smem_bytes, int* ctas_per_sm);
+
+}  // namespace gqa_av

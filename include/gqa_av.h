@@ -88,9 +88,13 @@ int gqa_av_decode_per_head(const float *attn, const void *v_cache, const int32_t
  * pipeline stage (8..256); stages: pipeline depth (2..8); early_stages:
  * stages each CTA issues before it has read its sequence length (1..stages;
  * the library issues one, since rows past a length are read for nothing and
- * the first stage lands later behind the others). Results stay within the
- * stated tolerance for every choice, and are bitwise reproducible for a fixed
- * choice.
+ * the first stage lands later behind the others); engine: 0 lets the library
+ * pick, 1 forces the CUDA-core packed-FMA kernel, 2 the tcgen05 tensor-core
+ * kernel (head groups of <= 64 heads and D >= 64 with D <= 128 or
+ * D % 128 == 0; the library picks it wherever it applies unless dtile is
+ * set, and with it dtile must be min(D, 128) or unset; rows_per_stage must
+ * then be a multiple of 16). Results stay within the stated tolerance for
+ * every choice, and are bitwise reproducible for a fixed choice.
  */
 typedef struct gqa_av_tuning {
     int nsplit;
@@ -98,6 +102,7 @@ typedef struct gqa_av_tuning {
     int rows_per_stage;
     int stages;
     int early_stages;
+    int engine;
 } gqa_av_tuning;
 
 int gqa_av_decode_tuned(const float *attn, const void *v_cache, const int32_t *seq_lens,
@@ -113,6 +118,7 @@ typedef struct gqa_av_plan_info {
     int rows_per_stage;
     int stages;
     int early_stages;    /* stages issued before the sequence length is read */
+    int engine;          /* 1 CUDA-core packed FMA, 2 tcgen05 tensor cores */
     int nsplit;          /* context splits per tile */
     int combine_ctas;    /* CTAs of the split-combine kernel (0: not launched) */
     int rows_per_split;

@@ -67,8 +67,9 @@ def test_hand_worked_fixture_exact(gq, vd, mode):
     assert np.array_equal(out[..., 2:], np.zeros((2, 4, 6)))
 
 
+@pytest.mark.parametrize("engine", [1, 2], ids=["fma", "tensor"])
 @pytest.mark.parametrize("vd", ["bf16", "fp16"])
-def test_one_hot_returns_the_row_exactly(gq, vd):
+def test_one_hot_returns_the_row_exactly(gq, vd, engine):
     rng = np.random.default_rng(21)
     B, C, Hq, Hkv, D = 2, 700, 12, 3, 128
     _, v, sl = rand_case(rng, B, C, Hq, Hkv, D, vd, [700, 333])
@@ -77,7 +78,7 @@ def test_one_hot_returns_the_row_exactly(gq, vd):
         a = torch.zeros((B, C, Hq), dtype=torch.float32)
         a[:, c0, :] = 1.0
         for mode in (0, 1):
-            out = run_gpu(gq, a, v, sl, mode)
+            out = run_gpu(gq, a, v, sl, mode, dict(engine=engine))
             for b in range(B):
                 for q in range(Hq):
                     assert np.array_equal(out[b, q], vv[b, c0, q // 4]), (c0, mode, b, q)
@@ -91,8 +92,20 @@ for G in (1, 2, 3, 4, 5, 7, 8, 12, 16, 32):
 SWEEP += [(4, 8), (6, 24), (3, 80), (9, 96), (10, 128), (14, 64), (20, 64), (11, 40)]
 
 
+def tensor_engine_applies(heads, D):
+    """Shapes the tcgen05 kernel takes (the library's own rule, restated)."""
+    return heads <= 64 and D >= 64 and (D <= 128 or D % 128 == 0)
+
+
+def tensor_engine_preferred(B, C, Hq, heads, D):
+    """Where the library picks it by default: 8+ heads a CTA or >= 2^18 tile rows."""
+    tile_rows = B * (Hq // heads) * C * ((D + 127) // 128)
+    return tensor_engine_applies(heads, D) and (heads >= 8 or tile_rows >= 1 << 18)
+
+
+@pytest.mark.parametrize("engine", [0, 1, 2], ids=["auto", "fma", "tensor"])
 @pytest.mark.parametrize("G,D", SWEEP, ids=[f"G{g}-D{d}" for g, d in SWEEP])
-def test_shape_sweep(gq, G, D):
+def test_shape_sweep(gq, G, D, engine):
     rng = np.random.default_rng(1000 * G + D)
     Hkv = 2 if G <= 16 else 1
     B, C = 3, 517
@@ -101,7 +114,15 @@ def test_shape_sweep(gq, G, D):
         attn, v, sl = rand_case(rng, B, C, G * Hkv, Hkv, D, vd, lens)
         ref = run_oracle(attn, v, sl, vd)
         for mode in (0, 1):
-            assert_close(run_gpu(gq, attn, v, sl, mode), ref, f"G={G} D={D} {vd} mode={mode}")
+            heads = G if mode == 1 else 1
+            if engine == 2 and not tensor_engine_applies(heads, D):
+                continue
+            if engine == 0:
+                want = 2 if tensor_engine_preferred(B, C, G * Hkv, heads, D) else 1
+                plan = gq.gqa_av_plan(B, C, G * Hkv, Hkv, D, 0 if vd == "bf16" else 1, mode)
+                assert plan["engine"] == want, (G, D, mode, plan["engine"])
+            out = run_gpu(gq, attn, v, sl, mode, dict(engine=engine) if engine else None)
+            assert_close(out, ref, f"G={G} D={D} {vd} mode={mode} engine={engine}")
 
 
 @pytest.mark.parametrize("L", [0, 1, 2, 7, 8, 9, 31, 32, 33, 63, 64, 65, 255, 256, 257, 1000])
@@ -143,10 +164,24 @@ TUNINGS = [dict(nsplit=1), dict(nsplit=2), dict(nsplit=7), dict(nsplit=1000),
            dict(nsplit=2, rows_per_stage=64, stages=8, early_stages=8)]
 
 
+def tensor_tuning_applies(t):
+    """The tcgen05 kernel takes dtile = min(D, 128) only and rows in 16s."""
+    return t.get("dtile", 128) == 128 and t.get("rows_per_stage", 16) % 16 == 0
+
+
+@pytest.mark.parametrize("engine", [1, 2], ids=["fma", "tensor"])
 @pytest.mark.parametrize("tuning", TUNINGS, ids=[str(t) for t in TUNINGS])
-def test_tunings_agree_and_are_deterministic(gq, tuning):
+def test_tunings_agree_and_are_deterministic(gq, tuning, engine):
+    if engine == 2 and not tensor_tuning_applies(tuning):
+        pytest.skip("launch shape the tensor-core kernel does not take")
+    tuning = dict(tuning, engine=engine)
     rng = np.random.default_rng(99)
     B, C, Hq, Hkv, D = 2, 1500, 24, 8, 128
+    try:
+        gq.gqa_av_plan(B, C, Hq, Hkv, D, 0, 1, tuning)
+    except gq.GqaAvError as e:
+        assert e.status == 2 and "shared memory" in str(e), e
+        pytest.skip("ring larger than shared memory for this kernel")
     for vd in ("bf16", "fp16"):
         attn, v, sl = rand_case(rng, B, C, Hq, Hkv, D, vd, [1500, 777])
         ref = run_oracle(attn, v, sl, vd)
@@ -155,6 +190,28 @@ def test_tunings_agree_and_are_deterministic(gq, tuning):
             b = run_gpu(gq, attn, v, sl, mode, tuning)
             assert_close(a, ref, f"{tuning} {vd} mode={mode}")
             assert np.array_equal(a, b), "repeated call differs bitwise"
+
+
+def test_engine_choice_is_checked(gq):
+    # D = 40 is below the tensor-core kernel's 64 columns; 72 heads above its 64.
+    with pytest.raises(gq.GqaAvError) as e:
+        gq.gqa_av_plan(1, 64, 8, 2, 40, 0, 1, dict(engine=2))
+    assert e.value.status == 2
+    with pytest.raises(gq.GqaAvError) as e:
+        gq.gqa_av_plan(1, 64, 72, 1, 128, 0, 1, dict(engine=2))
+    assert e.value.status == 2
+    for bad in (dict(engine=3), dict(engine=-1), dict(engine=2, dtile=64),
+                dict(engine=2, rows_per_stage=24)):
+        with pytest.raises(gq.GqaAvError) as e:
+            gq.gqa_av_plan(1, 512, 8, 2, 128, 0, 1, bad)
+        assert e.value.status == 1, bad
+    # Default choice: tensor cores for 8+ heads or long streams, else FMA.
+    assert gq.gqa_av_plan(1, 512, 16, 2, 128, 0, 1)["engine"] == 2
+    assert gq.gqa_av_plan(1, 512, 8, 2, 128, 0, 1)["engine"] == 1
+    assert gq.gqa_av_plan(4, 16384, 24, 8, 128, 0, 1)["engine"] == 2
+    assert gq.gqa_av_plan(1, 8192, 32, 8, 128, 0, 1)["engine"] == 1
+    assert gq.gqa_av_plan(1, 512, 16, 2, 128, 0, 1, dict(dtile=64))["engine"] == 1
+    assert gq.gqa_av_plan(1, 512, 16, 2, 40, 0, 1)["engine"] == 1
 
 
 def test_modes_agree_and_identical_weights_give_identical_heads(gq):
