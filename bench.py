@@ -41,8 +41,11 @@ UNIT = "GB/s"
 DEFAULT_WORKLOAD = "llama"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["gqa_attention_weighted_gb300/csrc/gqa_av_kernel.cuh",
+                  "gqa_attention_weighted_gb300/csrc/gqa_av_mma.cuh",
                   "gqa_attention_weighted_gb300/csrc/gqa_av_instances.cuh",
                   "gqa_attention_weighted_gb300/csrc/gqa_av_api.cu"]
+ENGINES = {"auto": 0, "fma": 1, "tensor": 2}
+KERNEL_NAMES = {1: "gqa_av_kernel", 2: "gqa_av_mma_kernel"}
 
 
 def kernel_hash() -> str:
@@ -62,9 +65,9 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def committed_traffic(workload: str, mode: int):
+def committed_traffic(workload: str, mode: int, engine: int):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source for this workload and mode."""
+    on the current kernel source for this workload, mode and engine."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
@@ -73,7 +76,7 @@ def committed_traffic(workload: str, mode: int):
         return None
     for e in entries:
         if (e.get("kernel_hash") == kernel_hash() and e.get("workload") == workload
-                and e.get("mode") == mode):
+                and e.get("mode") == mode and e.get("engine") == engine):
             return e.get("traffic_bytes_per_launch")
     return None
 
@@ -171,6 +174,15 @@ def run_gpu(args, rank, world, local):
     w = W.get(args.workload)
     dev = torch.device("cuda", torch.cuda.current_device())
     mode = {"auto": gq.MODE_AUTO, "gqa": gq.MODE_GQA, "per_head": gq.MODE_PER_HEAD}[args.mode]
+    tuning = dict(engine=ENGINES[args.engine]) if args.engine != "auto" else None
+
+    def call(s, out):
+        if tuning is None:
+            gq.gqa_av_decode(s["attn"], s["v"], s["seq_lens"], out, mode=mode)
+        else:
+            gq.gqa_av_decode_tuned(s["attn"], s["v"], s["seq_lens"], out, mode=mode,
+                                   tuning=tuning)
+
     x = W.generate(w, dev, pad="zero")
     lens = x["seq_lens"].cpu().tolist()
     cbytes = W.compulsory_bytes(w, lens)
@@ -187,8 +199,7 @@ def run_gpu(args, rank, world, local):
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
-            s = sets[i % n_sets]
-            gq.gqa_av_decode(s["attn"], s["v"], s["seq_lens"], outs[i % n_sets], mode=mode)
+            call(sets[i % n_sets], outs[i % n_sets])
         stream.synchronize()
         gq.gqa_av_device_status(stream)
 
@@ -199,9 +210,7 @@ def run_gpu(args, rank, world, local):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 for i in range(n):
-                    s = sets[i % n_sets]
-                    gq.gqa_av_decode(s["attn"], s["v"], s["seq_lens"], outs[i % n_sets],
-                                     mode=mode)
+                    call(sets[i % n_sets], outs[i % n_sets])
             return g
 
         g_main = capture(chunk)
@@ -233,8 +242,9 @@ def run_gpu(args, rank, world, local):
     achieved = cbytes / per_launch_s / 1e9
     peak, peak_kind = measured_peak()
 
-    e2e = run_e2e(gq, w, x, mode, dev, args, world)
-    plan = gq.gqa_av_plan(w.B, w.Cmax, w.Hq, w.Hkv, w.D, gq.native.v_dtype_code(x["v"].dtype), mode)
+    e2e = run_e2e(gq, w, x, call, dev, args, world)
+    plan = gq.gqa_av_plan(w.B, w.Cmax, w.Hq, w.Hkv, w.D, gq.native.v_dtype_code(x["v"].dtype), mode,
+                          tuning)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -246,6 +256,7 @@ def run_gpu(args, rank, world, local):
         "us_per_call": ms_per_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {**w.describe(), "mode": args.mode, "resolved_mode": plan["mode"],
+                   "engine": args.engine, "resolved_engine": plan["engine"],
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "compulsory_bytes_per_call": cbytes, "flops_per_call": flops,
                    "l2": f"rotating {n_sets} input sets, {n_sets * set_bytes / 1e6:.0f} MB "
@@ -257,8 +268,8 @@ def run_gpu(args, rank, world, local):
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_kind": f"{peak_kind} hbm_gbs (copy)",
                      "frac_of_8tbs_nominal": round(achieved / 8000.0, 4),
-                     "traffic": committed_traffic(w.name, plan["mode"]),
-                     "kernel": "gqa_av_kernel", "kernel_hash": kernel_hash(),
+                     "traffic": committed_traffic(w.name, plan["mode"], plan["engine"]),
+                     "kernel": KERNEL_NAMES[plan["engine"]], "kernel_hash": kernel_hash(),
                      "duration": "average time of one whole call (main kernel and, when the "
                                  "context is split, the split-combine kernel) over the timed "
                                  "region; the main kernel alone is shorter"},
@@ -272,7 +283,7 @@ def run_gpu(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(gq, w, x, mode, dev, args, world):
+def run_e2e(gq, w, x, call, dev, args, world):
     """Same call with host inputs: pinned H2D copies, the call, D2H of out."""
     host = {k: t.cpu().pin_memory() for k, t in x.items()}
     out_host = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32).pin_memory()
@@ -286,7 +297,7 @@ def run_e2e(gq, w, x, mode, dev, args, world):
     def step():
         for k in host:
             dbuf[k].copy_(host[k], non_blocking=True)
-        gq.gqa_av_decode(dbuf["attn"], dbuf["v"], dbuf["seq_lens"], out, mode=mode)
+        call(dbuf, out)
         out_host.copy_(out, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -396,6 +407,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     help="one of: " + ", ".join(W.ALIASES))
     ap.add_argument("--mode", choices=["auto", "gqa", "per_head"], default="auto")
+    ap.add_argument("--engine", choices=list(ENGINES), default="auto",
+                    help="kernel: the library's choice, the CUDA-core FMA kernel or the "
+                         "tcgen05 tensor-core kernel")
     ap.add_argument("--graph-len", type=int, default=500)
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -301,10 +301,17 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
   // two); with many tiles it runs in waves (a split with no context exits at
   // once) and splits only balance ragged lengths.
   p->tiles = p->hgroups * B * p->ndt;
-  const bool one_wave = !(t && t->nsplit > 0) && p->tiles < di.sms;
+  // The tensor-core kernel runs one CTA per SM (its tensor memory limits
+  // residency) and pays a fixed cost per CTA: with few tiles it is given
+  // about three waves of short splits instead, which also balances ragged
+  // lengths (measured faster than one wave of long splits).
+  const bool few_tiles = !(t && t->nsplit > 0) && p->tiles < di.sms;
+  const bool one_wave = few_tiles && !tensor;
   long long want;
   if (t && t->nsplit > 0) {
     want = t->nsplit;
+  } else if (few_tiles && tensor) {
+    want = (3LL * di.sms + p->tiles - 1) / p->tiles;
   } else if (one_wave) {
     want = di.sms / p->tiles;
   } else {
@@ -329,9 +336,10 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
     iters = (rps0 + p->R - 1) / p->R;
   } else {
     // The tensor-core kernel pays a fixed cost per stage (measured): about
-    // 48 KiB of V per stage there, 32 KiB for the FMA kernel.
+    // 48 KiB of V per stage there (16 KiB for its short splits), 32 KiB for
+    // the FMA kernel.
     const int row_bytes = tensor ? 256 : 2 * p->dt;
-    const int stage_bytes = tensor ? 49152 : 32768;
+    const int stage_bytes = tensor ? (few_tiles ? 16384 : 49152) : 32768;
     const int rmax = std::max(rq, std::min(256, stage_bytes / row_bytes) / rq * rq);
     iters = (rps0 + rmax - 1) / rmax;
     p->R = static_cast<int>(align_up((rps0 + iters - 1) / iters, rq));
