@@ -82,6 +82,9 @@ WORKLOADS: Dict[str, Workload] = {w.name: w for w in [
     # Large batch, G=8, ~8.6 GB of V, lengths in [C/4, C].
     Workload("large_b32_c131072_hq64_hkv8_d128_ragged", 32, 131072, 64, 8, 128, "bf16",
              1.0, 2.0, 32768, 131072),
+    # V-traffic comparison shape: Llama-style heads (G=4) with 537 MB of V, four
+    # times the L2, so per-head re-reads of V cannot all be L2 hits.
+    Workload("traffic_b8_c32768_hq32_hkv8_d128", 8, 32768, 32, 8, 128, "bf16", 1.0, 2.0),
 ]}
 
 # Short aliases, in the order above.
@@ -91,6 +94,7 @@ ALIASES = {
     "phi": "phi_b4_c16384_hq24_hkv8_d128_ragged",
     "mqa": "mqa_b8_c32768_hq16_hkv1_d256_fp16_ragged",
     "large": "large_b32_c131072_hq64_hkv8_d128_ragged",
+    "traffic": "traffic_b8_c32768_hq32_hkv8_d128",
 }
 
 
