@@ -301,10 +301,11 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
   // two); with many tiles it runs in waves (a split with no context exits at
   // once) and splits only balance ragged lengths.
   p->tiles = p->hgroups * B * p->ndt;
-  // The tensor-core kernel runs one CTA per SM (its tensor memory limits
-  // residency) and pays a fixed cost per CTA: with few tiles it is given
-  // about three waves of short splits instead, which also balances ragged
-  // lengths (measured faster than one wave of long splits).
+  // The tensor-core kernel keeps a small ring, so two of its CTAs share an
+  // SM (measured: the occupancy query reports one, but per-SM traces show
+  // two alive at once), and it pays a fixed cost per CTA: with few tiles it
+  // is given about three times as many short splits as there are SMs, which
+  // also balances ragged lengths (measured faster than one long split per SM).
   const bool few_tiles = !(t && t->nsplit > 0) && p->tiles < di.sms;
   const bool one_wave = few_tiles && !tensor;
   long long want;
@@ -335,11 +336,12 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
     p->R = t->rows_per_stage;
     iters = (rps0 + p->R - 1) / p->R;
   } else {
-    // The tensor-core kernel pays a fixed cost per stage (measured): about
-    // 48 KiB of V per stage there (16 KiB for its short splits), 32 KiB for
-    // the FMA kernel.
+    // The tensor-core kernel runs faster the less shared memory a CTA holds
+    // (measured: more CTAs stay resident, and the next call's CTAs start on an
+    // SM while this call drains): 12 KiB of V per stage (16 KiB for the short
+    // splits of few-tile shapes) in a 3-stage ring. 32 KiB for the FMA kernel.
     const int row_bytes = tensor ? 256 : 2 * p->dt;
-    const int stage_bytes = tensor ? (few_tiles ? 16384 : 49152) : 32768;
+    const int stage_bytes = tensor ? (few_tiles ? 16384 : 12288) : 32768;
     const int rmax = std::max(rq, std::min(256, stage_bytes / row_bytes) / rq * rq);
     iters = (rps0 + rmax - 1) / rmax;
     p->R = static_cast<int>(align_up((rps0 + iters - 1) / iters, rq));
