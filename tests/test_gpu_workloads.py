@@ -35,24 +35,44 @@ def _gate(got, ref, what):
     assert err <= tol, f"{what}: max|gpu-oracle| = {err:.3e} > {tol:.3e}"
 
 
+_REFS = {}
+
+
+def _dense_case(name):
+    """Inputs (NaN padding) and the oracle's result, drawn once per workload."""
+    if name not in _REFS:
+        w = W.get(name)
+        x = W.generate(w, "cpu", pad="nan")
+        ref = oracle.gqa_av(x["attn"].numpy(), bits(x["v"]), w.v_dtype, x["seq_lens"].numpy(),
+                            nthreads=oracle.host_cores())
+        _REFS[name] = (w, x, ref)
+    return _REFS[name]
+
+
+@pytest.mark.parametrize("engine", [0, 1, 2], ids=["auto", "fma", "tensor"])
 @pytest.mark.parametrize("name", ["small", "llama", "phi", "mqa"])
-def test_workload_dense(gq, name):
-    w = W.get(name)
-    x = W.generate(w, "cpu", pad="nan")
-    ref = oracle.gqa_av(x["attn"].numpy(), bits(x["v"]), w.v_dtype, x["seq_lens"].numpy(),
-                        nthreads=oracle.host_cores())
+def test_workload_dense(gq, name, engine):
+    w, x, ref = _dense_case(name)
     dev = torch.device("cuda")
     attn, v, sl = x["attn"].to(dev), x["v"].to(dev), x["seq_lens"].to(dev)
+    tuning = dict(engine=engine) if engine else None
+
+    def call(out, mode=gq.MODE_AUTO):
+        if tuning is None:
+            gq.gqa_av_decode(attn, v, sl, out, mode=mode)
+        else:
+            gq.gqa_av_decode_tuned(attn, v, sl, out, mode=mode, tuning=tuning)
+
     outs = []
     for mode in (gq.MODE_AUTO, gq.MODE_GQA, gq.MODE_PER_HEAD):
         out = torch.full((w.B, w.Hq, w.D), float("nan"), device=dev)
-        gq.gqa_av_decode(attn, v, sl, out, mode=mode)
+        call(out, mode)
         gq.gqa_av_device_status()
         got = out.cpu().double().numpy()
-        _gate(got, ref, f"{name} mode={mode}")
+        _gate(got, ref, f"{name} mode={mode} engine={engine}")
         outs.append(got)
     again = torch.empty((w.B, w.Hq, w.D), device=dev)
-    gq.gqa_av_decode(attn, v, sl, again)
+    call(again)
     assert np.array_equal(again.cpu().double().numpy(), outs[0]), "not bitwise reproducible"
 
 
@@ -83,3 +103,8 @@ def test_workload_large_sampled(gq):
     gq.gqa_av_device_status()
     tol = TOL * max(1.0, float(out.abs().max()))
     assert float((per - out).abs().max()) <= tol
+    # The other engine on the whole output (the library picks tensor cores here).
+    fma = torch.empty_like(out)
+    gq.gqa_av_decode_tuned(attn, v, sl, fma, tuning=dict(engine=1))
+    gq.gqa_av_device_status()
+    assert float((fma - out).abs().max()) <= tol
