@@ -174,6 +174,7 @@ struct Plan {
   int nmma;                                // tensor core: N (heads padded to 16)
   int v_halves;                            // tensor core: 64-column V boxes per stage
   int tmem_cols;                           // tensor core: tensor-memory columns
+  int cvt_warps;                           // tensor core: weight-conversion warps
   uint32_t b_off;                          // tensor core: B ring offset
   int attn_tma;                            // attn weights by TMA (rows of Hq % 4 == 0 floats)
   uint32_t v_stage_bytes, a_off, bar_off;
@@ -271,6 +272,10 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
 
   if (tensor) {
     // One MMA covers 128 output columns; D <= 64 leaves the second half idle.
+    // Two weight-conversion warps (8 warps, up to four CTAs an SM) where the
+    // shape has fewer tiles than SMs, four (10 warps, two CTAs an SM) where
+    // many long CTAs run in waves: each measured faster in its regime.
+    p->cvt_warps = B * p->hgroups * ((D + kMmaM - 1) / kMmaM) < di.sms ? 2 : 4;
     p->dt = std::min(D, kMmaM);
     p->nmma = static_cast<int>(align_up(p->heads, 16));
     p->v_halves = p->dt > 64 ? 2 : 1;
@@ -291,6 +296,7 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
     p->nmma = 0;
     p->v_halves = 0;
     p->tmem_cols = 0;
+    p->cvt_warps = 0;
   }
   p->ndt = D / p->dt;
   p->ct = p->dt / 8;
@@ -338,10 +344,11 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
   } else {
     // The tensor-core kernel runs faster the less shared memory a CTA holds
     // (measured: more CTAs stay resident, and the next call's CTAs start on an
-    // SM while this call drains): 12 KiB of V per stage (16 KiB for the short
-    // splits of few-tile shapes) in a 3-stage ring. 32 KiB for the FMA kernel.
+    // SM while this call drains): 12 KiB of V per stage in a 3-stage ring, or
+    // 16 KiB for the short splits of shapes with under 48 tiles (measured
+    // faster there). 32 KiB for the FMA kernel.
     const int row_bytes = tensor ? 256 : 2 * p->dt;
-    const int stage_bytes = tensor ? (few_tiles ? 16384 : 12288) : 32768;
+    const int stage_bytes = tensor ? (few_tiles && p->tiles < 48 ? 16384 : 12288) : 32768;
     const int rmax = std::max(rq, std::min(256, stage_bytes / row_bytes) / rq * rq);
     iters = (rps0 + rmax - 1) / rmax;
     p->R = static_cast<int>(align_up((rps0 + iters - 1) / iters, rq));
@@ -428,6 +435,7 @@ void fill_params(Params* p, const Plan& pl, const float* attn, const int32_t* se
   p->v_stage_bytes = pl.v_stage_bytes; p->a_off = pl.a_off; p->bar_off = pl.bar_off;
   p->timeout_ns = kWaitTimeoutNs;
   p->v_halves = pl.v_halves; p->b_off = pl.b_off; p->tmem_cols = static_cast<uint32_t>(pl.tmem_cols);
+  p->cvt_warps = pl.cvt_warps;
   // attn is 16-byte aligned (checked before planning): a TMA source or a
   // cp.async of up to 16 bytes can start at any 4-head boundary of it.
 }
@@ -661,7 +669,7 @@ int gqa_av_plan(int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode,
   info->rows_per_split = p.rows_per_split;
   info->tiles = p.tiles;
   info->ctas = p.tiles * p.nsplit;
-  info->threads_per_cta = p.engine == kEngineTensor ? kMmaThreads : cta_threads(p.gc);
+  info->threads_per_cta = p.engine == kEngineTensor ? mma_threads(p.cvt_warps) : cta_threads(p.gc);
   info->engine = p.engine;
   info->smem_bytes = p.smem;
   info->ctas_per_sm = p.occ;

@@ -42,7 +42,7 @@ template <typename Tag, int NB>
 cudaError_t launch_mma(const Params& p, int grid, int smem_bytes, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kMmaThreads);
+  cfg.blockDim = dim3(mma_threads(p.cvt_warps));
   cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -60,7 +60,7 @@ cudaError_t occupancy_mma(int smem_limit, int smem_bytes, int* ctas_per_sm) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem_limit);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, gqa_av_mma_kernel<Tag, NB>,
-                                                       kMmaThreads, smem_bytes);
+                                                       kMmaMaxThreads, smem_bytes);
 }
 
 #define GQA_AV_INSTANTIATE_MMA(TAG, NB)                                                  \

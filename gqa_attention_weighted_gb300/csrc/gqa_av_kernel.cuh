@@ -90,6 +90,7 @@ struct alignas(64) Params {
   int v_halves;                 // 64-column V boxes per stage (1 or 2)
   uint32_t b_off;               // shared-memory offset of the B (weights) ring
   uint32_t tmem_cols;           // tensor-memory columns allocated (4 x N, power of 2 >= 32)
+  int cvt_warps;                // weight-conversion warps (2 or 4)
 };
 
 // The split combine: out[tile column] = sum over the tile's splits with

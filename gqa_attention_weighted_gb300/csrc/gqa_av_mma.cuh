@@ -32,9 +32,12 @@
 //
 // Warp roles, each waiting only on its own inputs so the stages overlap:
 // warps 0-3 accumulate (warp w reads tensor-memory lanes 32w..32w+31 = output
-// columns), warps 4-7 write the weights of each stage as the B operand, warp 8
-// is the TMA producer, and warp 9 allocates tensor memory and one of its
-// threads issues the MMAs. Split partials and
+// columns), the next 2 or 4 warps write the weights of each stage as the B
+// operand, then come the TMA producer warp and a warp that allocates tensor
+// memory and one of whose threads issues the MMAs. With 2 converter warps the
+// CTA's 8 warps spread evenly over the SM's four sub-partitions, so with at
+// most 64 registers a thread (one 16-head block) four CTAs fit on an SM by
+// registers; with 4 (10 warps) two do. Split partials and
 // the split combine are the FMA kernel's (same workspace layout). Every
 // mbarrier wait is bounded; on expiry the CTA sets the device status word,
 // lets its copies and MMAs in flight finish, frees its tensor memory and
@@ -49,10 +52,10 @@ namespace gqa_av {
 
 constexpr int kMmaM = 128;         // output columns per MMA (D rows)
 constexpr int kMmaAccWarps = 4;    // warps 0-3: one per tensor-memory lane quarter
-constexpr int kMmaCvtWarps = 4;    // warps 4-7: weight conversion
-constexpr int kMmaProducerWarp = kMmaAccWarps + kMmaCvtWarps;
-constexpr int kMmaIssuerWarp = kMmaProducerWarp + 1;
-constexpr int kMmaThreads = 32 * (kMmaIssuerWarp + 1);
+constexpr int kMmaMaxCvtWarps = 4;  // weight-conversion warps: 2 or 4 (a plan choice)
+constexpr int kMmaMaxThreads = 32 * (kMmaAccWarps + kMmaMaxCvtWarps + 2);
+// Threads of a CTA with `cvt` converter warps (+ producer and MMA warps).
+__host__ __device__ constexpr int mma_threads(int cvt) { return 32 * (kMmaAccWarps + cvt + 2); }
 constexpr unsigned kErrMmaWait = 8u;
 
 // tcgen05 shared-memory matrix descriptor: start address, leading- and
@@ -148,7 +151,8 @@ __device__ __forceinline__ void mma_team_sync() {
 //   [mbarriers: full, empty, bready (kMaxStages each), dfull[2], dfree[2], drain]
 //   [tensor-memory address]
 template <typename Tag, int NB>
-__global__ void __launch_bounds__(kMmaThreads, 1) gqa_av_mma_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kMmaMaxThreads, NB == 1 ? 3 : (NB == 2 ? 2 : 1))
+    gqa_av_mma_kernel(const __grid_constant__ Params p) {
   constexpr int N = 16 * NB;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_addr(smem_raw);
@@ -158,6 +162,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gqa_av_mma_kernel(const __grid
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  const int cvt_warps = p.cvt_warps;
+  const int producer_warp = kMmaAccWarps + cvt_warps;
+  const int issuer_warp = producer_warp + 1;
 
   const int tiles_per_hg = p.B * p.ndt;
   const int tile = blockIdx.x / p.nsplit;
@@ -187,7 +194,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gqa_av_mma_kernel(const __grid
   const uint32_t drain = smem_addr(bars + 3 * kMaxStages + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * kMaxStages + 5);
 
-  if (warp == kMmaIssuerWarp) {
+  if (warp == issuer_warp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(tmem_slot)),
                  "r"(p.tmem_cols)
@@ -198,7 +205,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gqa_av_mma_kernel(const __grid
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(full0 + 8 * s, p.attn_tma ? 1 : 1 + 32);
       mbar_init(empty0 + 8 * s, 1);                     // one tcgen05.commit per stage
-      mbar_init(bready0 + 8 * s, kMmaCvtWarps);         // one arrival per converter warp
+      mbar_init(bready0 + 8 * s, cvt_warps);            // one arrival per converter warp
     }
     for (int j = 0; j < 2; ++j) {
       mbar_init(dfull0 + 8 * j, 1);
@@ -207,7 +214,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gqa_av_mma_kernel(const __grid
     mbar_init(drain, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == kMmaProducerWarp && lane == 0) {
+  if (warp == producer_warp && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.v_map)) : "memory");
     if (p.attn_tma)
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.a_map)) : "memory");
@@ -221,7 +228,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gqa_av_mma_kernel(const __grid
   grid_dependency_wait();
   grid_launch_dependents();
 
-  if (warp == kMmaProducerWarp) {
+  if (warp == producer_warp) {
     // ----------------------------------------------------------------- producer
     const float* attn_b = p.attn + (size_t)b * p.Cmax * p.Hq + h0;
     const int per_row = p.heads / p.avec;
@@ -295,7 +302,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gqa_av_mma_kernel(const __grid
   const int n_iters = split < nsplit_b ? max((c_end - c_begin + p.R - 1) / p.R, 1) : 0;
   const uint32_t b_half = (uint32_t)N * p.R * 2;   // bytes of one of hi / lo
 
-  if (warp == kMmaIssuerWarp) {
+  if (warp == issuer_warp) {
     // -------------------------------------------------------------- MMA issuer
     bool ok = true;
     if (lane == 0) {
@@ -360,7 +367,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gqa_av_mma_kernel(const __grid
       const int valid = min(p.R, c_end - c0);
       const float* ast = aring + (size_t)stage * p.R * p.ap + a_shift;
       uint8_t* bst = smem + p.b_off + (size_t)stage * 2 * b_half;
-      for (int t = ctid; t < items; t += kMmaCvtWarps * 32) {
+      for (int t = ctid; t < items; t += cvt_warps * 32) {
         const int n = t % N, kc = t / N;
         float w[8];
 #pragma unroll
@@ -379,7 +386,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gqa_av_mma_kernel(const __grid
       if (valid < p.R) {
         uint8_t* vst = smem + (size_t)stage * p.v_stage_bytes;
         const int chunks = (p.R - valid) * 8;  // 16-byte chunks of one half
-        for (int t = ctid; t < chunks * p.v_halves; t += kMmaCvtWarps * 32) {
+        for (int t = ctid; t < chunks * p.v_halves; t += cvt_warps * 32) {
           const int h = t / chunks, c = t - h * chunks;
           const int k = valid + c / 8;
           const size_t off = (size_t)h * (p.v_stage_bytes / 2) + (size_t)(k >> 3) * 1024 +
