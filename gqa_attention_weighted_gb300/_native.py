@@ -38,13 +38,14 @@ class GqaAvError(RuntimeError):
 class Tuning(ctypes.Structure):
     _fields_ = [("nsplit", ctypes.c_int), ("dtile", ctypes.c_int),
                 ("rows_per_stage", ctypes.c_int), ("stages", ctypes.c_int),
-                ("early_stages", ctypes.c_int), ("engine", ctypes.c_int)]
+                ("early_stages", ctypes.c_int), ("engine", ctypes.c_int),
+                ("split_mode", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "mode", "heads_per_cta", "head_chunk", "dtile", "rows_per_stage", "stages",
-        "early_stages", "engine", "nsplit",
+        "early_stages", "engine", "split_mode", "nsplit",
         "combine_ctas", "rows_per_split", "tiles", "ctas", "threads_per_cta", "smem_bytes",
         "ctas_per_sm")] + [
         ("workspace_bytes", ctypes.c_size_t)]
@@ -159,7 +160,8 @@ def _tuning(t) -> Optional[Tuning]:
         return t
     return Tuning(int(t.get("nsplit", 0)), int(t.get("dtile", 0)),
                   int(t.get("rows_per_stage", 0)), int(t.get("stages", 0)),
-                  int(t.get("early_stages", 0)), int(t.get("engine", 0)))
+                  int(t.get("early_stages", 0)), int(t.get("engine", 0)),
+                  int(t.get("split_mode", 0)))
 
 
 def gqa_av_decode_tuned(attn, v_cache, seq_lens, out, mode=MODE_AUTO, tuning=None,

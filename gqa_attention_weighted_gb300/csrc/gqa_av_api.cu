@@ -167,7 +167,11 @@ int ctas_per_sm(int dev, int smem_limit, int v_dtype, int engine, int sel, int s
 struct Plan {
   int mode, heads, gc, nc, dt, ndt, ct, row_par, R, stages, nsplit, rows_per_split;
   int hgroups, tiles, ap, avec, smem, occ;
-  int parts, cols_per_cta, ctas_per_tile;  // split combine launch (nsplit > 1)
+  int parts, cols_per_cta, ctas_per_tile;  // split combine launch (combine set)
+  int combine;                             // the split combine runs after the main kernel
+  int grid;                                // CTAs of the main kernel
+  int split_units;                         // tensor core: CTAs the context is balanced over
+  int balanced;                            // tensor core: splits balanced over the batch's lengths
   int one_per_sm;                          // shared memory padded so one CTA fits per SM
   int early;                               // stages issued before the length is read
   int engine;                              // kEngineFma or kEngineTensor
@@ -210,7 +214,7 @@ void layout_mma(Plan* p, int min_smem) {
   p->b_off = static_cast<uint32_t>(align_up(p->a_off + aring, 128));
   const size_t bring = static_cast<size_t>(p->stages) * 2 * p->nmma * p->R * 2;
   p->bar_off = static_cast<uint32_t>(align_up(p->b_off + bring, 16));
-  const size_t bars = (3 * kMaxStages + 5) * 8 + 8;
+  const size_t bars = (3 * kMaxStages + 5) * 8 + 8 + 48;  // + the CTA's split record (9 ints)
   p->smem = std::max(static_cast<int>(p->bar_off + bars + 1024), min_smem);
 }
 
@@ -355,8 +359,27 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
   }
   p->rows_per_split = p->R * iters;
   p->nsplit = (Cmax + p->rows_per_split - 1) / p->rows_per_split;
-  if (static_cast<long long>(p->tiles) * p->nsplit > 0x7fffffffLL)
-    return fail(GQA_AV_ERR_UNSUPPORTED, "grid too large");
+  // Splits of the tensor-core kernel on shapes that run in waves (as many
+  // tiles as SMs or more): the context rows of the whole batch, read from
+  // seq_lens, are spread evenly over tiles x nsplit CTAs, so ragged lengths
+  // leave no CTA idle and every wave is full (measured 12% faster on the
+  // ragged large-batch shape); rounding can give each sequence one split
+  // more, so the grid has tiles more CTAs, and the split combine always runs.
+  // With fewer tiles than SMs the grid is one wave and fixed splits are
+  // faster: a CTA issues its first stage before it reads any length.
+  const int want_split = t && t->split_mode > 0 ? t->split_mode : 0;
+  if (want_split > 2)
+    return fail(GQA_AV_ERR_INVALID, "split_mode=%d must be 0 (auto), 1 (fixed) or 2 (balanced)",
+                want_split);
+  if (want_split == 2 && !tensor)
+    return fail(GQA_AV_ERR_UNSUPPORTED, "balanced splits need the tensor-core engine");
+  p->balanced = tensor && (want_split == 2 || (want_split == 0 && p->tiles >= di.sms));
+  const long long grid =
+      static_cast<long long>(p->tiles) * (p->balanced ? p->nsplit + 1 : p->nsplit);
+  if (grid > 0x7fffffffLL) return fail(GQA_AV_ERR_UNSUPPORTED, "grid too large");
+  p->grid = static_cast<int>(grid);
+  p->split_units = p->balanced ? p->tiles * p->nsplit : 0;
+  p->combine = p->balanced || p->nsplit > 1;
 
   if (t && t->stages > 0) {
     if (t->stages < 2 || t->stages > kMaxStages)
@@ -398,18 +421,21 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
   } else {
     p->early = 1;
   }
+  // With balanced splits a CTA finds its split from the lengths, so it issues
+  // nothing before it has read them.
+  if (p->balanced) p->early = 0;
 
   if ((rc = ctas_per_sm(dev, di.smem_optin, v_dtype, p->engine, kernel_sel(*p), p->smem,
                         &p->occ)))
     return rc;
   if (p->occ < 1) return fail(GQA_AV_ERR_UNSUPPORTED, "kernel does not fit on an SM");
 
-  p->ws_bytes = p->nsplit > 1
-                    ? static_cast<size_t>(p->tiles) * p->nsplit * p->heads * p->dt * sizeof(float)
-                    : 0;
+  p->ws_bytes = p->combine
+                    ? static_cast<size_t>(p->grid) * p->heads * p->dt * sizeof(float)
+                    : 0;  // one partial slot a CTA
   // Split combine: `parts` threads per float4 column, a power of two <= 16.
   p->parts = 1;
-  while (p->parts < 16 && p->parts < p->nsplit) p->parts *= 2;
+  while (p->parts < 16 && (p->balanced || p->parts < p->nsplit)) p->parts *= 2;
   p->cols_per_cta = kCombineThreads / p->parts;
   const int ncol4 = p->heads * p->dt / 4;
   p->ctas_per_tile = (ncol4 + p->cols_per_cta - 1) / p->cols_per_cta;
@@ -436,6 +462,8 @@ void fill_params(Params* p, const Plan& pl, const float* attn, const int32_t* se
   p->timeout_ns = kWaitTimeoutNs;
   p->v_halves = pl.v_halves; p->b_off = pl.b_off; p->tmem_cols = static_cast<uint32_t>(pl.tmem_cols);
   p->cvt_warps = pl.cvt_warps;
+  p->split_units = pl.split_units;
+  p->balanced = pl.balanced;
   // attn is 16-byte aligned (checked before planning): a TMA source or a
   // cp.async of up to 16 bytes can start at any 4-head boundary of it.
 }
@@ -443,8 +471,8 @@ void fill_params(Params* p, const Plan& pl, const float* attn, const int32_t* se
 // Launches the main kernel and, when the tile has several splits, the split
 // combine right after it on the same stream.
 cudaError_t launch_call(const Kernel& kern, const Plan& pl, const Params& p, cudaStream_t stream) {
-  cudaError_t e = kern.launch(p, pl.tiles * pl.nsplit, pl.smem, stream);
-  if (e != cudaSuccess || pl.nsplit == 1) return e;
+  cudaError_t e = kern.launch(p, pl.grid, pl.smem, stream);
+  if (e != cudaSuccess || !pl.combine) return e;
   CombineParams c;
   c.ws = p.ws;
   c.seq_lens = p.seq_lens;
@@ -454,6 +482,8 @@ cudaError_t launch_call(const Kernel& kern, const Plan& pl, const Params& p, cud
   c.rows_per_split = pl.rows_per_split; c.nsplit = pl.nsplit;
   c.tile_elems = pl.heads * pl.dt;
   c.parts = pl.parts; c.cols_per_cta = pl.cols_per_cta; c.ctas_per_tile = pl.ctas_per_tile;
+  c.balanced = pl.balanced;
+  c.R = pl.R; c.hgroups = pl.hgroups; c.split_units = pl.split_units;
   return launch_combine(c, pl.tiles * pl.ctas_per_tile, stream);
 }
 
@@ -619,7 +649,8 @@ cudaError_t launch_combine(const CombineParams& p, int grid, cudaStream_t stream
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gqa_av_combine_kernel, p);
+  cudaError_t e = p.balanced ? cudaLaunchKernelEx(&cfg, gqa_av_combine_kernel<true>, p)
+                             : cudaLaunchKernelEx(&cfg, gqa_av_combine_kernel<false>, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -665,12 +696,13 @@ int gqa_av_plan(int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode,
   info->stages = p.stages;
   info->early_stages = p.early;
   info->nsplit = p.nsplit;
-  info->combine_ctas = p.nsplit > 1 ? p.tiles * p.ctas_per_tile : 0;
+  info->combine_ctas = p.combine ? p.tiles * p.ctas_per_tile : 0;
   info->rows_per_split = p.rows_per_split;
   info->tiles = p.tiles;
-  info->ctas = p.tiles * p.nsplit;
+  info->ctas = p.grid;
   info->threads_per_cta = p.engine == kEngineTensor ? mma_threads(p.cvt_warps) : cta_threads(p.gc);
   info->engine = p.engine;
+  info->split_mode = p.balanced ? 2 : 1;
   info->smem_bytes = p.smem;
   info->ctas_per_sm = p.occ;
   info->workspace_bytes = kHeaderBytes + p.ws_bytes;

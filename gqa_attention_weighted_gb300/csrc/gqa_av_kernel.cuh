@@ -63,7 +63,7 @@ struct alignas(64) Params {
   const float* attn;            // [B, Cmax, Hq]
   const int32_t* seq_lens;      // [B] or null
   float* out;                   // [B, Hq, D]
-  float* ws;                    // [tiles][nsplit][heads * dt] split partials
+  float* ws;                    // split partials: [tiles][nsplit][heads * dt], or one slot a CTA
   unsigned int* status;         // device status word
   int B, Cmax, Hq, Hkv, D, G;
   int heads;                    // query heads per CTA
@@ -91,12 +91,14 @@ struct alignas(64) Params {
   uint32_t b_off;               // shared-memory offset of the B (weights) ring
   uint32_t tmem_cols;           // tensor-memory columns allocated (4 x N, power of 2 >= 32)
   int cvt_warps;                // weight-conversion warps (2 or 4)
+  int split_units;              // CTAs the batch's context is spread over (length-balanced splits)
+  int balanced;                 // splits balanced over the batch's lengths (else fixed)
 };
 
 // The split combine: out[tile column] = sum over the tile's splits with
 // context, ws[tile][s][column], in split order.
 struct CombineParams {
-  const float* ws;              // [tiles][nsplit][tile_elems]
+  const float* ws;              // [tiles][nsplit][tile_elems], or one slot a CTA (balanced)
   const int32_t* seq_lens;      // [B] or null
   float* out;                   // [B, Hq, D]
   int B, Cmax, Hq, D;
@@ -106,6 +108,8 @@ struct CombineParams {
   int parts;                    // threads per column (fixed chunks of splits)
   int cols_per_cta;             // float4 columns per CTA (kCombineThreads / parts)
   int ctas_per_tile;
+  int balanced;                 // length-balanced splits of the tensor-core kernel
+  int R, hgroups, split_units;  // their stage rows, head groups and CTA count
 };
 
 // ---------------------------------------------------------------------------
@@ -184,6 +188,18 @@ __device__ __forceinline__ void grid_dependency_wait() {
 }
 __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Named barrier `id` of `count` threads (a multiple of 32). The warp is
+// reconverged first and the unaligned form is used, so a warp whose lanes
+// left divergent code apart still arrives as one warp.
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
+  __syncwarp();
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_arrive(uint32_t id, uint32_t count) {
+  __syncwarp();
+  asm volatile("barrier.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -313,6 +329,90 @@ __device__ __forceinline__ void sum_strided(float4& s, const float4* src, size_t
     for (int i = 0; i < kBatch; ++i)
       if (i0 + i < hi) add4(s, x[i]);
   }
+}
+
+// ---------------------------------------------------------------------------
+// Length-balanced splits (the tensor-core kernel and its combine).
+//
+// The context rows of the whole batch are spread evenly over `units` CTAs,
+// whatever the lengths: sequence b (length L_b, ceil(L_b / R) stages of R
+// rows) is cut into n_b = max(1, ceil(ceil(L_b / R) / sps)) splits of sps
+// stages, where sps = ceil(K * sum_b ceil(L_b / R) / units) and K = hgroups *
+// ndt is the number of tiles of one sequence. CTA u takes tile k = u % K of
+// its sequence and batch split q = u / K, which is split q - P_b of the
+// sequence b with P_b <= q < P_b + n_b (P_b = n_0 + ... + n_{b-1}); at most
+// units + K * B CTAs have work and the rest exit. A split's partial is slot u
+// of the workspace, so the partials of one tile lie K slots apart.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int clamped_len(const int32_t* seq_lens, int b, int Cmax) {
+  const int L = seq_lens ? seq_lens[b] : Cmax;
+  return L < 0 ? 0 : (L > Cmax ? Cmax : L);
+}
+
+__device__ __forceinline__ int balanced_splits_of(int L, int R, int sps) {
+  const int n = ((L + R - 1) / R + sps - 1) / sps;
+  return n > 1 ? n : 1;
+}
+
+// Stages per split. Warp-collective: all 32 lanes take part.
+__device__ __forceinline__ int balanced_sps(const int32_t* seq_lens, int B, int Cmax, int R, int K,
+                                            int units) {
+  long long s = 0;
+  for (int b = threadIdx.x & 31; b < B; b += 32)
+    s += (clamped_len(seq_lens, b, Cmax) + R - 1) / R;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const long long sps = (s * K + units - 1) / units;
+  return sps > 1 ? static_cast<int>(sps) : 1;
+}
+
+struct BalancedSplit {
+  int b, L;        // sequence and its clamped length
+  int split, n;    // split of the sequence and the sequence's split count
+  int found;       // 0: the batch has fewer splits than q + 1
+};
+
+// Sequence and split of batch split q. Warp-collective.
+__device__ __forceinline__ BalancedSplit balanced_find(const int32_t* seq_lens, int B, int Cmax,
+                                                       int R, int sps, int q) {
+  const int lane = threadIdx.x & 31;
+  int base = 0;  // splits of the sequences before this chunk of 32
+  for (int b0 = 0; b0 < B; b0 += 32) {
+    const int b = b0 + lane;
+    const int L = b < B ? clamped_len(seq_lens, b, Cmax) : 0;
+    const int n = b < B ? balanced_splits_of(L, R, sps) : 0;
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, n > 0 && q >= base + incl - n && q < base + incl);
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      BalancedSplit r;
+      r.b = b0 + src;
+      r.L = __shfl_sync(0xffffffffu, L, src);
+      r.n = __shfl_sync(0xffffffffu, n, src);
+      r.split = q - base - __shfl_sync(0xffffffffu, incl - n, src);
+      r.found = 1;
+      return r;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  BalancedSplit none{0, 0, 0, 0, 0};
+  return none;
+}
+
+// P_b (splits of the sequences before b) and n_b. Warp-collective.
+__device__ __forceinline__ int2 balanced_prefix(const int32_t* seq_lens, int Cmax, int R, int sps,
+                                                int b) {
+  int s = 0;
+  for (int i = threadIdx.x & 31; i < b; i += 32)
+    s += balanced_splits_of(clamped_len(seq_lens, i, Cmax), R, sps);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return make_int2(s, balanced_splits_of(clamped_len(seq_lens, b, Cmax), R, sps));
 }
 
 // Two fp32 lanes in one 64-bit register pair, and the packed FMA on them:
@@ -579,8 +679,10 @@ gqa_av_kernel(const __grid_constant__ Params p) {
 // ---------------------------------------------------------------------------
 // The split combine. CTA (tile, column block): `parts` threads per float4
 // column each sum a fixed chunk of the splits (their loads in flight
-// together), then the chunks are added in chunk order.
+// together), then the chunks are added in chunk order. kBalanced: the
+// partials of length-balanced splits (one slot a CTA of the main kernel).
 // ---------------------------------------------------------------------------
+template <bool kBalanced>
 __global__ void __launch_bounds__(kCombineThreads)
 gqa_av_combine_kernel(const __grid_constant__ CombineParams p) {
   __shared__ float4 chunk_sum[kCombineThreads];
@@ -596,25 +698,43 @@ gqa_av_combine_kernel(const __grid_constant__ CombineParams p) {
   // grid this one depends on, does not write it, and the main kernel started
   // (and so could trigger this launch) only after everything before it was
   // done.
-  int L = p.seq_lens ? p.seq_lens[b] : p.Cmax;
-  L = L < 0 ? 0 : (L > p.Cmax ? p.Cmax : L);
-  const int nunit = L > 0 ? (L + p.rows_per_split - 1) / p.rows_per_split : 1;
-  const int ncl = p.nsplit;
+  const int ncol4 = p.tile_elems >> 2;
+  int nunit;              // splits of the tile
+  size_t first, stride;   // float4 offsets of its split 0 and between its splits
+  if constexpr (kBalanced) {
+    __shared__ int2 prefix;
+    if (threadIdx.x < 32) {
+      const int K = p.hgroups * p.ndt;
+      const int sps = balanced_sps(p.seq_lens, p.B, p.Cmax, p.R, K, p.split_units);
+      const int2 r = balanced_prefix(p.seq_lens, p.Cmax, p.R, sps, b);
+      if (threadIdx.x == 0) prefix = r;
+    }
+    __syncthreads();
+    const int K = p.hgroups * p.ndt;
+    nunit = prefix.y;
+    first = ((size_t)prefix.x * K + hg * p.ndt + dti) * ncol4;
+    stride = (size_t)K * ncol4;
+  } else {
+    int L = p.seq_lens ? p.seq_lens[b] : p.Cmax;
+    L = L < 0 ? 0 : (L > p.Cmax ? p.Cmax : L);
+    nunit = L > 0 ? (L + p.rows_per_split - 1) / p.rows_per_split : 1;
+    first = (size_t)tile * p.nsplit * ncol4;
+    stride = ncol4;
+  }
   grid_dependency_wait();  // the partials of the main kernel are complete and visible
   grid_launch_dependents();
   if (nunit == 1) return;  // the main kernel wrote this tile's output
 
-  const int ncol4 = p.tile_elems >> 2;
   const int t = threadIdx.x;
   const int j = t / p.cols_per_cta;                     // chunk of splits
   const int col = blk * p.cols_per_cta + (t - j * p.cols_per_cta);
   const int chunk = (nunit + p.parts - 1) / p.parts;
   const int lo = j * chunk, hi = min(lo + chunk, nunit);
-  const float4* base = reinterpret_cast<const float4*>(p.ws) + (size_t)tile * ncl * ncol4;
+  const float4* base = reinterpret_cast<const float4*>(p.ws) + first;
   float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
   if (col < ncol4 && lo < hi) {
-    sum = __ldcg(base + (size_t)lo * ncol4 + col);
-    sum_strided<true>(sum, base + col, ncol4, lo + 1, hi);
+    sum = __ldcg(base + (size_t)lo * stride + col);
+    sum_strided<true>(sum, base + col, stride, lo + 1, hi);
   }
   chunk_sum[t] = sum;
   __syncthreads();

@@ -6,7 +6,11 @@
 //
 // One CTA owns the same tile as the FMA kernel (head group, b, d-tile of up to
 // 128 columns) and one context split of it, and reads each V row of its KV
-// head from HBM once for all heads of the group. Per pipeline stage of R
+// head from HBM once for all heads of the group. The splits are balanced over
+// the batch: after the dependency wait every CTA reads all sequence lengths
+// and cuts the batch's context rows into equal splits of whole stages (the
+// length-balanced split helpers in gqa_av_kernel.cuh), so short sequences
+// leave no CTA idle and every SM gets a like share of rows. Per pipeline stage of R
 // context rows it computes the stage's contribution
 //   D[m][n] = sum_k V[c0 + k][d0 + m] * attn[c0 + k][h0 + n]
 // as one tcgen05 matrix product with M = 128 (output columns), N = the group's
@@ -37,8 +41,8 @@
 // memory and one of whose threads issues the MMAs. With 2 converter warps the
 // CTA's 8 warps spread evenly over the SM's four sub-partitions, so with at
 // most 64 registers a thread (one 16-head block) four CTAs fit on an SM by
-// registers; with 4 (10 warps) two do. Split partials and
-// the split combine are the FMA kernel's (same workspace layout). Every
+// registers; with 4 (10 warps) two do. The split combine is the FMA kernel's,
+// reading one partial slot per CTA of this kernel. Every
 // mbarrier wait is bounded; on expiry the CTA sets the device status word,
 // lets its copies and MMAs in flight finish, frees its tensor memory and
 // returns.
@@ -141,7 +145,7 @@ __host__ __device__ constexpr float weight_unscale(Fp16Tag) { return 1.0f / 4096
 // Named barrier of the accumulator warps and the MMA warp: the warps that
 // touch tensor memory.
 __device__ __forceinline__ void mma_team_sync() {
-  asm volatile("bar.sync 2, %0;" ::"n"(32 * (kMmaAccWarps + 1)) : "memory");
+  named_sync(2, 32 * (kMmaAccWarps + 1));
 }
 
 // Shared memory (offsets from a 1024-byte-aligned base):
@@ -149,7 +153,90 @@ __device__ __forceinline__ void mma_team_sync() {
 //   [attn ring: stages x R x ap floats]
 //   [B ring: stages x 2N (hi rows, then lo rows) x R x 2 B]
 //   [mbarriers: full, empty, bready (kMaxStages each), dfull[2], dfree[2], drain]
-//   [tensor-memory address]
+//   [tensor-memory address] [the CTA's balanced split: 5 ints]
+// The split of CTA blockIdx.x (length-balanced, see gqa_av_kernel.cuh).
+struct MmaSplit {
+  int b, c_begin, c_end, n_iters, alone;
+  __device__ bool operator==(const MmaSplit& o) const {
+    return b == o.b && c_begin == o.c_begin && c_end == o.c_end && n_iters == o.n_iters &&
+           alone == o.alone;
+  }
+};
+
+// Warp-collective. seq_lens null: every length is Cmax.
+__device__ __forceinline__ MmaSplit mma_split(const int32_t* seq_lens, const Params& p, int K) {
+  const int sps = balanced_sps(seq_lens, p.B, p.Cmax, p.R, K, p.split_units);
+  const BalancedSplit bs =
+      balanced_find(seq_lens, p.B, p.Cmax, p.R, sps, static_cast<int>(blockIdx.x) / K);
+  MmaSplit r;
+  r.b = bs.b;
+  r.c_begin = bs.split * sps * p.R;
+  r.c_end = min(r.c_begin + sps * p.R, bs.L);
+  r.n_iters = bs.found ? max((r.c_end - r.c_begin + p.R - 1) / p.R, 1) : 0;
+  r.alone = bs.n == 1;
+  return r;
+}
+
+// Lengths a lane keeps in registers: batches of up to 256 sequences find
+// their split from one round of loads.
+constexpr int kLenRegs = 8;
+
+__device__ __forceinline__ void load_lens(const int32_t* seq_lens, int B, int Cmax,
+                                          int (&L)[kLenRegs]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int j = 0; j < kLenRegs; ++j) {
+    const int b = 32 * j + lane;
+    L[j] = b < B ? clamped_len(seq_lens, b, Cmax) : 0;
+  }
+}
+
+// mma_split from lengths in registers (B <= 32 * kLenRegs). Warp-collective.
+__device__ __forceinline__ MmaSplit split_from_lens(const int (&L)[kLenRegs], const Params& p,
+                                                    int K) {
+  const int lane = threadIdx.x & 31;
+  long long s = 0;
+#pragma unroll
+  for (int j = 0; j < kLenRegs; ++j) s += (L[j] + p.R - 1) / p.R;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const long long sps_l = (s * K + p.split_units - 1) / p.split_units;
+  const int sps = sps_l > 1 ? static_cast<int>(sps_l) : 1;
+  const int q = static_cast<int>(blockIdx.x) / K;
+  int base = 0, hb = -1, hL = 0, hn = 0, hsplit = 0;
+#pragma unroll
+  for (int j = 0; j < kLenRegs; ++j) {
+    if (32 * j < p.B && hb < 0) {  // warp-uniform
+      const int n = 32 * j + lane < p.B ? balanced_splits_of(L[j], p.R, sps) : 0;
+      int incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const unsigned hit =
+          __ballot_sync(0xffffffffu, n > 0 && q >= base + incl - n && q < base + incl);
+      if (hit) {
+        const int src = __ffs(hit) - 1;
+        hb = 32 * j + src;
+        hL = __shfl_sync(0xffffffffu, L[j], src);
+        hn = __shfl_sync(0xffffffffu, n, src);
+        hsplit = q - base - __shfl_sync(0xffffffffu, incl - n, src);
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  MmaSplit r{0, 0, 0, 0, 0};
+  if (hb >= 0) {
+    r.b = hb;
+    r.c_begin = hsplit * sps * p.R;
+    r.c_end = min(r.c_begin + sps * p.R, hL);
+    r.n_iters = max((r.c_end - r.c_begin + p.R - 1) / p.R, 1);
+    r.alone = hn == 1;
+  }
+  return r;
+}
+
 template <typename Tag, int NB>
 __global__ void __launch_bounds__(kMmaMaxThreads, NB == 1 ? 3 : (NB == 2 ? 2 : 1))
     gqa_av_mma_kernel(const __grid_constant__ Params p) {
@@ -165,21 +252,6 @@ __global__ void __launch_bounds__(kMmaMaxThreads, NB == 1 ? 3 : (NB == 2 ? 2 : 1
   const int cvt_warps = p.cvt_warps;
   const int producer_warp = kMmaAccWarps + cvt_warps;
   const int issuer_warp = producer_warp + 1;
-
-  const int tiles_per_hg = p.B * p.ndt;
-  const int tile = blockIdx.x / p.nsplit;
-  const int split = blockIdx.x - tile * p.nsplit;
-  const int hg = tile / tiles_per_hg;
-  const int rem = tile - hg * tiles_per_hg;
-  const int b = rem / p.ndt;
-  const int dti = rem - b * p.ndt;
-  const int h0 = hg * p.heads;
-  const int kv_h = h0 / p.G;
-  const int d0 = dti * p.dt;
-  const int c_begin = split * p.rows_per_split;
-  const int a_shift = p.attn_tma ? (h0 & 3) : 0;
-  const int pre = min(min(min(p.early_stages, p.stages), p.rows_per_split / p.R),
-                      (p.Cmax - c_begin + p.R - 1) / p.R);
 
   const uint32_t vring_s = base_s;
   const uint32_t aring_s = base_s + p.a_off;
@@ -225,14 +297,53 @@ __global__ void __launch_bounds__(kMmaMaxThreads, NB == 1 ? 3 : (NB == 2 ? 2 : 1
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // The CTA's tile and context split. Fixed splits (p.balanced == 0): CTA
+  // (tile, split) = (blockIdx / nsplit, blockIdx % nsplit), split s covering
+  // rows [s * rows_per_split, (s + 1) * rows_per_split) of its sequence, so
+  // the first stages can be issued before the length is read, and every warp
+  // reads the one length it needs itself. Balanced splits: tile k = blockIdx
+  // % K of a sequence the batch's lengths decide (length-balanced split
+  // helpers in gqa_av_kernel.cuh); the producer warp works the split out and
+  // hands it to the other warps through shared memory at named barrier 3.
+  // A CTA with no context rows has n_iters 0.
+  const int K = p.hgroups * p.ndt;
+  int hg, dti, tile = 0, split = 0;
+  if (p.balanced) {
+    const int k = blockIdx.x % K;
+    hg = k / p.ndt;
+    dti = k - hg * p.ndt;
+  } else {
+    tile = blockIdx.x / p.nsplit;
+    split = blockIdx.x - tile * p.nsplit;
+    hg = tile / (p.B * p.ndt);
+    dti = tile - hg * (p.B * p.ndt);
+    dti -= (dti / p.ndt) * p.ndt;
+  }
+  const int h0 = hg * p.heads;
+  const int kv_h = h0 / p.G;
+  const int d0 = dti * p.dt;
+  const int a_shift = p.attn_tma ? (h0 & 3) : 0;
+  const int b_fixed = p.balanced ? 0 : (tile - hg * (p.B * p.ndt)) / p.ndt;
+  int* split_info = reinterpret_cast<int*>(bars + 3 * kMaxStages + 6);
+  // The fixed split of this CTA once the sequence length is known.
+  auto fixed_split = [&](MmaSplit& f) {
+    const int L = clamped_len(p.seq_lens, b_fixed, p.Cmax);
+    const int nsplit_b = L > 0 ? (L + p.rows_per_split - 1) / p.rows_per_split : 1;
+    f.b = b_fixed;
+    f.c_begin = split * p.rows_per_split;
+    f.c_end = min(f.c_begin + p.rows_per_split, L);
+    f.n_iters = split < nsplit_b ? max((f.c_end - f.c_begin + p.R - 1) / p.R, 1) : 0;
+    f.alone = nsplit_b == 1;
+    return tile * p.nsplit + split;
+  };
+
   grid_dependency_wait();
   grid_launch_dependents();
 
   if (warp == producer_warp) {
     // ----------------------------------------------------------------- producer
-    const float* attn_b = p.attn + (size_t)b * p.Cmax * p.Hq + h0;
     const int per_row = p.heads / p.avec;
-    auto issue = [&](int stage, int c0, int rows) {
+    auto issue = [&](int stage, int b, int c0, int rows) {
       const uint32_t full = full0 + 8 * stage;
       const uint32_t vdst = vring_s + (uint32_t)stage * p.v_stage_bytes;
       if (lane == 0) {
@@ -246,41 +357,62 @@ __global__ void __launch_bounds__(kMmaMaxThreads, NB == 1 ? 3 : (NB == 2 ? 2 : 1
                       full, policy);
       }
       if (p.attn_tma) return;
-      const float* src = attn_b + (size_t)c0 * p.Hq;
+      const float* src = p.attn + ((size_t)b * p.Cmax + c0) * p.Hq + h0;
       const uint32_t dst = aring_s + 4u * (uint32_t)(stage * p.R * p.ap);
       const int n = rows * per_row;
       for (int i = lane; i < n; i += 32) {
-        const int r = i / per_row, k = (i - r * per_row) * p.avec;
-        const uint32_t d = dst + 4u * (r * p.ap + k);
-        const float* sp = src + (size_t)r * p.Hq + k;
+        const int r = i / per_row, col = (i - r * per_row) * p.avec;
+        const uint32_t d = dst + 4u * (r * p.ap + col);
+        const float* sp = src + (size_t)r * p.Hq + col;
         if (p.avec == 4) cp_async<16>(d, sp);
         else if (p.avec == 2) cp_async<8>(d, sp);
         else cp_async<4>(d, sp);
       }
       cp_async_arrive_noinc(full);
     };
-    int L = p.seq_lens ? p.seq_lens[b] : p.Cmax;
-    issue(0, c_begin, min(p.R, p.Cmax - c_begin));
-    for (int it = 1; it < pre; ++it) {
-      const int c0 = c_begin + it * p.R;
-      issue(it, c0, min(p.R, p.Cmax - c0));
+
+    MmaSplit f;
+    int pre = 0;
+    if (!p.balanced) {
+      // The first stage(s) go out before the length is read.
+      const int c_begin = split * p.rows_per_split;
+      pre = min(min(min(p.early_stages, p.stages), p.rows_per_split / p.R),
+                (p.Cmax - c_begin + p.R - 1) / p.R);
+      for (int it = 0; it < pre; ++it) {
+        const int c0 = c_begin + it * p.R;
+        issue(it, b_fixed, c0, min(p.R, p.Cmax - c0));
+      }
+      fixed_split(f);
+    } else {
+      if (p.B <= 32 * kLenRegs) {
+        int lens[kLenRegs];
+        load_lens(p.seq_lens, p.B, p.Cmax, lens);
+        f = split_from_lens(lens, p, K);
+      } else {
+        f = mma_split(p.seq_lens, p, K);
+      }
+      if (lane == 0) {
+        split_info[0] = f.b;
+        split_info[1] = f.c_begin;
+        split_info[2] = f.c_end;
+        split_info[3] = f.n_iters;
+        split_info[4] = f.alone;
+      }
+      named_arrive(3, blockDim.x);
     }
-    L = L < 0 ? 0 : (L > p.Cmax ? p.Cmax : L);
-    const int nsplit_b = L > 0 ? (L + p.rows_per_split - 1) / p.rows_per_split : 1;
-    const int c_end = min(c_begin + p.rows_per_split, L);
-    const int n_iters = split < nsplit_b ? max((c_end - c_begin + p.R - 1) / p.R, 1) : 0;
+
     int issued = pre;
     bool ok = true;
-    for (int it = pre; it < n_iters; ++it) {
+    for (int it = pre; it < f.n_iters; ++it) {
       const int stage = it % p.stages;
-      const uint32_t parity = ((it / p.stages) & 1) ^ 1;
+      const uint32_t parity = ((it / p.stages) & 1) ^ 1;  // a fresh slot passes at once
       if (!mbar_wait(empty0 + 8 * stage, parity, p.timeout_ns)) {
         atomicOr(p.status, kErrEmptyWait);
         ok = false;
         break;
       }
-      const int c0 = c_begin + it * p.R;
-      issue(stage, c0, min(p.R, c_end - c0));
+      const int c0 = f.c_begin + it * p.R;
+      issue(stage, f.b, c0, min(p.R, f.c_end - c0));
       issued = it + 1;
     }
     cp_async_wait_all();
@@ -289,26 +421,37 @@ __global__ void __launch_bounds__(kMmaMaxThreads, NB == 1 ? 3 : (NB == 2 ? 2 : 1
         if (!mbar_wait(full0 + 8 * (it % p.stages), (it / p.stages) & 1, p.timeout_ns))
           atomicOr(p.status, kErrDrain);
     }
-    for (int it = n_iters; it < pre; ++it)
+    // Early stages past the split's context (a split past its length): let
+    // them land before the CTA exits.
+    for (int it = f.n_iters; it < pre; ++it)
       if (!mbar_wait(full0 + 8 * it, 0, p.timeout_ns) && lane == 0) atomicOr(p.status, kErrDrain);
     return;
   }
 
-  // Converters, accumulators and the MMA warp: the split's context.
-  int L = p.seq_lens ? p.seq_lens[b] : p.Cmax;
-  L = L < 0 ? 0 : (L > p.Cmax ? p.Cmax : L);
-  const int nsplit_b = L > 0 ? (L + p.rows_per_split - 1) / p.rows_per_split : 1;
-  const int c_end = min(c_begin + p.rows_per_split, L);
-  const int n_iters = split < nsplit_b ? max((c_end - c_begin + p.R - 1) / p.R, 1) : 0;
+  MmaSplit f;
+  int slot;
+  if (!p.balanced) {
+    slot = fixed_split(f);
+  } else {
+    named_sync(3, blockDim.x);
+    f.b = split_info[0];
+    f.c_begin = split_info[1];
+    f.c_end = split_info[2];
+    f.n_iters = split_info[3];
+    f.alone = split_info[4];
+    slot = blockIdx.x;
+  }
+  const int b = f.b, c_begin = f.c_begin, c_end = f.c_end, n_iters = f.n_iters, alone = f.alone;
+
   const uint32_t b_half = (uint32_t)N * p.R * 2;   // bytes of one of hi / lo
 
   if (warp == issuer_warp) {
     // -------------------------------------------------------------- MMA issuer
+    const uint32_t idesc = mma_idesc<Tag>(2 * N);
+    const uint32_t a_lbo = (uint32_t)p.R * 128;      // second 64-column half
+    const uint32_t b_sbo = (uint32_t)(p.R / 8) * 128;  // next 8 rows of B
     bool ok = true;
     if (lane == 0) {
-      const uint32_t idesc = mma_idesc<Tag>(2 * N);
-      const uint32_t a_lbo = (uint32_t)p.R * 128;      // second 64-column half
-      const uint32_t b_sbo = (uint32_t)(p.R / 8) * 128;  // next 8 rows of B
       int issued = 0;
       for (int it = 0; it < n_iters; ++it) {
         const int stage = it % p.stages, j = it & 1;
@@ -341,8 +484,8 @@ __global__ void __launch_bounds__(kMmaMaxThreads, NB == 1 ? 3 : (NB == 2 ? 2 : 1
         if (!mbar_wait(drain, 0, p.timeout_ns)) atomicOr(p.status, kErrMmaWait);
       }
     }
-    __syncwarp();
     (void)ok;
+    __syncwarp();
     mma_team_sync();  // consumers are done with tensor memory
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(p.tmem_cols)
@@ -432,9 +575,8 @@ __global__ void __launch_bounds__(kMmaMaxThreads, NB == 1 ? 3 : (NB == 2 ? 2 : 1
 
   if (ok && n_iters > 0) {
     const float unscale = weight_unscale(Tag{});
-    const bool alone = nsplit_b == 1;
     const int tile_elems = p.heads * p.dt;
-    float* part = p.ws + ((size_t)tile * p.nsplit + split) * tile_elems;
+    float* part = p.ws + (size_t)slot * tile_elems;
     if (m < p.dt && d0 + m < p.D) {
 #pragma unroll
       for (int n = 0; n < N; ++n) {

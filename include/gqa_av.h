@@ -83,18 +83,28 @@ int gqa_av_decode_per_head(const float *attn, const void *v_cache, const int32_t
 
 /*
  * Launch-shape overrides for sweeps and tests. A field <= 0 keeps the
- * library's choice. nsplit: context splits per tile; dtile: output columns
+ * library's choice. nsplit: context splits per tile (of a full-length
+ * sequence; with balanced splits, see split_mode, the CTAs the batch's
+ * context is spread over are tiles x nsplit); dtile: output columns
  * per CTA (a multiple of 8 dividing D, <= 256); rows_per_stage: V rows per
  * pipeline stage (8..256); stages: pipeline depth (2..8); early_stages:
  * stages each CTA issues before it has read its sequence length (1..stages;
  * the library issues one, since rows past a length are read for nothing and
- * the first stage lands later behind the others); engine: 0 lets the library
+ * the first stage lands later behind the others; with balanced splits none
+ * are, though the value is still checked against stages); engine: 0 lets the library
  * pick, 1 forces the CUDA-core packed-FMA kernel, 2 the tcgen05 tensor-core
  * kernel (head groups of <= 64 heads and D >= 64 with D <= 128 or
  * D % 128 == 0; the library picks it wherever it applies unless dtile is
  * set, and with it dtile must be min(D, 128) or unset; rows_per_stage must
- * then be a multiple of 16). Results stay within the stated tolerance for
- * every choice, and are bitwise reproducible for a fixed choice.
+ * then be a multiple of 16); split_mode: 1 fixed splits (split s of each
+ * sequence covers rows [s, s + 1) x rows_per_split, and splits past a
+ * sequence's length have no work), 2 balanced splits (tensor-core engine
+ * only: every CTA reads all lengths and the batch's context rows are cut into
+ * equal splits of whole stages, each sequence getting splits in proportion
+ * to its length), 0 lets the library pick (balanced for the tensor-core
+ * engine on shapes with at least as many tiles as SMs, else fixed). Results
+ * stay within the stated tolerance for every choice, and are bitwise
+ * reproducible for a fixed choice and fixed lengths.
  */
 typedef struct gqa_av_tuning {
     int nsplit;
@@ -103,6 +113,7 @@ typedef struct gqa_av_tuning {
     int stages;
     int early_stages;
     int engine;
+    int split_mode;
 } gqa_av_tuning;
 
 int gqa_av_decode_tuned(const float *attn, const void *v_cache, const int32_t *seq_lens,
@@ -117,13 +128,14 @@ typedef struct gqa_av_plan_info {
     int dtile;           /* output columns per CTA */
     int rows_per_stage;
     int stages;
-    int early_stages;    /* stages issued before the sequence length is read */
+    int early_stages;    /* stages issued before the sequence length is read (0: none) */
     int engine;          /* 1 CUDA-core packed FMA, 2 tcgen05 tensor cores */
-    int nsplit;          /* context splits per tile */
+    int split_mode;      /* 1 fixed splits, 2 balanced over the batch's lengths */
+    int nsplit;          /* context splits per tile (of a full-length sequence) */
     int combine_ctas;    /* CTAs of the split-combine kernel (0: not launched) */
-    int rows_per_split;
+    int rows_per_split;  /* of a full-length sequence */
     int tiles;           /* (head groups) x B x (D / dtile) */
-    int ctas;            /* tiles x nsplit */
+    int ctas;            /* tiles x nsplit; tiles x (nsplit + 1) with balanced splits */
     int threads_per_cta;
     int smem_bytes;
     int ctas_per_sm;     /* occupancy of this kernel at this shared-memory size */

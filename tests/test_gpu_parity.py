@@ -125,29 +125,70 @@ def test_shape_sweep(gq, G, D, engine):
             assert_close(out, ref, f"G={G} D={D} {vd} mode={mode} engine={engine}")
 
 
+@pytest.mark.parametrize("engine", [0, 2], ids=["auto", "tensor"])
 @pytest.mark.parametrize("L", [0, 1, 2, 7, 8, 9, 31, 32, 33, 63, 64, 65, 255, 256, 257, 1000])
-def test_lengths_and_ragged_tails(gq, L):
+def test_lengths_and_ragged_tails(gq, L, engine):
     rng = np.random.default_rng(L + 7)
     B, C, Hq, Hkv, D = 2, 1024, 8, 2, 64
     attn, v, sl = rand_case(rng, B, C, Hq, Hkv, D, "bf16", [L, max(0, 1024 - L)])
     ref = run_oracle(attn, v, sl, "bf16")
     for mode in (0, 1):
-        out = run_gpu(gq, attn, v, sl, mode)
+        out = run_gpu(gq, attn, v, sl, mode, dict(engine=engine) if engine else None)
         assert_close(out, ref, f"L={L} mode={mode}")
         if L == 0:
             assert np.array_equal(out[0], np.zeros_like(out[0]))
 
 
-def test_lengths_are_clamped_and_null_means_full(gq):
+@pytest.mark.parametrize("engine", [0, 1, 2], ids=["auto", "fma", "tensor"])
+def test_lengths_are_clamped_and_null_means_full(gq, engine):
     rng = np.random.default_rng(5)
     B, C, Hq, Hkv, D = 3, 300, 8, 2, 64
+    tun = dict(engine=engine) if engine else None
     attn, v, _ = rand_case(rng, B, C, Hq, Hkv, D, "bf16", [300, 300, 300], pad_nan=False)
     full = run_oracle(attn, v, None, "bf16")
-    assert_close(run_gpu(gq, attn, v, None), full, "seq_lens=NULL")
+    assert_close(run_gpu(gq, attn, v, None, -1, tun), full, "seq_lens=NULL")
     sl = torch.tensor([300, 301, 1 << 30], dtype=torch.int32)
-    assert_close(run_gpu(gq, attn, v, sl), full, "lengths above Cmax")
-    neg = run_gpu(gq, attn, v, torch.tensor([-5, 0, -(1 << 30)], dtype=torch.int32))
+    assert_close(run_gpu(gq, attn, v, sl, -1, tun), full, "lengths above Cmax")
+    neg = run_gpu(gq, attn, v, torch.tensor([-5, 0, -(1 << 30)], dtype=torch.int32), -1, tun)
     assert np.array_equal(neg, np.zeros_like(neg))
+
+
+# Balanced splits (tensor-core engine) spread the batch's rows over the CTAs
+# from the lengths read on the device: batches past one and several warps of
+# lengths (the prefix scan runs in chunks of 32) and past the 256 lengths a
+# warp keeps in registers, empty sequences, one long sequence among short ones
+# (it takes nearly every split), and split counts from one per tile to many;
+# the same cases with fixed splits.
+BALANCED = [(33, [None]), (70, [0, 1, 5]), (130, [1]), (300, [0, 300]), (40, "one_long"),
+            (5, "all_empty")]
+
+
+@pytest.mark.parametrize("split_mode", [1, 2], ids=["fixed", "balanced"])
+@pytest.mark.parametrize("nsplit", [0, 1, 3, 40])
+@pytest.mark.parametrize("B,kind", BALANCED, ids=[f"B{b}-{k if isinstance(k, str) else 'mix'}"
+                                                  for b, k in BALANCED])
+def test_balanced_splits_over_the_batch(gq, B, kind, nsplit, split_mode):
+    rng = np.random.default_rng(B * 10 + nsplit)
+    C, Hq, Hkv, D = 300, 16, 2, 64
+    if kind == "one_long":
+        lens = [3] * B
+        lens[B // 2] = C
+    elif kind == "all_empty":
+        lens = [0] * B
+    else:
+        lens = list(rng.integers(0, C + 1, size=B))
+        for i, L in enumerate(x for x in kind if x is not None):
+            lens[(7 * i + 3) % B] = L
+    attn, v, sl = rand_case(rng, B, C, Hq, Hkv, D, "bf16", lens)
+    ref = run_oracle(attn, v, sl, "bf16")
+    tun = dict(engine=2, nsplit=nsplit, split_mode=split_mode)
+    assert gq.gqa_av_plan(B, C, Hq, Hkv, D, 0, 1, tun)["split_mode"] == split_mode
+    out = run_gpu(gq, attn, v, sl, 1, tun)
+    assert_close(out, ref, f"B={B} {kind} nsplit={nsplit}")
+    assert np.array_equal(run_gpu(gq, attn, v, sl, 1, tun), out), "not reproducible"
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert np.array_equal(out[b], np.zeros_like(out[b])), b
 
 
 # ------------------------------------------------------ launch-shape sweep
@@ -305,7 +346,7 @@ def test_invalid_calls_launch_nothing(gq):
     v8 = torch.zeros((1, 16, 2, 64), dtype=torch.bfloat16, device=dev)
     out8 = torch.full((1, 8, 64), 7.0, device=dev)
     for bad in (dict(stages=9), dict(stages=1), dict(rows_per_stage=7), dict(dtile=12),
-                dict(stages=2, early_stages=3)):
+                dict(stages=2, early_stages=3), dict(split_mode=3)):
         with pytest.raises(gq.GqaAvError) as e:
             gq.gqa_av_decode_tuned(attn8, v8, None, out8, mode=1, tuning=bad)
         assert e.value.status == 1, bad
@@ -343,5 +384,13 @@ def test_plan_reports_the_launch(gq):
     r = gq.gqa_av_plan(8, 32768, 16, 1, 256, 1, -1)
     assert r["heads_per_cta"] == 16 and r["head_chunk"] == 8
     assert p["early_stages"] == 1
+    t = gq.gqa_av_plan(4, 16384, 24, 8, 128, 0, -1)  # tensor core, 32 tiles: fixed splits
+    assert t["engine"] == 2 and t["split_mode"] == 1 and t["early_stages"] == 1
+    assert t["ctas"] == t["tiles"] * t["nsplit"]
+    u = gq.gqa_av_plan(32, 131072, 64, 8, 128, 0, -1)  # 256 tiles: balanced splits
+    assert u["engine"] == 2 and u["split_mode"] == 2 and u["early_stages"] == 0
+    assert u["ctas"] == u["tiles"] * (u["nsplit"] + 1) and u["combine_ctas"] > 0
+    with pytest.raises(gq.GqaAvError):
+        gq.gqa_av_plan(1, 8192, 32, 8, 128, 0, -1, dict(engine=1, split_mode=2))
     e = gq.gqa_av_plan(1, 8192, 32, 8, 128, 0, -1, dict(stages=3, early_stages=3))
     assert e["stages"] == 3 and e["early_stages"] == 3
