@@ -433,11 +433,18 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
   p->ws_bytes = p->combine
                     ? static_cast<size_t>(p->grid) * p->heads * p->dt * sizeof(float)
                     : 0;  // one partial slot a CTA
-  // Split combine: `parts` threads per float4 column, a power of two <= 16.
-  p->parts = 1;
-  while (p->parts < 16 && (p->balanced || p->parts < p->nsplit)) p->parts *= 2;
-  p->cols_per_cta = kCombineThreads / p->parts;
+  // Split combine: `parts` threads per float4 column (a power of two <= 16),
+  // as many as keep its grid within about one CTA per SM. Its CTAs are small
+  // enough to start next to the main kernel's while that runs, so they are
+  // all waiting when the partials are complete (measured faster than a grid
+  // that only starts as the main kernel's CTAs leave).
   const int ncol4 = p->heads * p->dt / 4;
+  const long long cols = static_cast<long long>(p->tiles) * ncol4;
+  p->parts = 1;
+  while (p->parts < 16 && (p->balanced || p->parts < p->nsplit) &&
+         cols * p->parts * 2 <= static_cast<long long>(di.sms) * kCombineThreads)
+    p->parts *= 2;
+  p->cols_per_cta = kCombineThreads / p->parts;
   p->ctas_per_tile = (ncol4 + p->cols_per_cta - 1) / p->cols_per_cta;
   return GQA_AV_OK;
 }

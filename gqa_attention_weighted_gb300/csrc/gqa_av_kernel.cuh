@@ -50,7 +50,7 @@ namespace gqa_av {
 __host__ __device__ constexpr int consumer_warps(int gc) { return gc >= 12 ? 8 : 12; }
 __host__ __device__ constexpr int cta_threads(int gc) { return 32 * (consumer_warps(gc) + 1); }
 constexpr int kMaxStages = 8;
-constexpr int kCombineThreads = 256;
+constexpr int kCombineThreads = 128;
 
 // Device status word bits.
 constexpr unsigned kErrFullWait = 1u;
