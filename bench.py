@@ -45,6 +45,7 @@ KERNEL_SOURCES = ["gqa_attention_weighted_gb300/csrc/gqa_av_kernel.cuh",
                   "gqa_attention_weighted_gb300/csrc/gqa_av_instances.cuh",
                   "gqa_attention_weighted_gb300/csrc/gqa_av_api.cu"]
 ENGINES = {"auto": 0, "fma": 1, "tensor": 2}
+SPLIT_MODES = {"auto": 0, "fixed": 1, "balanced": 2}
 KERNEL_NAMES = {1: "gqa_av_kernel", 2: "gqa_av_mma_kernel"}
 
 
@@ -65,9 +66,9 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def committed_traffic(workload: str, mode: int, engine: int):
+def committed_traffic(workload: str, mode: int, engine: int, split_mode: int):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source for this workload, mode and engine."""
+    on the current kernel source for this workload, mode, engine and splits."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
@@ -76,7 +77,8 @@ def committed_traffic(workload: str, mode: int, engine: int):
         return None
     for e in entries:
         if (e.get("kernel_hash") == kernel_hash() and e.get("workload") == workload
-                and e.get("mode") == mode and e.get("engine") == engine):
+                and e.get("mode") == mode and e.get("engine") == engine
+                and e.get("split_mode") == split_mode):
             return e.get("traffic_bytes_per_launch")
     return None
 
@@ -174,7 +176,12 @@ def run_gpu(args, rank, world, local):
     w = W.get(args.workload)
     dev = torch.device("cuda", torch.cuda.current_device())
     mode = {"auto": gq.MODE_AUTO, "gqa": gq.MODE_GQA, "per_head": gq.MODE_PER_HEAD}[args.mode]
-    tuning = dict(engine=ENGINES[args.engine]) if args.engine != "auto" else None
+    tuning = {}
+    if args.engine != "auto":
+        tuning["engine"] = ENGINES[args.engine]
+    if args.split_mode != "auto":
+        tuning["split_mode"] = SPLIT_MODES[args.split_mode]
+    tuning = tuning or None
 
     def call(s, out):
         if tuning is None:
@@ -257,6 +264,7 @@ def run_gpu(args, rank, world, local):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {**w.describe(), "mode": args.mode, "resolved_mode": plan["mode"],
                    "engine": args.engine, "resolved_engine": plan["engine"],
+                   "split_mode": args.split_mode, "resolved_split_mode": plan["split_mode"],
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "compulsory_bytes_per_call": cbytes, "flops_per_call": flops,
                    "l2": f"rotating {n_sets} input sets, {n_sets * set_bytes / 1e6:.0f} MB "
@@ -268,7 +276,8 @@ def run_gpu(args, rank, world, local):
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_kind": f"{peak_kind} hbm_gbs (copy)",
                      "frac_of_8tbs_nominal": round(achieved / 8000.0, 4),
-                     "traffic": committed_traffic(w.name, plan["mode"], plan["engine"]),
+                     "traffic": committed_traffic(w.name, plan["mode"], plan["engine"],
+                                                  plan["split_mode"]),
                      "kernel": KERNEL_NAMES[plan["engine"]], "kernel_hash": kernel_hash(),
                      "duration": "average time of one whole call (main kernel and, when the "
                                  "context is split, the split-combine kernel) over the timed "
@@ -410,6 +419,9 @@ def main():
     ap.add_argument("--engine", choices=list(ENGINES), default="auto",
                     help="kernel: the library's choice, the CUDA-core FMA kernel or the "
                          "tcgen05 tensor-core kernel")
+    ap.add_argument("--split-mode", choices=list(SPLIT_MODES), default="auto",
+                    help="context splits: the library's choice, fixed splits of each "
+                         "sequence, or splits balanced over the batch's lengths")
     ap.add_argument("--graph-len", type=int, default=500)
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -85,6 +85,10 @@ WORKLOADS: Dict[str, Workload] = {w.name: w for w in [
     # V-traffic comparison shape: Llama-style heads (G=4) with 537 MB of V, four
     # times the L2, so per-head re-reads of V cannot all be L2 hits.
     Workload("traffic_b8_c32768_hq32_hkv8_d128", 8, 32768, 32, 8, 128, "bf16", 1.0, 2.0),
+    # The large-batch shape at an eighth of the context (~1.07 GB of V, lengths
+    # in [C/4, C]): the same 256 tiles and split rule, small enough to profile.
+    Workload("ragged_b32_c16384_hq64_hkv8_d128", 32, 16384, 64, 8, 128, "bf16",
+             1.0, 2.0, 4096, 16384),
 ]}
 
 # Short aliases, in the order above.
@@ -95,6 +99,7 @@ ALIASES = {
     "mqa": "mqa_b8_c32768_hq16_hkv1_d256_fp16_ragged",
     "large": "large_b32_c131072_hq64_hkv8_d128_ragged",
     "traffic": "traffic_b8_c32768_hq32_hkv8_d128",
+    "ragged": "ragged_b32_c16384_hq64_hkv8_d128",
 }
 
 

@@ -202,7 +202,9 @@ TUNINGS = [dict(nsplit=1), dict(nsplit=2), dict(nsplit=7), dict(nsplit=1000),
            dict(nsplit=14, dtile=32, stages=4, rows_per_stage=24),
            dict(early_stages=1), dict(stages=3, early_stages=2),
            dict(nsplit=7, stages=4, early_stages=4), dict(nsplit=16, early_stages=2),
-           dict(nsplit=2, rows_per_stage=64, stages=8, early_stages=8)]
+           dict(nsplit=2, rows_per_stage=64, stages=8, early_stages=8),
+           dict(split_mode=1), dict(split_mode=2), dict(nsplit=7, split_mode=2),
+           dict(nsplit=1, split_mode=2), dict(rows_per_stage=32, stages=2, split_mode=2)]
 
 
 def tensor_tuning_applies(t):
@@ -215,6 +217,8 @@ def tensor_tuning_applies(t):
 def test_tunings_agree_and_are_deterministic(gq, tuning, engine):
     if engine == 2 and not tensor_tuning_applies(tuning):
         pytest.skip("launch shape the tensor-core kernel does not take")
+    if engine == 1 and tuning.get("split_mode") == 2:
+        pytest.skip("balanced splits are a tensor-core engine plan")
     tuning = dict(tuning, engine=engine)
     rng = np.random.default_rng(99)
     B, C, Hq, Hkv, D = 2, 1500, 24, 8, 128

@@ -76,8 +76,9 @@ def test_workload_dense(gq, name, engine):
     assert np.array_equal(again.cpu().double().numpy(), outs[0]), "not bitwise reproducible"
 
 
-def test_workload_large_sampled(gq):
-    w = W.get("large")
+@pytest.mark.parametrize("name", ["large", "ragged"])
+def test_workload_large_sampled(gq, name):
+    w = W.get(name)
     dev = torch.device("cuda")
     x = W.generate(w, dev, pad="zero")
     attn, v, sl = x["attn"], x["v"], x["seq_lens"]
@@ -94,7 +95,7 @@ def test_workload_large_sampled(gq):
         a_col = attn[b, :L, q].contiguous().cpu().numpy().reshape(1, L, 1)
         v_col = v[b, :L, q // w.G, :].contiguous().cpu().reshape(1, L, 1, w.D)
         ref = oracle.gqa_av(a_col, bits(v_col), w.v_dtype, None, nthreads=1)[0, 0]
-        _gate(got[b, q], ref, f"large b={b} q={q}")
+        _gate(got[b, q], ref, f"{name} b={b} q={q}")
     again = torch.empty_like(out)
     gq.gqa_av_decode(attn, v, sl, again)
     assert torch.equal(again, out), "not bitwise reproducible"
