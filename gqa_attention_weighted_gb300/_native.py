@@ -76,9 +76,14 @@ def _load() -> ctypes.CDLL:
     lib.gqa_av_last_error.argtypes = []
     lib.gqa_av_last_error.restype = ctypes.c_char_p
     lib.gqa_av_version.argtypes = []
+    lib.gqa_qk_softmax_decode.argtypes = [P, P, P, P, *sizes, I, ctypes.c_float, I, P]
+    lib.gqa_qk_device_status.argtypes = [P, I]
+    lib.gqa_qk_last_error.argtypes = []
+    lib.gqa_qk_last_error.restype = ctypes.c_char_p
     for f in ("gqa_av_decode", "gqa_av_decode_per_head", "gqa_av_decode_tuned",
               "gqa_av_decode_noalloc", "gqa_av_plan",
-              "gqa_av_set_workspace", "gqa_av_device_status", "gqa_av_version"):
+              "gqa_av_set_workspace", "gqa_av_device_status", "gqa_av_version",
+              "gqa_qk_softmax_decode", "gqa_qk_device_status"):
         getattr(lib, f).restype = I
     return lib
 
@@ -208,3 +213,42 @@ def gqa_av_last_error() -> str:
 
 def v_dtype_code(dtype: torch.dtype) -> int:
     return _V_DTYPE[dtype]
+
+
+# ------------------------------------------------------------ score step
+def _check_qk(status: int) -> None:
+    if status != GQA_AV_OK:
+        name = lib.gqa_av_status_string(status).decode()
+        raise GqaAvError(status, f"{name}: {lib.gqa_qk_last_error().decode()}")
+
+
+def gqa_qk_softmax_decode(q, k_cache, seq_lens, attn, mode: int = MODE_AUTO, scale=None,
+                          stream=None) -> torch.Tensor:
+    """attn[b,c,q] = softmax over c < L_b of scale * q[b,q,:] . k_cache[b,c,q//G,:]
+    (scale defaults to 1/sqrt(D)); rows c >= L_b of ``attn`` are left as they are."""
+    if q.dim() != 3 or k_cache.dim() != 4 or attn.dim() != 3:
+        raise ValueError("q must be [B,Hq,D], k_cache [B,Cmax,Hkv,D], attn [B,Cmax,Hq]")
+    B, Hq, D = q.shape
+    B2, Cmax, Hkv, D2 = k_cache.shape
+    if (B2, D2) != (B, D) or tuple(attn.shape) != (B, Cmax, Hq):
+        raise ValueError(f"inconsistent shapes: q {tuple(q.shape)}, k {tuple(k_cache.shape)}, "
+                         f"attn {tuple(attn.shape)}")
+    for name, t in (("q", q), ("k_cache", k_cache), ("attn", attn)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if q.dtype != torch.float32 or attn.dtype != torch.float32:
+        raise ValueError("q and attn must be float32")
+    if k_cache.dtype not in _V_DTYPE:
+        raise ValueError("k_cache must be bfloat16 or float16")
+    if seq_lens is not None and (not seq_lens.is_cuda or seq_lens.dtype != torch.int32
+                                 or seq_lens.numel() != B or not seq_lens.is_contiguous()):
+        raise ValueError("seq_lens must be a contiguous CUDA int32 tensor of B elements")
+    sc = float(D) ** -0.5 if scale is None else float(scale)
+    _check_qk(lib.gqa_qk_softmax_decode(_ptr(q), _ptr(k_cache), _ptr(seq_lens), _ptr(attn),
+                                        B, Cmax, Hq, Hkv, D, _V_DTYPE[k_cache.dtype], sc,
+                                        int(mode), _stream_handle(stream)))
+    return attn
+
+
+def gqa_qk_device_status(stream=None, clear: bool = True) -> None:
+    _check_qk(lib.gqa_qk_device_status(_stream_handle(stream), 1 if clear else 0))

@@ -1,0 +1,338 @@
+// Host side of the C ABI declared in include/gqa_qk.h: argument checks, mode
+// resolution, launch planning, the call's own workspace, the K tensor map and
+// dispatch to the score and normalise kernels.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <map>
+#include <mutex>
+#include <string>
+
+#include "gqa_qk.h"
+#include "gqa_qk_kernel.cuh"
+
+namespace gqa_av {
+namespace {
+
+constexpr size_t kQkHeaderBytes = 256;              // device status word + padding
+constexpr long long kQkTimeoutNs = 2000000000LL;    // 2 s bound on every mbarrier wait
+constexpr int kQkMaxStageBytes = 65536;
+
+thread_local std::string g_qk_error;
+std::mutex g_qk_mu;
+
+int qfail(int status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_qk_error = buf;
+  return status;
+}
+
+int qfail_cuda(cudaError_t e, const char* what) {
+  return qfail(GQA_AV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+using QkKernel = void (*)(QkParams);
+
+template <typename Tag>
+QkKernel pick(int gc) {
+  switch (gc) {
+    case 1: return gqa_qk_kernel<Tag, 1>;
+    case 2: return gqa_qk_kernel<Tag, 2>;
+    case 3: return gqa_qk_kernel<Tag, 3>;
+    case 4: return gqa_qk_kernel<Tag, 4>;
+    case 5: return gqa_qk_kernel<Tag, 5>;
+    case 6: return gqa_qk_kernel<Tag, 6>;
+    case 7: return gqa_qk_kernel<Tag, 7>;
+    case 8: return gqa_qk_kernel<Tag, 8>;
+    case 9: return gqa_qk_kernel<Tag, 9>;
+    case 10: return gqa_qk_kernel<Tag, 10>;
+    case 11: return gqa_qk_kernel<Tag, 11>;
+    case 12: return gqa_qk_kernel<Tag, 12>;
+    case 13: return gqa_qk_kernel<Tag, 13>;
+    case 14: return gqa_qk_kernel<Tag, 14>;
+    case 15: return gqa_qk_kernel<Tag, 15>;
+    case 16: return gqa_qk_kernel<Tag, 16>;
+    default: return nullptr;
+  }
+}
+
+struct QkPlan {
+  int mode, heads, hgroups, gc, nc, rs, R, stages, parts, rows_per_split, nsplit, tiles;
+  int smem, q_off, red_off, bar_off, stage_bytes;
+  int norm_rows, norm_ctas_per_b;
+  size_t ws_bytes;  // per-split pairs only
+};
+
+// Argument checks that need no CUDA call.
+int check_args(int B, int Cmax, int Hq, int Hkv, int D, int k_dtype, int mode) {
+  if (B <= 0 || Cmax <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0)
+    return qfail(GQA_AV_ERR_INVALID, "sizes must be positive (B=%d Cmax=%d Hq=%d Hkv=%d D=%d)", B,
+                 Cmax, Hq, Hkv, D);
+  if (Hq % Hkv) return qfail(GQA_AV_ERR_INVALID, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+  if (k_dtype != GQA_AV_BF16 && k_dtype != GQA_AV_FP16)
+    return qfail(GQA_AV_ERR_INVALID, "k_dtype=%d must be GQA_AV_BF16 or GQA_AV_FP16", k_dtype);
+  if (mode < -1 || mode > 1) return qfail(GQA_AV_ERR_INVALID, "mode=%d must be -1, 0 or 1", mode);
+  if (D % 64 || D > 256)
+    return qfail(GQA_AV_ERR_UNSUPPORTED, "D=%d must be a multiple of 64, at most 256", D);
+  if (Hq > kQkMaxHeads * 32) return qfail(GQA_AV_ERR_UNSUPPORTED, "Hq=%d above 2048", Hq);
+  return GQA_AV_OK;
+}
+
+int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int k_dtype, int mode, QkPlan* p) {
+  int rc = check_args(B, Cmax, Hq, Hkv, D, k_dtype, mode);
+  if (rc) return rc;
+  const int G = Hq / Hkv;
+  p->mode = mode == GQA_AV_MODE_AUTO ? (G > 1 ? GQA_AV_MODE_GQA : GQA_AV_MODE_PER_HEAD) : mode;
+  p->heads = p->mode == GQA_AV_MODE_GQA ? G : 1;
+  if (p->heads > kQkMaxHeads)
+    return qfail(GQA_AV_ERR_UNSUPPORTED, "%d heads per KV head, at most %d", p->heads, kQkMaxHeads);
+  p->hgroups = Hq / p->heads;
+  // Head chunks: the fewest of 1, 2, 4, 8 that leave at most 16 heads a thread.
+  p->nc = 0;
+  for (int nc = 1; nc <= 8; nc *= 2)
+    if (p->heads % nc == 0 && p->heads / nc <= 16) { p->nc = nc; break; }
+  if (!p->nc)
+    return qfail(GQA_AV_ERR_UNSUPPORTED, "%d heads per CTA do not split into <= 8 chunks of <= 16",
+                 p->heads);
+  p->gc = p->heads / p->nc;
+  p->rs = kQkConsumerThreads / p->nc;
+  // One K row per consumer thread and stage, at most 64 KiB a stage, a
+  // multiple of 32 rows so a warp is busy or idle as a whole.
+  p->R = std::min(p->rs, kQkMaxStageBytes / (2 * D)) / 32 * 32;
+  p->parts = D / 64;
+  p->stage_bytes = p->R * D * 2;
+
+  cudaDeviceProp prop;
+  cudaError_t e = cudaGetDeviceProperties(&prop, dev);
+  if (e != cudaSuccess) return qfail_cuda(e, "cudaGetDeviceProperties");
+  const int sms = prop.multiProcessorCount;
+  const int optin = static_cast<int>(prop.sharedMemPerBlockOptin);
+
+  p->tiles = p->hgroups * B;
+  long long want = p->tiles < sms ? std::max(1, sms / p->tiles)
+                                  : (2LL * sms + p->tiles - 1) / p->tiles;
+  want = std::max<long long>(1, std::min<long long>(want, (Cmax + p->R - 1) / p->R));
+  const int rps0 = static_cast<int>((Cmax + want - 1) / want);
+  p->rows_per_split = (rps0 + p->R - 1) / p->R * p->R;
+  p->nsplit = (Cmax + p->rows_per_split - 1) / p->rows_per_split;
+  if (static_cast<long long>(p->tiles) * p->nsplit > 0x7fffffffLL)
+    return qfail(GQA_AV_ERR_UNSUPPORTED, "grid too large");
+
+  const int q_bytes = p->heads * D * 4;
+  for (p->stages = 3; p->stages >= 2; --p->stages) {
+    p->q_off = p->stages * p->stage_bytes;
+    p->red_off = p->q_off + (q_bytes + 127) / 128 * 128;
+    p->bar_off = p->red_off + kQkConsumerWarps * 16 * 8;
+    p->smem = p->bar_off + 2 * kMaxStages * 8 + 1024;  // + alignment slack
+    if (p->smem <= optin) break;
+  }
+  if (p->smem > optin)
+    return qfail(GQA_AV_ERR_UNSUPPORTED, "plan needs %d B of shared memory (limit %d)", p->smem,
+                 optin);
+  p->ws_bytes = static_cast<size_t>(p->tiles) * p->nsplit * p->heads * sizeof(float2);
+
+  // Normalise: about two CTAs per SM over the batch's rows.
+  p->norm_ctas_per_b = static_cast<int>(
+      std::max<long long>(1, std::min<long long>((2LL * sms + B - 1) / B, (Cmax + 7) / 8)));
+  p->norm_rows = (Cmax + p->norm_ctas_per_b - 1) / p->norm_ctas_per_b;
+  p->norm_ctas_per_b = (Cmax + p->norm_rows - 1) / p->norm_rows;
+  return GQA_AV_OK;
+}
+
+struct Ws {
+  void* base = nullptr;
+  size_t bytes = 0;
+};
+std::map<int, Ws> g_qk_ws;
+
+int workspace(int dev, size_t need, cudaStream_t stream, Ws* out) {
+  std::lock_guard<std::mutex> lk(g_qk_mu);
+  Ws& w = g_qk_ws[dev];
+  if (w.base && w.bytes >= need) {
+    *out = w;
+    return GQA_AV_OK;
+  }
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+  if (e != cudaSuccess) return qfail_cuda(e, "cudaStreamIsCapturing");
+  if (cs != cudaStreamCaptureStatusNone)
+    return qfail(GQA_AV_ERR_NOMEM,
+                 "workspace must grow to %zu B but the stream is capturing; make one call with "
+                 "the largest shape before capture",
+                 need);
+  const size_t bytes = std::max(need, w.bytes + w.bytes / 2);
+  if (w.base) {
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return qfail_cuda(e, "cudaDeviceSynchronize");
+    cudaFree(w.base);
+    w.base = nullptr;
+    w.bytes = 0;
+  }
+  void* p = nullptr;
+  e = cudaMalloc(&p, bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return qfail(GQA_AV_ERR_NOMEM, "cudaMalloc(%zu) failed: %s", bytes, cudaGetErrorString(e));
+  }
+  e = cudaMemset(p, 0, kQkHeaderBytes);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaFree(p);
+    return qfail_cuda(e, "zeroing the workspace header");
+  }
+  w.base = p;
+  w.bytes = bytes;
+  *out = w;
+  return GQA_AV_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_qk_encode = nullptr;
+
+// K viewed as 4-D {D, Hkv, Cmax, B} (innermost first); box {64, 1, R, 1} in
+// the 128-byte swizzle (one 128-byte line per row and part).
+int encode_k_map(CUtensorMap* m, const void* k, int B, int Cmax, int Hkv, int D, int R) {
+  {
+    std::lock_guard<std::mutex> lk(g_qk_mu);
+    if (!g_qk_encode) {
+      void* f = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                                       cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !f)
+        return qfail(GQA_AV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+      g_qk_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+  }
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)Cmax, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2,
+                                 (cuuint64_t)Cmax * Hkv * D * 2};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)R, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_qk_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(k), dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return qfail(GQA_AV_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled (K) failed (%d)", (int)r);
+  return GQA_AV_OK;
+}
+
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+}  // namespace
+}  // namespace gqa_av
+
+using namespace gqa_av;
+
+extern "C" int gqa_qk_softmax_decode(const float* q, const void* k_cache, const int32_t* seq_lens,
+                                     float* attn, int B, int Cmax, int Hq, int Hkv, int D,
+                                     int k_dtype, float scale, int mode, void* stream_) {
+  g_qk_error.clear();
+  if (!q || !k_cache || !attn)
+    return qfail(GQA_AV_ERR_INVALID, "q, k_cache and attn must be non-NULL");
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
+       reinterpret_cast<uintptr_t>(attn)) & 15u)
+    return qfail(GQA_AV_ERR_UNSUPPORTED, "q, k_cache and attn must be 16-byte aligned");
+  int rc = check_args(B, Cmax, Hq, Hkv, D, k_dtype, mode);
+  if (rc) return rc;
+  const int G = Hq / Hkv;
+  const int heads = (mode == GQA_AV_MODE_GQA || (mode == GQA_AV_MODE_AUTO && G > 1)) ? G : 1;
+  if (heads > kQkMaxHeads)
+    return qfail(GQA_AV_ERR_UNSUPPORTED, "%d heads per KV head, at most %d", heads, kQkMaxHeads);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return qfail_cuda(e, "cudaGetDevice");
+  QkPlan pl;
+  if ((rc = plan(dev, B, Cmax, Hq, Hkv, D, k_dtype, mode, &pl))) return rc;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  Ws ws;
+  if ((rc = workspace(dev, kQkHeaderBytes + pl.ws_bytes, stream, &ws))) return rc;
+
+  QkParams p;
+  if ((rc = encode_k_map(&p.k_map, k_cache, B, Cmax, Hkv, D, pl.R))) return rc;
+  p.q = q;
+  p.seq_lens = seq_lens;
+  p.attn = attn;
+  p.status = static_cast<unsigned int*>(ws.base);
+  p.stats = reinterpret_cast<float2*>(static_cast<char*>(ws.base) + kQkHeaderBytes);
+  p.scale = scale;
+  p.B = B; p.Cmax = Cmax; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.G = Hq / Hkv;
+  p.heads = pl.heads; p.hgroups = pl.hgroups; p.nc = pl.nc; p.rs = pl.rs; p.R = pl.R;
+  p.stages = pl.stages; p.rows_per_split = pl.rows_per_split; p.nsplit = pl.nsplit;
+  p.parts = pl.parts; p.stage_bytes = static_cast<uint32_t>(pl.stage_bytes);
+  p.q_off = pl.q_off; p.red_off = pl.red_off; p.bar_off = pl.bar_off;
+  p.timeout_ns = kQkTimeoutNs;
+
+  QkKernel k = k_dtype == GQA_AV_BF16 ? pick<Bf16Tag>(pl.gc) : pick<Fp16Tag>(pl.gc);
+  if (!k) return qfail(GQA_AV_ERR_UNSUPPORTED, "no score kernel for %d heads a thread", pl.gc);
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
+  if (e != cudaSuccess) return qfail_cuda(e, "cudaFuncSetAttribute");
+  void* args1[] = {&p};
+  e = launch_pdl(reinterpret_cast<const void*>(k), dim3(pl.tiles * pl.nsplit), dim3(kQkThreads),
+                 pl.smem, stream, args1);
+  if (e != cudaSuccess) return qfail_cuda(e, "score kernel launch");
+
+  QkNormParams n;
+  n.stats = p.stats;
+  n.seq_lens = seq_lens;
+  n.attn = attn;
+  n.B = B; n.Cmax = Cmax; n.Hq = Hq; n.heads = pl.heads; n.hgroups = pl.hgroups;
+  n.rows_per_split = pl.rows_per_split; n.nsplit = pl.nsplit;
+  n.rows_per_cta = pl.norm_rows; n.ctas_per_b = pl.norm_ctas_per_b;
+  void* args2[] = {&n};
+  e = launch_pdl(reinterpret_cast<const void*>(gqa_qk_normalize_kernel),
+                 dim3(B * pl.norm_ctas_per_b), dim3(kQkNormThreads), 0, stream, args2);
+  if (e != cudaSuccess) return qfail_cuda(e, "normalise kernel launch");
+  return GQA_AV_OK;
+}
+
+extern "C" int gqa_qk_device_status(void* stream_, int clear) {
+  g_qk_error.clear();
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return qfail_cuda(e, "cudaGetDevice");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return qfail_cuda(e, "cudaStreamSynchronize");
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_qk_mu);
+    auto it = g_qk_ws.find(dev);
+    if (it != g_qk_ws.end()) base = it->second.base;
+  }
+  if (!base) return GQA_AV_OK;
+  unsigned word = 0;
+  e = cudaMemcpy(&word, base, sizeof word, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return qfail_cuda(e, "reading the status word");
+  if (word && clear) {
+    e = cudaMemset(base, 0, sizeof word);
+    if (e != cudaSuccess) return qfail_cuda(e, "clearing the status word");
+  }
+  if (word)
+    return qfail(GQA_AV_ERR_DEVICE_TIMEOUT, "a bounded wait in the score kernel ran out (0x%x)",
+                 word);
+  return GQA_AV_OK;
+}
+
+extern "C" const char* gqa_qk_last_error(void) { return g_qk_error.c_str(); }

@@ -1,0 +1,70 @@
+/*
+ * gqa_qk.h -- C ABI of the GB300 (sm_103a) decode score step: the softmax-
+ * normalised query-key products that the AV reduction (gqa_av.h) consumes.
+ *
+ * Operation: for every b < B, q_h < Hq and c < L_b,
+ *
+ *     s[b, c, q_h]    = scale * sum_d q[b, q_h, d] * K[b, c, kv_h, d],
+ *     attn[b, c, q_h] = exp(s[b, c, q_h] - M) / sum_{c' < L_b} exp(s[b, c', q_h] - M),
+ *     kv_h = q_h / G,   G = Hq / Hkv,   M = max_{c' < L_b} s[b, c', q_h],
+ *     L_b = clamp(seq_lens[b], 0, Cmax).
+ *
+ * It is the step before the AV coop-GEMV of LLM decode (page "pytorch/
+ * executorch pull 21063", summary paragraph), with the same grouping of
+ * query heads onto KV heads: in GQA-reuse mode each K row is read from HBM
+ * once for the G query heads of its group, in per-head mode once per query
+ * head. The mode switch follows the AV call's: -1 auto, 0 per-head, 1 GQA.
+ *
+ * Layouts (all contiguous, row-major, caller-owned DEVICE memory, 16-byte
+ * aligned):
+ *     q         [B, Hq, D]          float32
+ *     k_cache   [B, Cmax, Hkv, D]   bf16 (GQA_AV_BF16) or fp16 (GQA_AV_FP16)
+ *     seq_lens  [B]                 int32, or NULL meaning every L_b = Cmax
+ *     attn      [B, Cmax, Hq]       float32: rows c < L_b are written;
+ *                                   rows c >= L_b are left untouched
+ * attn is the layout gqa_av_decode takes, so the two calls chain directly.
+ *
+ * Numerics: products and sums in fp32 (bf16/fp16 -> fp32 widening is exact),
+ * the softmax in fp32 with per-split (max, sum of exp) pairs merged in a
+ * fixed order, so repeated calls with the same shape give bitwise-identical
+ * attn.
+ *
+ * Limits (GQA_AV_ERR_UNSUPPORTED otherwise): D a multiple of 64, D <= 256;
+ * at most 64 query heads per KV head in GQA mode, and a head count per CTA
+ * that splits into at most 8 chunks of at most 16 heads; Hq <= 2048.
+ *
+ * Execution: asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ * default stream), no host synchronisation. The call keeps its own
+ * per-device workspace (per-split softmax pairs and a status word), grown on
+ * demand with cudaMalloc outside stream capture; calls that may overlap on the
+ * GPU must not be issued concurrently. Errors: a status code from gqa_av.h;
+ * on error nothing is launched and gqa_qk_last_error() holds a message.
+ */
+#ifndef GQA_QK_H
+#define GQA_QK_H
+
+#include <stdint.h>
+
+#include "gqa_av.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+int gqa_qk_softmax_decode(const float *q, const void *k_cache, const int32_t *seq_lens,
+                          float *attn, int B, int Cmax, int Hq, int Hkv, int D, int k_dtype,
+                          float scale, int mode, void *stream);
+
+/* Synchronise `stream`, then read this call's device status word (set when a
+ * bounded wait inside a kernel runs out): GQA_AV_OK or
+ * GQA_AV_ERR_DEVICE_TIMEOUT; with clear != 0 the word is reset. */
+int gqa_qk_device_status(void *stream, int clear);
+
+/* Message of the calling thread's last score-step error ("" if none). */
+const char *gqa_qk_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_QK_H */

@@ -7,13 +7,15 @@ import re
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "gqa_av.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("gqa_av.h", "gqa_qk.h")]
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(gqa_av_\w+)\s*\(", text, re.M)))
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(gqa_(?:av|qk)_\w+)\s*\(", text, re.M))
+    return sorted(names)
 
 
 @pytest.fixture(scope="module")
@@ -27,7 +29,7 @@ def native():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for f in ("gqa_av_decode", "gqa_av_decode_per_head", "gqa_av_status_string",
-              "gqa_av_workspace_bytes"):
+              "gqa_av_workspace_bytes", "gqa_qk_softmax_decode", "gqa_qk_device_status"):
         assert f in names
 
 
@@ -71,3 +73,21 @@ def test_host_checks_reject_before_launch(native, args, status):
 def test_per_head_entry_checks(native):
     rc = native.lib.gqa_av_decode_per_head(FAKE, FAKE, None, FAKE, 1, 8, 6, 4, 8, 0, None)
     assert rc == 1 and "multiple" in native.gqa_av_last_error()
+
+
+@pytest.mark.parametrize("args,status", [
+    ((FAKE, FAKE, None, FAKE, 1, 8, 6, 4, 64, 0, 1.0, -1), 1),    # Hq % Hkv != 0
+    ((FAKE, FAKE, None, FAKE, 0, 8, 4, 4, 64, 0, 1.0, -1), 1),    # B == 0
+    ((FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 64, 2, 1.0, -1), 1),    # unknown dtype
+    ((FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 64, 0, 1.0, 3), 1),     # unknown mode
+    ((None, FAKE, None, FAKE, 1, 8, 4, 4, 64, 0, 1.0, -1), 1),    # NULL q
+    ((FAKE, FAKE, None, None, 1, 8, 4, 4, 64, 0, 1.0, 1), 1),     # NULL attn
+    ((FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 96, 0, 1.0, 1), 2),     # D % 64 != 0
+    ((FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 320, 0, 1.0, 1), 2),    # D > 256
+    ((FAKE, FAKE, None, FAKE, 1, 8, 128, 1, 64, 0, 1.0, 1), 2),   # 128 heads on one KV head
+    ((FAKE + 4, FAKE, None, FAKE, 1, 8, 4, 4, 64, 0, 1.0, 0), 2),  # misaligned q
+])
+def test_score_step_host_checks_reject_before_launch(native, args, status):
+    rc = native.lib.gqa_qk_softmax_decode(*args, None)
+    assert rc == status, native.lib.gqa_qk_last_error()
+    assert native.lib.gqa_qk_last_error() != b""

@@ -1,0 +1,144 @@
+"""GPU parity of the decode score step (through the C ABI) against its fp64 oracle.
+
+Gate: max|gpu - oracle| <= 1e-4 * max(1, max|oracle|) over the written rows
+(c < L_b); rows c >= L_b must keep the value they had. K rows past a length
+hold NaN, so a kernel that uses an out-of-range row fails.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import gqa_qk
+from helpers import TORCH_V, bits
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4
+SENTINEL = 7.0
+
+
+@pytest.fixture(scope="module")
+def gq():
+    from gqa_attention_weighted_gb300 import build
+    build.build()
+    import gqa_attention_weighted_gb300 as pkg
+    return pkg
+
+
+def qk_case(rng, B, C, Hq, Hkv, D, kd, lens, pad_nan=True):
+    q = torch.tensor(rng.standard_normal((B, Hq, D)), dtype=torch.float32)
+    k = torch.tensor(rng.standard_normal((B, C, Hkv, D)), dtype=torch.float32).to(TORCH_V[kd])
+    sl = torch.tensor(np.asarray(lens), dtype=torch.int32)
+    if pad_nan:
+        for b in range(B):
+            k[b, max(0, min(int(lens[b]), C)):] = float("nan")
+    return q, k, sl
+
+
+def run_qk(gq, q, k, sl, mode=-1, scale=None):
+    dev = torch.device("cuda")
+    B, Hq, D = q.shape
+    C = k.shape[1]
+    attn = torch.full((B, C, Hq), SENTINEL, dtype=torch.float32, device=dev)
+    gq.gqa_qk_softmax_decode(q.to(dev), k.to(dev), None if sl is None else sl.to(dev), attn,
+                             mode=mode, scale=scale)
+    gq.gqa_qk_device_status()
+    return attn.cpu().double().numpy()
+
+
+def check(got, ref, lens, what):
+    B, C, _ = got.shape
+    for b in range(B):
+        L = max(0, min(int(lens[b]), C)) if lens is not None else C
+        assert np.all(np.isfinite(got[b, :L])), f"{what}: non-finite at b={b}"
+        err = float(np.abs(got[b, :L] - ref[b, :L]).max()) if L else 0.0
+        assert err <= TOL, f"{what}: b={b} max|gpu-oracle| = {err:.3e}"
+        assert np.all(got[b, L:] == SENTINEL), f"{what}: rows past L_b={L} were written"
+
+
+SWEEP = [(g, d) for g in (1, 2, 3, 4, 8, 16, 32, 64) for d in (64, 128, 256)] + [(5, 192), (12, 128)]
+
+
+@pytest.mark.parametrize("G,D", SWEEP, ids=[f"G{g}-D{d}" for g, d in SWEEP])
+def test_score_step_shape_sweep(gq, G, D):
+    rng = np.random.default_rng(100 * G + D)
+    Hkv = 2 if G <= 16 else 1
+    B, C = 3, 517
+    lens = [517, 1, 200]
+    for kd in ("bf16", "fp16"):
+        q, k, sl = qk_case(rng, B, C, G * Hkv, Hkv, D, kd, lens)
+        scale = D ** -0.5
+        ref = gqa_qk.gqa_qk_softmax(q.numpy(), bits(k), kd, sl.numpy(), scale)
+        for mode in (0, 1):
+            got = run_qk(gq, q, k, sl, mode)
+            check(got, ref, lens, f"G={G} D={D} {kd} mode={mode}")
+
+
+@pytest.mark.parametrize("L", [0, 1, 2, 31, 32, 33, 255, 256, 257, 1000, 4095, 4096])
+def test_score_step_lengths(gq, L):
+    rng = np.random.default_rng(L + 3)
+    B, C, Hq, Hkv, D = 2, 4096, 8, 2, 128
+    lens = [L, 4096 - L]
+    q, k, sl = qk_case(rng, B, C, Hq, Hkv, D, "bf16", lens)
+    ref = gqa_qk.gqa_qk_softmax(q.numpy(), bits(k), "bf16", sl.numpy(), D ** -0.5)
+    check(run_qk(gq, q, k, sl), ref, lens, f"L={L}")
+
+
+def test_score_step_null_lengths_clamping_scale_and_determinism(gq):
+    rng = np.random.default_rng(7)
+    B, C, Hq, Hkv, D = 3, 300, 8, 2, 64
+    q, k, _ = qk_case(rng, B, C, Hq, Hkv, D, "fp16", [C] * B, pad_nan=False)
+    full = gqa_qk.gqa_qk_softmax(q.numpy(), bits(k), "fp16", None, 0.3)
+    a = run_qk(gq, q, k, None, scale=0.3)
+    check(a, full, None, "seq_lens=NULL")
+    over = torch.tensor([300, 301, 1 << 30], dtype=torch.int32)
+    check(run_qk(gq, q, k, over, scale=0.3), full, [300, 300, 300], "lengths above Cmax")
+    neg = run_qk(gq, q, k, torch.tensor([0, -4, -(1 << 30)], dtype=torch.int32), scale=0.3)
+    assert np.all(neg == SENTINEL), "non-positive lengths wrote rows"
+    assert np.array_equal(run_qk(gq, q, k, None, scale=0.3), a), "not bitwise reproducible"
+    # The two modes agree.
+    check(run_qk(gq, q, k, None, 0, 0.3), full, None, "per-head")
+
+
+@pytest.mark.parametrize("name", ["small", "llama", "phi", "mqa"])
+def test_score_step_workload_shapes(gq, name):
+    """The AV workloads' shapes, with K drawn like V, and the chained call:
+    the AV reduction on the score step's weights against the oracles' chain."""
+    from gqa_attention_weighted_gb300 import workloads as W
+    w = W.get(name)
+    rng = np.random.default_rng(5)
+    gen = torch.Generator().manual_seed(w.seed)
+    lens = torch.randint(w.lo, w.hi + 1, (w.B,), generator=gen).to(torch.int32).numpy()
+    q, k, sl = qk_case(rng, w.B, w.Cmax, w.Hq, w.Hkv, w.D, w.v_dtype, lens)
+    scale = w.D ** -0.5
+    ref = gqa_qk.gqa_qk_softmax(q.numpy(), bits(k), w.v_dtype, sl.numpy(), scale)
+    got = run_qk(gq, q, k, sl)
+    check(got, ref, lens, name)
+    # Chain: out = AV(attn from the score step, V); V reuses K's shape.
+    dev = torch.device("cuda")
+    v = torch.tensor(rng.standard_normal((w.B, w.Cmax, w.Hkv, w.D)),
+                     dtype=torch.float32).to(TORCH_V[w.v_dtype])
+    attn = torch.tensor(got, dtype=torch.float32)
+    for b in range(w.B):
+        attn[b, int(lens[b]):] = 0.0
+    out = torch.empty((w.B, w.Hq, w.D), device=dev)
+    gq.gqa_av_decode(attn.to(dev), v.to(dev), sl.to(dev), out)
+    gq.gqa_av_device_status()
+    ref_attn = ref.astype(np.float32)
+    ref_out = oracle.gqa_av(ref_attn, bits(v), w.v_dtype, sl.numpy(), nthreads=oracle.host_cores())
+    o = out.cpu().double().numpy()
+    tol = TOL * max(1.0, float(np.abs(ref_out).max()))
+    assert float(np.abs(o - ref_out).max()) <= tol, "chained score step + AV"
+
+
+def test_score_step_errors_launch_nothing(gq):
+    dev = torch.device("cuda")
+    q = torch.zeros((1, 4, 96), device=dev)
+    k = torch.zeros((1, 16, 2, 96), dtype=torch.bfloat16, device=dev)
+    attn = torch.full((1, 16, 4), SENTINEL, device=dev)
+    with pytest.raises(gq.GqaAvError) as e:
+        gq.gqa_qk_softmax_decode(q, k, None, attn)
+    assert e.value.status == 2
+    torch.cuda.synchronize()
+    assert torch.all(attn == SENTINEL)
