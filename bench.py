@@ -38,6 +38,11 @@ from gqa_attention_weighted_gb300 import workloads as W  # noqa: E402
 
 METRIC = "GQA AV decode achieved HBM GB/s over compulsory bytes (V read once), µs/call"
 UNIT = "GB/s"
+METRIC_QK = ("GQA QK-softmax decode achieved HBM GB/s over compulsory bytes (K read once), "
+             "µs/call")
+QK_SOURCES = ["gqa_attention_weighted_gb300/csrc/gqa_qk_kernel.cuh",
+              "gqa_attention_weighted_gb300/csrc/gqa_qk_api.cu",
+              "gqa_attention_weighted_gb300/csrc/gqa_av_kernel.cuh"]
 DEFAULT_WORKLOAD = "llama"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["gqa_attention_weighted_gb300/csrc/gqa_av_kernel.cuh",
@@ -49,9 +54,9 @@ SPLIT_MODES = {"auto": 0, "fixed": 1, "balanced": 2}
 KERNEL_NAMES = {1: "gqa_av_kernel", 2: "gqa_av_mma_kernel"}
 
 
-def kernel_hash() -> str:
+def kernel_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in sources or KERNEL_SOURCES:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -292,6 +297,184 @@ def run_gpu(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+def run_gpu_qk(args, rank, world, local):
+    """The decode score step (include/gqa_qk.h) on the workload's shape: q drawn
+    N(0, 1), K drawn like the workload's V, attn [B, Cmax, Hq] written."""
+    import gqa_attention_weighted_gb300 as gq
+
+    w = W.get(args.workload)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    mode = {"auto": gq.MODE_AUTO, "gqa": gq.MODE_GQA, "per_head": gq.MODE_PER_HEAD}[args.mode]
+    x = W.generate(w, dev, pad="zero")
+    g = torch.Generator(device=dev).manual_seed(w.seed + 1)
+    x = {"q": torch.randn((w.B, w.Hq, w.D), generator=g, device=dev, dtype=torch.float32),
+         "k": x["v"], "seq_lens": x["seq_lens"]}
+    lens = x["seq_lens"].cpu().tolist()
+    cbytes = W.compulsory_bytes(w, lens)  # K once, attn written once, q, seq_lens
+    flops = W.flops(w, lens)
+    scale = w.D ** -0.5
+
+    def call(st, attn):
+        gq.gqa_qk_softmax_decode(st["q"], st["k"], st["seq_lens"], attn, mode=mode, scale=scale)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    set_bytes = x["k"].numel() * 2 + w.B * w.Cmax * w.Hq * 4 + x["q"].numel() * 4
+    n_sets = max(1, math.ceil(3 * l2 / set_bytes)) if set_bytes < 3 * l2 else 1
+    sets = [x] + [{k: t.clone() for k, t in x.items()} for _ in range(n_sets - 1)]
+    outs = [torch.zeros((w.B, w.Cmax, w.Hq), dtype=torch.float32, device=dev)
+            for _ in range(n_sets)]
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            call(sets[i % n_sets], outs[i % n_sets])
+        gq.gqa_qk_device_status(stream)
+        chunk = min(args.steps, args.graph_len)
+        reps, rem = divmod(args.steps, chunk)
+
+        def capture(n):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                for i in range(n):
+                    call(sets[i % n_sets], outs[i % n_sets])
+            return gr
+
+        g_main = capture(chunk)
+        g_rem = capture(rem) if rem else None
+        g_main.replay()
+        stream.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        with ClockSampler(local) as clk:
+            start.record(stream)
+            for _ in range(reps):
+                g_main.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            end.record(stream)
+            end.synchronize()
+        torch.cuda.synchronize()
+        barrier(world)
+        elapsed_ms = start.elapsed_time(end)
+        gq.gqa_qk_device_status(stream)
+    elapsed_ms = max_over_ranks(elapsed_ms, world)
+    ms_per_step = elapsed_ms / args.steps
+    value = cbytes * args.steps * world / (elapsed_ms * 1e-3) / 1e9
+    achieved = cbytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+
+    # End to end: pinned H2D of q, K and seq_lens, the call, D2H of attn.
+    host = {k: t.cpu().pin_memory() for k, t in x.items()}
+    dbuf = {k: torch.empty_like(t) for k, t in x.items()}
+    attn_d = torch.zeros((w.B, w.Cmax, w.Hq), dtype=torch.float32, device=dev)
+    attn_h = torch.empty_like(attn_d, device="cpu").pin_memory()
+    e_steps = max(1, min(args.e2e_steps, args.steps))
+    with torch.cuda.stream(stream):
+        def step():
+            for k in host:
+                dbuf[k].copy_(host[k], non_blocking=True)
+            call(dbuf, attn_d)
+            attn_h.copy_(attn_d, non_blocking=True)
+        for _ in range(3):
+            step()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        e0.record(stream)
+        for _ in range(e_steps):
+            step()
+        e1.record(stream)
+        e1.synchronize()
+        barrier(world)
+    e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e_steps
+    e2e = {"value": round(cbytes * world / (e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+           "ms_per_step": e_ms, "steps": e_steps,
+           "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host.values()),
+           "d2h_bytes_per_step": attn_h.numel() * 4}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_baseline_qk(w, x, scale, args.cpu_seconds)
+    resolved = 1 if (mode == gq.MODE_GQA or (mode == gq.MODE_AUTO and w.G > 1)) else 0
+    line = {
+        "metric": METRIC_QK, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "us_per_call": ms_per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {**w.describe(), "op": "qk", "mode": args.mode, "resolved_mode": resolved,
+                   "scale": scale, "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "compulsory_bytes_per_call": cbytes, "flops_per_call": flops,
+                   "l2": f"rotating {n_sets} input sets, {n_sets * set_bytes / 1e6:.0f} MB "
+                         f"(L2 {l2 / 1e6:.0f} MB)",
+                   "timing": f"CUDA graphs of {chunk} calls x {reps}"
+                             + (f" + {rem}" if rem else "") + ", events on the launch stream"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_kind": f"{peak_kind} hbm_gbs (copy)",
+                     "traffic": committed_traffic_qk(w.name, resolved),
+                     "kernel": "gqa_qk_kernel", "kernel_hash": kernel_hash(QK_SOURCES),
+                     "duration": "average time of one whole call (score kernel and the "
+                                 "normalise kernel) over the timed region"},
+        "e2e": e2e,
+        "gpu_launches": args.steps * 2,
+        "clocks": clk.summary(),
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def committed_traffic_qk(workload: str, mode: int):
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            entries = json.load(f)
+    except (OSError, ValueError):
+        return None
+    for e in entries:
+        if (e.get("op") == "qk" and e.get("kernel_hash") == kernel_hash(QK_SOURCES)
+                and e.get("workload") == workload and e.get("mode") == mode):
+            return e.get("traffic_bytes_per_launch")
+    return None
+
+
+def oracle_baseline_qk(w, x, scale, seconds):
+    """The score-step oracle, as it stands (numpy fp64), on a context prefix."""
+    import numpy as np
+    from oracle import gqa_qk
+    rows = w.Cmax
+    q = x["q"].cpu().numpy()
+
+    def inputs(n):
+        kb = x["k"][:, :n].contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+        return kb, x["seq_lens"].cpu().clamp(max=n).numpy().astype(np.int32)
+
+    kb, lens = inputs(rows)
+    t0 = time.perf_counter()
+    gqa_qk.gqa_qk_softmax(q, kb, w.v_dtype, lens, scale)
+    t1 = time.perf_counter() - t0
+    if t1 > seconds:
+        rows = max(1, int(rows * seconds / t1 / 2))
+        kb, lens = inputs(rows)
+    sample_bytes = W.compulsory_bytes(w, lens.tolist())
+    n, t_total = 0, 0.0
+    while t_total < seconds or n < 1:
+        t0 = time.perf_counter()
+        gqa_qk.gqa_qk_softmax(q, kb, w.v_dtype, lens, scale)
+        t_total += time.perf_counter() - t0
+        n += 1
+    import oracle
+    return {"value": round(sample_bytes * n / t_total / 1e9, 4), "unit": UNIT,
+            "cores": oracle.host_cores(), "kind": "oracle",
+            "sample": f"{n} passes over context positions [0, {rows}) of {w.name} "
+                      f"({sample_bytes} compulsory bytes per pass), numpy fp64 (its BLAS "
+                      f"threads over the affinity mask), {t_total:.1f} s"}
+
+
 def run_e2e(gq, w, x, call, dev, args, world):
     """Same call with host inputs: pinned H2D copies, the call, D2H of out."""
     host = {k: t.cpu().pin_memory() for k, t in x.items()}
@@ -422,6 +605,9 @@ def main():
     ap.add_argument("--split-mode", choices=list(SPLIT_MODES), default="auto",
                     help="context splits: the library's choice, fixed splits of each "
                          "sequence, or splits balanced over the batch's lengths")
+    ap.add_argument("--op", choices=["av", "qk"], default="av",
+                    help="av: the AV reduction (the benchmark); qk: the decode score step "
+                         "before it")
     ap.add_argument("--graph-len", type=int, default=500)
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -437,7 +623,7 @@ def main():
         else:
             if not torch.cuda.is_available():
                 raise SystemExit("bench.py: the GB300 arm needs a CUDA GPU")
-            run_gpu(args, rank, world, local)
+            (run_gpu_qk if args.op == "qk" else run_gpu)(args, rank, world, local)
     finally:
         if world > 1:
             import torch.distributed as dist

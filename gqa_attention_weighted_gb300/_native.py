@@ -77,13 +77,14 @@ def _load() -> ctypes.CDLL:
     lib.gqa_av_last_error.restype = ctypes.c_char_p
     lib.gqa_av_version.argtypes = []
     lib.gqa_qk_softmax_decode.argtypes = [P, P, P, P, *sizes, I, ctypes.c_float, I, P]
+    lib.gqa_qk_softmax_decode_tuned.argtypes = [P, P, P, P, *sizes, I, ctypes.c_float, I, I, P]
     lib.gqa_qk_device_status.argtypes = [P, I]
     lib.gqa_qk_last_error.argtypes = []
     lib.gqa_qk_last_error.restype = ctypes.c_char_p
     for f in ("gqa_av_decode", "gqa_av_decode_per_head", "gqa_av_decode_tuned",
               "gqa_av_decode_noalloc", "gqa_av_plan",
               "gqa_av_set_workspace", "gqa_av_device_status", "gqa_av_version",
-              "gqa_qk_softmax_decode", "gqa_qk_device_status"):
+              "gqa_qk_softmax_decode", "gqa_qk_softmax_decode_tuned", "gqa_qk_device_status"):
         getattr(lib, f).restype = I
     return lib
 
@@ -223,7 +224,7 @@ def _check_qk(status: int) -> None:
 
 
 def gqa_qk_softmax_decode(q, k_cache, seq_lens, attn, mode: int = MODE_AUTO, scale=None,
-                          stream=None) -> torch.Tensor:
+                          stream=None, engine: int = 0) -> torch.Tensor:
     """attn[b,c,q] = softmax over c < L_b of scale * q[b,q,:] . k_cache[b,c,q//G,:]
     (scale defaults to 1/sqrt(D)); rows c >= L_b of ``attn`` are left as they are."""
     if q.dim() != 3 or k_cache.dim() != 4 or attn.dim() != 3:
@@ -244,9 +245,9 @@ def gqa_qk_softmax_decode(q, k_cache, seq_lens, attn, mode: int = MODE_AUTO, sca
                                  or seq_lens.numel() != B or not seq_lens.is_contiguous()):
         raise ValueError("seq_lens must be a contiguous CUDA int32 tensor of B elements")
     sc = float(D) ** -0.5 if scale is None else float(scale)
-    _check_qk(lib.gqa_qk_softmax_decode(_ptr(q), _ptr(k_cache), _ptr(seq_lens), _ptr(attn),
-                                        B, Cmax, Hq, Hkv, D, _V_DTYPE[k_cache.dtype], sc,
-                                        int(mode), _stream_handle(stream)))
+    _check_qk(lib.gqa_qk_softmax_decode_tuned(_ptr(q), _ptr(k_cache), _ptr(seq_lens), _ptr(attn),
+                                              B, Cmax, Hq, Hkv, D, _V_DTYPE[k_cache.dtype], sc,
+                                              int(mode), int(engine), _stream_handle(stream)))
     return attn
 
 

@@ -14,13 +14,13 @@
 
 #include "gqa_qk.h"
 #include "gqa_qk_kernel.cuh"
+#include "gqa_qk_mma.cuh"
 
 namespace gqa_av {
 namespace {
 
 constexpr size_t kQkHeaderBytes = 256;              // device status word + padding
 constexpr long long kQkTimeoutNs = 2000000000LL;    // 2 s bound on every mbarrier wait
-constexpr int kQkMaxStageBytes = 65536;
 
 thread_local std::string g_qk_error;
 std::mutex g_qk_mu;
@@ -64,7 +64,21 @@ QkKernel pick(int gc) {
   }
 }
 
+template <typename Tag>
+QkKernel pick_mma(int nb) {
+  switch (nb) {
+    case 1: return gqa_qk_mma_kernel<Tag, 1>;
+    case 2: return gqa_qk_mma_kernel<Tag, 2>;
+    case 3: return gqa_qk_mma_kernel<Tag, 3>;
+    case 4: return gqa_qk_mma_kernel<Tag, 4>;
+    default: return nullptr;
+  }
+}
+
+constexpr int kQkEngineFma = 1, kQkEngineTensor = 2;
+
 struct QkPlan {
+  int engine, npad, b_off, tmem_cols, threads;
   int mode, heads, hgroups, gc, nc, rs, R, stages, parts, rows_per_split, nsplit, tiles;
   int smem, q_off, red_off, bar_off, stage_bytes;
   int norm_rows, norm_ctas_per_b;
@@ -80,15 +94,20 @@ int check_args(int B, int Cmax, int Hq, int Hkv, int D, int k_dtype, int mode) {
   if (k_dtype != GQA_AV_BF16 && k_dtype != GQA_AV_FP16)
     return qfail(GQA_AV_ERR_INVALID, "k_dtype=%d must be GQA_AV_BF16 or GQA_AV_FP16", k_dtype);
   if (mode < -1 || mode > 1) return qfail(GQA_AV_ERR_INVALID, "mode=%d must be -1, 0 or 1", mode);
-  if (D % 64 || D > 256)
-    return qfail(GQA_AV_ERR_UNSUPPORTED, "D=%d must be a multiple of 64, at most 256", D);
+  if (D != 64 && D != 128 && D != 256)
+    return qfail(GQA_AV_ERR_UNSUPPORTED, "D=%d must be 64, 128 or 256", D);
   if (Hq > kQkMaxHeads * 32) return qfail(GQA_AV_ERR_UNSUPPORTED, "Hq=%d above 2048", Hq);
   return GQA_AV_OK;
 }
 
-int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int k_dtype, int mode, QkPlan* p) {
+int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int k_dtype, int mode, int engine,
+         QkPlan* p) {
   int rc = check_args(B, Cmax, Hq, Hkv, D, k_dtype, mode);
   if (rc) return rc;
+  if (engine < 0 || engine > kQkEngineTensor)
+    return qfail(GQA_AV_ERR_INVALID, "engine=%d must be 0 (auto), 1 (FMA) or 2 (tensor)", engine);
+  // The tensor-core kernel takes every shape the limits allow; it is the default.
+  p->engine = engine ? engine : kQkEngineTensor;
   const int G = Hq / Hkv;
   p->mode = mode == GQA_AV_MODE_AUTO ? (G > 1 ? GQA_AV_MODE_GQA : GQA_AV_MODE_PER_HEAD) : mode;
   p->heads = p->mode == GQA_AV_MODE_GQA ? G : 1;
@@ -104,10 +123,23 @@ int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int k_dtype, int mode
                  p->heads);
   p->gc = p->heads / p->nc;
   p->rs = kQkConsumerThreads / p->nc;
-  // One K row per consumer thread and stage, at most 64 KiB a stage, a
-  // multiple of 32 rows so a warp is busy or idle as a whole.
-  p->R = std::min(p->rs, kQkMaxStageBytes / (2 * D)) / 32 * 32;
   p->parts = D / 64;
+  const bool tensor = p->engine == kQkEngineTensor;
+  if (tensor) {
+    // 128 context rows (the MMA's M) a stage; N = 2 x heads padded to 16.
+    p->R = kQkMmaRows;
+    p->npad = (p->heads + 15) / 16 * 16;
+    p->tmem_cols = 32;
+    while (p->tmem_cols < 4 * p->npad) p->tmem_cols *= 2;
+    p->threads = kQkMmaThreads;
+  } else {
+    // One K row per consumer thread and stage, at most 64 KiB a stage, a
+    // multiple of 32 rows so a warp is busy or idle as a whole.
+    p->R = std::min(p->rs, 32768 / D) / 32 * 32;
+    p->npad = 0;
+    p->tmem_cols = 0;
+    p->threads = kQkThreads;
+  }
   p->stage_bytes = p->R * D * 2;
 
   cudaDeviceProp prop;
@@ -127,11 +159,24 @@ int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int k_dtype, int mode
     return qfail(GQA_AV_ERR_UNSUPPORTED, "grid too large");
 
   const int q_bytes = p->heads * D * 4;
-  for (p->stages = 3; p->stages >= 2; --p->stages) {
-    p->q_off = p->stages * p->stage_bytes;
-    p->red_off = p->q_off + (q_bytes + 127) / 128 * 128;
-    p->bar_off = p->red_off + kQkConsumerWarps * 16 * 8;
-    p->smem = p->bar_off + 2 * kMaxStages * 8 + 1024;  // + alignment slack
+  // FMA kernel: 3 stages (2 if that does not fit). Tensor-core kernel: as deep
+  // a ring as about 160 KiB holds (2 to 8 stages).
+  const int want_stages =
+      tensor ? std::max(2, std::min(kMaxStages, 163840 / p->stage_bytes)) : 3;
+  for (p->stages = want_stages; p->stages >= 2; --p->stages) {
+    if (tensor) {
+      p->b_off = p->stages * p->stage_bytes;
+      p->red_off = p->b_off + 2 * p->npad * D * 2;
+      p->bar_off = p->red_off + kMmaAccWarps * p->npad * 8;
+      p->q_off = 0;
+      p->smem = p->bar_off + (2 * kMaxStages + 6) * 8 + 8 + 1024;
+    } else {
+      p->q_off = p->stages * p->stage_bytes;
+      p->red_off = p->q_off + (q_bytes + 127) / 128 * 128;
+      p->bar_off = p->red_off + kQkConsumerWarps * 16 * 8;
+      p->b_off = 0;
+      p->smem = p->bar_off + 2 * kMaxStages * 8 + 1024;  // + alignment slack
+    }
     if (p->smem <= optin) break;
   }
   if (p->smem > optin)
@@ -245,9 +290,10 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaS
 
 using namespace gqa_av;
 
-extern "C" int gqa_qk_softmax_decode(const float* q, const void* k_cache, const int32_t* seq_lens,
-                                     float* attn, int B, int Cmax, int Hq, int Hkv, int D,
-                                     int k_dtype, float scale, int mode, void* stream_) {
+extern "C" int gqa_qk_softmax_decode_tuned(const float* q, const void* k_cache,
+                                           const int32_t* seq_lens, float* attn, int B, int Cmax,
+                                           int Hq, int Hkv, int D, int k_dtype, float scale,
+                                           int mode, int engine, void* stream_) {
   g_qk_error.clear();
   if (!q || !k_cache || !attn)
     return qfail(GQA_AV_ERR_INVALID, "q, k_cache and attn must be non-NULL");
@@ -264,7 +310,7 @@ extern "C" int gqa_qk_softmax_decode(const float* q, const void* k_cache, const 
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return qfail_cuda(e, "cudaGetDevice");
   QkPlan pl;
-  if ((rc = plan(dev, B, Cmax, Hq, Hkv, D, k_dtype, mode, &pl))) return rc;
+  if ((rc = plan(dev, B, Cmax, Hq, Hkv, D, k_dtype, mode, engine, &pl))) return rc;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   Ws ws;
   if ((rc = workspace(dev, kQkHeaderBytes + pl.ws_bytes, stream, &ws))) return rc;
@@ -283,13 +329,19 @@ extern "C" int gqa_qk_softmax_decode(const float* q, const void* k_cache, const 
   p.parts = pl.parts; p.stage_bytes = static_cast<uint32_t>(pl.stage_bytes);
   p.q_off = pl.q_off; p.red_off = pl.red_off; p.bar_off = pl.bar_off;
   p.timeout_ns = kQkTimeoutNs;
+  p.b_off = pl.b_off;
+  p.tmem_cols = static_cast<uint32_t>(pl.tmem_cols);
 
-  QkKernel k = k_dtype == GQA_AV_BF16 ? pick<Bf16Tag>(pl.gc) : pick<Fp16Tag>(pl.gc);
-  if (!k) return qfail(GQA_AV_ERR_UNSUPPORTED, "no score kernel for %d heads a thread", pl.gc);
+  QkKernel k;
+  if (pl.engine == kQkEngineTensor)
+    k = k_dtype == GQA_AV_BF16 ? pick_mma<Bf16Tag>(pl.npad / 16) : pick_mma<Fp16Tag>(pl.npad / 16);
+  else
+    k = k_dtype == GQA_AV_BF16 ? pick<Bf16Tag>(pl.gc) : pick<Fp16Tag>(pl.gc);
+  if (!k) return qfail(GQA_AV_ERR_UNSUPPORTED, "no score kernel for this head count");
   e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
   if (e != cudaSuccess) return qfail_cuda(e, "cudaFuncSetAttribute");
   void* args1[] = {&p};
-  e = launch_pdl(reinterpret_cast<const void*>(k), dim3(pl.tiles * pl.nsplit), dim3(kQkThreads),
+  e = launch_pdl(reinterpret_cast<const void*>(k), dim3(pl.tiles * pl.nsplit), dim3(pl.threads),
                  pl.smem, stream, args1);
   if (e != cudaSuccess) return qfail_cuda(e, "score kernel launch");
 
@@ -305,6 +357,13 @@ extern "C" int gqa_qk_softmax_decode(const float* q, const void* k_cache, const 
                  dim3(B * pl.norm_ctas_per_b), dim3(kQkNormThreads), 0, stream, args2);
   if (e != cudaSuccess) return qfail_cuda(e, "normalise kernel launch");
   return GQA_AV_OK;
+}
+
+extern "C" int gqa_qk_softmax_decode(const float* q, const void* k_cache, const int32_t* seq_lens,
+                                     float* attn, int B, int Cmax, int Hq, int Hkv, int D,
+                                     int k_dtype, float scale, int mode, void* stream) {
+  return gqa_qk_softmax_decode_tuned(q, k_cache, seq_lens, attn, B, Cmax, Hq, Hkv, D, k_dtype,
+                                     scale, mode, 0, stream);
 }
 
 extern "C" int gqa_qk_device_status(void* stream_, int clear) {

@@ -56,6 +56,9 @@ struct alignas(64) QkParams {
   uint32_t stage_bytes;         // R * D * 2
   uint32_t q_off, red_off, bar_off;  // shared-memory offsets from the 1024-aligned base
   long long timeout_ns;
+  // Tensor-core kernel only.
+  uint32_t b_off;               // shared-memory offset of the B (query hi / lo) operand
+  uint32_t tmem_cols;           // tensor-memory columns allocated (power of 2 >= 4 x Npad)
 };
 
 struct QkNormParams {
@@ -282,15 +285,25 @@ gqa_qk_normalize_kernel(const __grid_constant__ QkNormParams p) {
   const int c0 = blk * p.rows_per_cta;
   const int c1 = min(c0 + p.rows_per_cta, L);
   if (c0 >= c1) return;
-  for (int h = threadIdx.x; h < p.Hq; h += kQkNormThreads) {
+  // One warp per head: its lanes load the splits' pairs together (split s on
+  // lane s % 32), merge their own in split order, then the lanes are merged
+  // in a fixed butterfly order.
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int h = warp; h < p.Hq; h += kQkNormThreads / 32) {
     const int hg = h / p.heads, hh = h - hg * p.heads;
     const float2* st = p.stats + ((size_t)(hg * p.B + b) * p.nsplit) * p.heads + hh;
     float M = -INFINITY, S = 0.0f;
-    for (int s = 0; s < nsplit_b; ++s) {
+    for (int s = lane; s < nsplit_b; s += 32) {
       const float2 v = __ldcg(st + (size_t)s * p.heads);
       lse_merge(M, S, v.x, v.y);
     }
-    ms[h] = make_float2(M, 1.0f / S);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
+      const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
+      lse_merge(M, S, m2, s2);
+    }
+    if (lane == 0) ms[h] = make_float2(M, 1.0f / S);
   }
   __syncthreads();
   const size_t n = (size_t)(c1 - c0) * p.Hq;

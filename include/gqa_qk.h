@@ -29,7 +29,7 @@
  * fixed order, so repeated calls with the same shape give bitwise-identical
  * attn.
  *
- * Limits (GQA_AV_ERR_UNSUPPORTED otherwise): D a multiple of 64, D <= 256;
+ * Limits (GQA_AV_ERR_UNSUPPORTED otherwise): D = 64, 128 or 256;
  * at most 64 query heads per KV head in GQA mode, and a head count per CTA
  * that splits into at most 8 chunks of at most 16 heads; Hq <= 2048.
  *
@@ -54,6 +54,15 @@ extern "C" {
 int gqa_qk_softmax_decode(const float *q, const void *k_cache, const int32_t *seq_lens,
                           float *attn, int B, int Cmax, int Hq, int Hkv, int D, int k_dtype,
                           float scale, int mode, void *stream);
+
+/* The same with the kernel chosen: engine 0 lets the library pick (the
+ * tensor-core kernel), 1 forces the CUDA-core FMA kernel, 2 the tcgen05
+ * tensor-core kernel (K rows as the A operand in place, the queries split
+ * into 16-bit hi and lo halves as B). Both give results within the stated
+ * tolerance. */
+int gqa_qk_softmax_decode_tuned(const float *q, const void *k_cache, const int32_t *seq_lens,
+                                float *attn, int B, int Cmax, int Hq, int Hkv, int D,
+                                int k_dtype, float scale, int mode, int engine, void *stream);
 
 /* Synchronise `stream`, then read this call's device status word (set when a
  * bounded wait inside a kernel runs out): GQA_AV_OK or

@@ -84,6 +84,7 @@ def test_per_head_entry_checks(native):
     ((FAKE, FAKE, None, None, 1, 8, 4, 4, 64, 0, 1.0, 1), 1),     # NULL attn
     ((FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 96, 0, 1.0, 1), 2),     # D % 64 != 0
     ((FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 320, 0, 1.0, 1), 2),    # D > 256
+    ((FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 192, 0, 1.0, 1), 2),    # D = 192
     ((FAKE, FAKE, None, FAKE, 1, 8, 128, 1, 64, 0, 1.0, 1), 2),   # 128 heads on one KV head
     ((FAKE + 4, FAKE, None, FAKE, 1, 8, 4, 4, 64, 0, 1.0, 0), 2),  # misaligned q
 ])

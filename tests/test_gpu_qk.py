@@ -36,13 +36,13 @@ def qk_case(rng, B, C, Hq, Hkv, D, kd, lens, pad_nan=True):
     return q, k, sl
 
 
-def run_qk(gq, q, k, sl, mode=-1, scale=None):
+def run_qk(gq, q, k, sl, mode=-1, scale=None, engine=0):
     dev = torch.device("cuda")
     B, Hq, D = q.shape
     C = k.shape[1]
     attn = torch.full((B, C, Hq), SENTINEL, dtype=torch.float32, device=dev)
     gq.gqa_qk_softmax_decode(q.to(dev), k.to(dev), None if sl is None else sl.to(dev), attn,
-                             mode=mode, scale=scale)
+                             mode=mode, scale=scale, engine=engine)
     gq.gqa_qk_device_status()
     return attn.cpu().double().numpy()
 
@@ -57,11 +57,16 @@ def check(got, ref, lens, what):
         assert np.all(got[b, L:] == SENTINEL), f"{what}: rows past L_b={L} were written"
 
 
-SWEEP = [(g, d) for g in (1, 2, 3, 4, 8, 16, 32, 64) for d in (64, 128, 256)] + [(5, 192), (12, 128)]
+SWEEP = [(g, d) for g in (1, 2, 3, 4, 8, 16, 32, 64) for d in (64, 128, 256)] + [(5, 256), (12, 128), (24, 64)]
 
 
+ENGINES = [0, 1, 2]
+ENGINE_IDS = ["auto", "fma", "tensor"]
+
+
+@pytest.mark.parametrize("engine", ENGINES, ids=ENGINE_IDS)
 @pytest.mark.parametrize("G,D", SWEEP, ids=[f"G{g}-D{d}" for g, d in SWEEP])
-def test_score_step_shape_sweep(gq, G, D):
+def test_score_step_shape_sweep(gq, G, D, engine):
     rng = np.random.default_rng(100 * G + D)
     Hkv = 2 if G <= 16 else 1
     B, C = 3, 517
@@ -71,38 +76,44 @@ def test_score_step_shape_sweep(gq, G, D):
         scale = D ** -0.5
         ref = gqa_qk.gqa_qk_softmax(q.numpy(), bits(k), kd, sl.numpy(), scale)
         for mode in (0, 1):
-            got = run_qk(gq, q, k, sl, mode)
-            check(got, ref, lens, f"G={G} D={D} {kd} mode={mode}")
+            got = run_qk(gq, q, k, sl, mode, engine=engine)
+            check(got, ref, lens, f"G={G} D={D} {kd} mode={mode} engine={engine}")
 
 
-@pytest.mark.parametrize("L", [0, 1, 2, 31, 32, 33, 255, 256, 257, 1000, 4095, 4096])
-def test_score_step_lengths(gq, L):
+@pytest.mark.parametrize("engine", [1, 2], ids=["fma", "tensor"])
+@pytest.mark.parametrize("L", [0, 1, 2, 31, 32, 33, 127, 128, 129, 255, 256, 257, 1000, 4095, 4096])
+def test_score_step_lengths(gq, L, engine):
     rng = np.random.default_rng(L + 3)
     B, C, Hq, Hkv, D = 2, 4096, 8, 2, 128
     lens = [L, 4096 - L]
     q, k, sl = qk_case(rng, B, C, Hq, Hkv, D, "bf16", lens)
     ref = gqa_qk.gqa_qk_softmax(q.numpy(), bits(k), "bf16", sl.numpy(), D ** -0.5)
-    check(run_qk(gq, q, k, sl), ref, lens, f"L={L}")
+    check(run_qk(gq, q, k, sl, engine=engine), ref, lens, f"L={L} engine={engine}")
 
 
-def test_score_step_null_lengths_clamping_scale_and_determinism(gq):
+@pytest.mark.parametrize("engine", [1, 2], ids=["fma", "tensor"])
+def test_score_step_null_lengths_clamping_scale_and_determinism(gq, engine):
     rng = np.random.default_rng(7)
     B, C, Hq, Hkv, D = 3, 300, 8, 2, 64
     q, k, _ = qk_case(rng, B, C, Hq, Hkv, D, "fp16", [C] * B, pad_nan=False)
     full = gqa_qk.gqa_qk_softmax(q.numpy(), bits(k), "fp16", None, 0.3)
-    a = run_qk(gq, q, k, None, scale=0.3)
+    a = run_qk(gq, q, k, None, scale=0.3, engine=engine)
     check(a, full, None, "seq_lens=NULL")
     over = torch.tensor([300, 301, 1 << 30], dtype=torch.int32)
-    check(run_qk(gq, q, k, over, scale=0.3), full, [300, 300, 300], "lengths above Cmax")
-    neg = run_qk(gq, q, k, torch.tensor([0, -4, -(1 << 30)], dtype=torch.int32), scale=0.3)
+    check(run_qk(gq, q, k, over, scale=0.3, engine=engine), full, [300, 300, 300],
+          "lengths above Cmax")
+    neg = run_qk(gq, q, k, torch.tensor([0, -4, -(1 << 30)], dtype=torch.int32), scale=0.3,
+                 engine=engine)
     assert np.all(neg == SENTINEL), "non-positive lengths wrote rows"
-    assert np.array_equal(run_qk(gq, q, k, None, scale=0.3), a), "not bitwise reproducible"
+    assert np.array_equal(run_qk(gq, q, k, None, scale=0.3, engine=engine), a), \
+        "not bitwise reproducible"
     # The two modes agree.
-    check(run_qk(gq, q, k, None, 0, 0.3), full, None, "per-head")
+    check(run_qk(gq, q, k, None, 0, 0.3, engine=engine), full, None, "per-head")
 
 
+@pytest.mark.parametrize("engine", [1, 2], ids=["fma", "tensor"])
 @pytest.mark.parametrize("name", ["small", "llama", "phi", "mqa"])
-def test_score_step_workload_shapes(gq, name):
+def test_score_step_workload_shapes(gq, name, engine):
     """The AV workloads' shapes, with K drawn like V, and the chained call:
     the AV reduction on the score step's weights against the oracles' chain."""
     from gqa_attention_weighted_gb300 import workloads as W
@@ -113,8 +124,8 @@ def test_score_step_workload_shapes(gq, name):
     q, k, sl = qk_case(rng, w.B, w.Cmax, w.Hq, w.Hkv, w.D, w.v_dtype, lens)
     scale = w.D ** -0.5
     ref = gqa_qk.gqa_qk_softmax(q.numpy(), bits(k), w.v_dtype, sl.numpy(), scale)
-    got = run_qk(gq, q, k, sl)
-    check(got, ref, lens, name)
+    got = run_qk(gq, q, k, sl, engine=engine)
+    check(got, ref, lens, f"{name} engine={engine}")
     # Chain: out = AV(attn from the score step, V); V reuses K's shape.
     dev = torch.device("cuda")
     v = torch.tensor(rng.standard_normal((w.B, w.Cmax, w.Hkv, w.D)),
