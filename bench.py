@@ -41,6 +41,7 @@ UNIT = "GB/s"
 METRIC_QK = ("GQA QK-softmax decode achieved HBM GB/s over compulsory bytes (K read once), "
              "µs/call")
 QK_SOURCES = ["gqa_attention_weighted_gb300/csrc/gqa_qk_kernel.cuh",
+              "gqa_attention_weighted_gb300/csrc/gqa_qk_mma.cuh",
               "gqa_attention_weighted_gb300/csrc/gqa_qk_api.cu",
               "gqa_attention_weighted_gb300/csrc/gqa_av_kernel.cuh"]
 DEFAULT_WORKLOAD = "llama"
@@ -314,8 +315,11 @@ def run_gpu_qk(args, rank, world, local):
     flops = W.flops(w, lens)
     scale = w.D ** -0.5
 
+    engine = ENGINES[args.engine]
+
     def call(st, attn):
-        gq.gqa_qk_softmax_decode(st["q"], st["k"], st["seq_lens"], attn, mode=mode, scale=scale)
+        gq.gqa_qk_softmax_decode(st["q"], st["k"], st["seq_lens"], attn, mode=mode, scale=scale,
+                                 engine=engine)
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     set_bytes = x["k"].numel() * 2 + w.B * w.Cmax * w.Hq * 4 + x["q"].numel() * 4
@@ -405,6 +409,7 @@ def run_gpu_qk(args, rank, world, local):
         "us_per_call": ms_per_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {**w.describe(), "op": "qk", "mode": args.mode, "resolved_mode": resolved,
+                   "engine": args.engine, "resolved_engine": engine or 2,
                    "scale": scale, "parallelism": f"replicas{world}" if world > 1 else "single",
                    "compulsory_bytes_per_call": cbytes, "flops_per_call": flops,
                    "l2": f"rotating {n_sets} input sets, {n_sets * set_bytes / 1e6:.0f} MB "
@@ -415,7 +420,8 @@ def run_gpu_qk(args, rank, world, local):
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_kind": f"{peak_kind} hbm_gbs (copy)",
                      "traffic": committed_traffic_qk(w.name, resolved),
-                     "kernel": "gqa_qk_kernel", "kernel_hash": kernel_hash(QK_SOURCES),
+                     "kernel": "gqa_qk_kernel" if engine == 1 else "gqa_qk_mma_kernel",
+                     "kernel_hash": kernel_hash(QK_SOURCES),
                      "duration": "average time of one whole call (score kernel and the "
                                  "normalise kernel) over the timed region"},
         "e2e": e2e,

@@ -149,8 +149,16 @@ int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int k_dtype, int mode
   const int optin = static_cast<int>(prop.sharedMemPerBlockOptin);
 
   p->tiles = p->hgroups * B;
-  long long want = p->tiles < sms ? std::max(1, sms / p->tiles)
-                                  : (2LL * sms + p->tiles - 1) / p->tiles;
+  // FMA kernel: one CTA per SM on few-tile shapes. Tensor-core kernel: on
+  // short streams with D <= 128 (at most 2048 rows a CTA at two CTAs per SM),
+  // about two CTAs per SM with a ring of about 96 KiB; otherwise, like the FMA
+  // kernel, a deep ring of about 160 KiB and one CTA per SM (each measured
+  // faster in its regime).
+  const long long tile_rows = static_cast<long long>(p->tiles) * Cmax;
+  const bool short_tc = tensor && D <= 128 && tile_rows <= 2048LL * 2 * sms;
+  long long want = short_tc ? (2LL * sms + p->tiles - 1) / p->tiles
+                   : p->tiles < sms ? std::max(1, sms / p->tiles)
+                                    : (2LL * sms + p->tiles - 1) / p->tiles;
   want = std::max<long long>(1, std::min<long long>(want, (Cmax + p->R - 1) / p->R));
   const int rps0 = static_cast<int>((Cmax + want - 1) / want);
   p->rows_per_split = (rps0 + p->R - 1) / p->R * p->R;
@@ -159,10 +167,12 @@ int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int k_dtype, int mode
     return qfail(GQA_AV_ERR_UNSUPPORTED, "grid too large");
 
   const int q_bytes = p->heads * D * 4;
-  // FMA kernel: 3 stages (2 if that does not fit). Tensor-core kernel: as deep
-  // a ring as about 160 KiB holds (2 to 8 stages).
+  // FMA kernel: 3 stages (2 if that does not fit). Tensor-core kernel: a stage
+  // per 128 rows of the split, as many as the ring above holds (2 to 8).
+  const int iters = p->rows_per_split / p->R;
+  const int ring = short_tc ? 98304 : 163840;
   const int want_stages =
-      tensor ? std::max(2, std::min(kMaxStages, 163840 / p->stage_bytes)) : 3;
+      tensor ? std::max(2, std::min(std::min(kMaxStages, iters), ring / p->stage_bytes)) : 3;
   for (p->stages = want_stages; p->stages >= 2; --p->stages) {
     if (tensor) {
       p->b_off = p->stages * p->stage_bytes;
@@ -184,11 +194,12 @@ int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int k_dtype, int mode
                  optin);
   p->ws_bytes = static_cast<size_t>(p->tiles) * p->nsplit * p->heads * sizeof(float2);
 
-  // Normalise: about two CTAs per SM over the batch's rows.
-  p->norm_ctas_per_b = static_cast<int>(
-      std::max<long long>(1, std::min<long long>((2LL * sms + B - 1) / B, (Cmax + 7) / 8)));
-  p->norm_rows = (Cmax + p->norm_ctas_per_b - 1) / p->norm_ctas_per_b;
+  // Normalise: about kQkNormBatch scores a thread, so each thread has one
+  // round of loads in flight.
+  p->norm_rows = std::max(1, kQkNormBatch * kQkNormThreads / Hq);
   p->norm_ctas_per_b = (Cmax + p->norm_rows - 1) / p->norm_rows;
+  if (static_cast<long long>(B) * p->norm_ctas_per_b > 0x7fffffffLL)
+    return qfail(GQA_AV_ERR_UNSUPPORTED, "normalise grid too large");
   return GQA_AV_OK;
 }
 

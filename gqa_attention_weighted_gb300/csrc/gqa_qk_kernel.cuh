@@ -34,6 +34,8 @@ constexpr int kQkConsumerWarps = 8;
 constexpr int kQkConsumerThreads = 32 * kQkConsumerWarps;
 constexpr int kQkThreads = kQkConsumerThreads + 32;  // + the producer warp
 constexpr int kQkNormThreads = 256;
+constexpr int kQkNormBatch = 8;          // scores each normalise thread loads at once
+constexpr int kQkNormMaxPairs = 3072;     // (head, split) pairs staged in shared memory
 constexpr int kQkMaxHeads = 64;
 
 struct alignas(64) QkParams {
@@ -285,16 +287,37 @@ gqa_qk_normalize_kernel(const __grid_constant__ QkNormParams p) {
   const int c0 = blk * p.rows_per_cta;
   const int c1 = min(c0 + p.rows_per_cta, L);
   if (c0 >= c1) return;
-  // One warp per head: its lanes load the splits' pairs together (split s on
-  // lane s % 32), merge their own in split order, then the lanes are merged
-  // in a fixed butterfly order.
+  // Every (head, split) pair of b in one round of loads into shared memory
+  // (when they fit), then one warp per head merges its splits: lanes take
+  // splits s, s + 32, ... in split order, then a fixed butterfly.
+  __shared__ float2 pairs[kQkNormMaxPairs];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int h = warp; h < p.Hq; h += kQkNormThreads / 32) {
+  const int npairs = p.Hq * nsplit_b;
+  const bool staged = npairs <= kQkNormMaxPairs;
+  auto pair_at = [&](int h, int s) {
     const int hg = h / p.heads, hh = h - hg * p.heads;
-    const float2* st = p.stats + ((size_t)(hg * p.B + b) * p.nsplit) * p.heads + hh;
+    return p.stats + ((size_t)(hg * p.B + b) * p.nsplit + s) * p.heads + hh;
+  };
+  if (staged) {
+    for (int i0 = threadIdx.x; i0 < npairs; i0 += kQkNormBatch * kQkNormThreads) {
+      float2 v[kQkNormBatch];
+#pragma unroll
+      for (int u = 0; u < kQkNormBatch; ++u) {
+        const int i = i0 + u * kQkNormThreads;
+        if (i < npairs) v[u] = __ldcg(pair_at(i / nsplit_b, i % nsplit_b));
+      }
+#pragma unroll
+      for (int u = 0; u < kQkNormBatch; ++u) {
+        const int i = i0 + u * kQkNormThreads;
+        if (i < npairs) pairs[i] = v[u];
+      }
+    }
+    __syncthreads();
+  }
+  for (int h = warp; h < p.Hq; h += kQkNormThreads / 32) {
     float M = -INFINITY, S = 0.0f;
     for (int s = lane; s < nsplit_b; s += 32) {
-      const float2 v = __ldcg(st + (size_t)s * p.heads);
+      const float2 v = staged ? pairs[h * nsplit_b + s] : __ldcg(pair_at(h, s));
       lse_merge(M, S, v.x, v.y);
     }
 #pragma unroll
@@ -306,12 +329,25 @@ gqa_qk_normalize_kernel(const __grid_constant__ QkNormParams p) {
     if (lane == 0) ms[h] = make_float2(M, 1.0f / S);
   }
   __syncthreads();
-  const size_t n = (size_t)(c1 - c0) * p.Hq;
+  // The block's rows are contiguous: each thread loads its (at most
+  // kQkNormBatch) scores together, then rewrites them.
+  const int n = (c1 - c0) * p.Hq;
   float* row0 = p.attn + ((size_t)b * p.Cmax + c0) * p.Hq;
-  for (size_t i = threadIdx.x; i < n; i += kQkNormThreads) {
-    const int h = (int)(i % p.Hq);
-    const float2 v = ms[h];
-    row0[i] = expf(__ldcg(row0 + i) - v.x) * v.y;
+  for (int i0 = threadIdx.x; i0 < n; i0 += kQkNormBatch * kQkNormThreads) {
+    float x[kQkNormBatch];
+#pragma unroll
+    for (int u = 0; u < kQkNormBatch; ++u) {
+      const int i = i0 + u * kQkNormThreads;
+      x[u] = i < n ? __ldcg(row0 + i) : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < kQkNormBatch; ++u) {
+      const int i = i0 + u * kQkNormThreads;
+      if (i < n) {
+        const float2 v = ms[i % p.Hq];
+        row0[i] = expf(x[u] - v.x) * v.y;
+      }
+    }
   }
 }
 
