@@ -419,7 +419,7 @@ def run_gpu_qk(args, rank, world, local):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_kind": f"{peak_kind} hbm_gbs (copy)",
-                     "traffic": committed_traffic_qk(w.name, resolved),
+                     "traffic": committed_traffic_qk(w.name, resolved, engine or 2),
                      "kernel": "gqa_qk_kernel" if engine == 1 else "gqa_qk_mma_kernel",
                      "kernel_hash": kernel_hash(QK_SOURCES),
                      "duration": "average time of one whole call (score kernel and the "
@@ -434,7 +434,7 @@ def run_gpu_qk(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
-def committed_traffic_qk(workload: str, mode: int):
+def committed_traffic_qk(workload: str, mode: int, engine: int):
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
@@ -443,7 +443,8 @@ def committed_traffic_qk(workload: str, mode: int):
         return None
     for e in entries:
         if (e.get("op") == "qk" and e.get("kernel_hash") == kernel_hash(QK_SOURCES)
-                and e.get("workload") == workload and e.get("mode") == mode):
+                and e.get("workload") == workload and e.get("mode") == mode
+                and e.get("engine") == engine):
             return e.get("traffic_bytes_per_launch")
     return None
 
