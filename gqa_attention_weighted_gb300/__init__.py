@@ -17,7 +17,7 @@ _BINDING = ("gqa_av_decode", "gqa_av_decode_per_head", "gqa_av_decode_tuned",
             "gqa_av_workspace_bytes", "gqa_av_set_workspace", "gqa_av_device_status",
             "gqa_av_status_string", "gqa_av_last_error", "GqaAvError", "MODE_AUTO",
             "MODE_PER_HEAD", "MODE_GQA", "GQA_AV_BF16", "GQA_AV_FP16",
-            "gqa_qk_softmax_decode", "gqa_qk_device_status")
+            "gqa_qk_softmax_decode", "gqa_qk_device_status", "gqa_av_decode_paged")
 
 
 def __getattr__(name):

@@ -66,6 +66,8 @@ def _load() -> ctypes.CDLL:
     lib.gqa_av_decode_per_head.argtypes = [P, P, P, P, *sizes, I, P]
     lib.gqa_av_decode_tuned.argtypes = [P, P, P, P, *sizes, I, I, ctypes.POINTER(Tuning), P]
     lib.gqa_av_decode_noalloc.argtypes = [P, P, P, P, *sizes, I, I, P]
+    lib.gqa_av_decode_paged.argtypes = [P, P, P, P, P, *sizes, I, I, I, I, I,
+                                        ctypes.POINTER(Tuning), P]
     lib.gqa_av_plan.argtypes = [*sizes, I, I, ctypes.POINTER(Tuning), ctypes.POINTER(PlanInfo)]
     lib.gqa_av_workspace_bytes.argtypes = [*sizes, I, I]
     lib.gqa_av_workspace_bytes.restype = S
@@ -81,7 +83,7 @@ def _load() -> ctypes.CDLL:
     lib.gqa_qk_device_status.argtypes = [P, I]
     lib.gqa_qk_last_error.argtypes = []
     lib.gqa_qk_last_error.restype = ctypes.c_char_p
-    for f in ("gqa_av_decode", "gqa_av_decode_per_head", "gqa_av_decode_tuned",
+    for f in ("gqa_av_decode", "gqa_av_decode_per_head", "gqa_av_decode_tuned", "gqa_av_decode_paged",
               "gqa_av_decode_noalloc", "gqa_av_plan",
               "gqa_av_set_workspace", "gqa_av_device_status", "gqa_av_version",
               "gqa_qk_softmax_decode", "gqa_qk_softmax_decode_tuned", "gqa_qk_device_status"):
@@ -176,6 +178,37 @@ def gqa_av_decode_tuned(attn, v_cache, seq_lens, out, mode=MODE_AUTO, tuning=Non
     t = _tuning(tuning)
     _check(lib.gqa_av_decode_tuned(_ptr(attn), _ptr(v_cache), _ptr(seq_lens), _ptr(out),
                                    B, C, Hq, Hkv, D, vd, int(mode),
+                                   ctypes.byref(t) if t is not None else None,
+                                   _stream_handle(stream)))
+    return out
+
+
+def gqa_av_decode_paged(attn, v_pool, block_table, seq_lens, out, mode=MODE_AUTO, tuning=None,
+                        stream=None) -> torch.Tensor:
+    """gqa_av_decode over a paged V cache: v_pool [num_blocks, block_size, Hkv, D],
+    block_table [B, max_blocks] int32 (row c of sequence b in block
+    block_table[b, c // block_size])."""
+    if attn.dim() != 3 or v_pool.dim() != 4 or out.dim() != 3 or block_table.dim() != 2:
+        raise ValueError("attn [B,Cmax,Hq], v_pool [blocks,block_size,Hkv,D], block_table "
+                         "[B,max_blocks], out [B,Hq,D]")
+    B, Cmax, Hq = attn.shape
+    num_blocks, block_size, Hkv, D = v_pool.shape
+    if tuple(out.shape) != (B, Hq, D) or block_table.shape[0] != B:
+        raise ValueError("inconsistent shapes")
+    for name, t in (("attn", attn), ("v_pool", v_pool), ("out", out), ("block_table", block_table)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if attn.dtype != torch.float32 or out.dtype != torch.float32:
+        raise ValueError("attn and out must be float32")
+    if v_pool.dtype not in _V_DTYPE or block_table.dtype != torch.int32:
+        raise ValueError("v_pool must be bfloat16 or float16 and block_table int32")
+    if seq_lens is not None and (not seq_lens.is_cuda or seq_lens.dtype != torch.int32
+                                 or seq_lens.numel() != B or not seq_lens.is_contiguous()):
+        raise ValueError("seq_lens must be a contiguous CUDA int32 tensor of B elements")
+    t = _tuning(tuning)
+    _check(lib.gqa_av_decode_paged(_ptr(attn), _ptr(v_pool), _ptr(block_table), _ptr(seq_lens),
+                                   _ptr(out), B, Cmax, Hq, Hkv, D, _V_DTYPE[v_pool.dtype],
+                                   block_size, num_blocks, block_table.shape[1], int(mode),
                                    ctypes.byref(t) if t is not None else None,
                                    _stream_handle(stream)))
     return out

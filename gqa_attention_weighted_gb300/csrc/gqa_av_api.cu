@@ -12,6 +12,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <numeric>
 #include <string>
 #include <tuple>
 
@@ -172,6 +173,7 @@ struct Plan {
   int grid;                                // CTAs of the main kernel
   int split_units;                         // tensor core: CTAs the context is balanced over
   int balanced;                            // tensor core: splits balanced over the batch's lengths
+  int chunk_rows;                          // rows per V box (R, or a paged block)
   int one_per_sm;                          // shared memory padded so one CTA fits per SM
   int early;                               // stages issued before the length is read
   int engine;                              // kEngineFma or kEngineTensor
@@ -230,7 +232,7 @@ void layout(Plan* p, int min_smem = 0) {
 }
 
 int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode,
-              const gqa_av_tuning* t, Plan* p) {
+              const gqa_av_tuning* t, Plan* p, int block_size = 0) {
   int rc = check_shape(B, Cmax, Hq, Hkv, D, v_dtype, mode);
   if (rc) return rc;
   DeviceInfo di;
@@ -357,6 +359,27 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
     iters = (rps0 + rmax - 1) / rmax;
     p->R = static_cast<int>(align_up((rps0 + iters - 1) / iters, rq));
   }
+  p->chunk_rows = p->R;
+  if (block_size > 0) {
+    // Paged V: a stage is whole blocks (one box each) or a divisor of a block.
+    if (p->R >= block_size) {
+      const int unit = std::lcm(block_size, rq);
+      if (unit > 256 || (t && t->rows_per_stage > 0 && p->R % unit))
+        return fail(GQA_AV_ERR_INVALID, "rows_per_stage=%d does not fit blocks of %d rows",
+                    p->R, block_size);
+      p->R = std::max(unit, p->R / unit * unit);
+      p->chunk_rows = block_size;
+    } else {
+      int r = p->R;
+      while (r > rq && block_size % r) r -= rq;
+      if (block_size % r || (t && t->rows_per_stage > 0 && r != p->R))
+        return fail(GQA_AV_ERR_INVALID, "no stage of a multiple of %d rows divides blocks of %d",
+                    rq, block_size);
+      p->R = r;
+      p->chunk_rows = r;
+    }
+    iters = (rps0 + p->R - 1) / p->R;
+  }
   p->rows_per_split = p->R * iters;
   p->nsplit = (Cmax + p->rows_per_split - 1) / p->rows_per_split;
   // Splits of the tensor-core kernel on shapes that run in waves (as many
@@ -471,6 +494,7 @@ void fill_params(Params* p, const Plan& pl, const float* attn, const int32_t* se
   p->cvt_warps = pl.cvt_warps;
   p->split_units = pl.split_units;
   p->balanced = pl.balanced;
+  p->chunk_rows = pl.chunk_rows;
   // attn is 16-byte aligned (checked before planning): a TMA source or a
   // cp.async of up to 16 bytes can start at any 4-head boundary of it.
 }
@@ -568,6 +592,8 @@ int encode_fn(PFN_cuTensorMapEncodeTiled_v12000* fn) {
 // V viewed as 4-D {D, Hkv, Cmax, B} (innermost first); box {dt, 1, R, 1}, or
 // for the tensor-core kernel {64, 1, R, 1} with the 128-byte swizzle its A
 // operand is read in.
+// A paged cache is the same view of the block pool: {D, Hkv, block_size,
+// num_blocks} with a box of `R` = chunk rows.
 int encode_v_map(CUtensorMap* m, const void* v, int B, int Cmax, int Hkv, int D, int dt, int R,
                  bool mma) {
   PFN_cuTensorMapEncodeTiled_v12000 enc;
@@ -609,10 +635,22 @@ int current_device(int* dev) {
 
 int run(const float* attn, const void* v, const int32_t* seq_lens, float* out, int B, int Cmax,
         int Hq, int Hkv, int D, int v_dtype, int mode, const gqa_av_tuning* tuning,
-        cudaStream_t stream) {
+        cudaStream_t stream, const int32_t* block_table = nullptr, int block_size = 0,
+        int num_blocks = 0, int max_blocks = 0) {
   g_last_error.clear();
   int rc = check_shape(B, Cmax, Hq, Hkv, D, v_dtype, mode);
   if (rc) return rc;
+  if (block_table) {
+    if (block_size <= 0 || block_size % 8 || num_blocks <= 0 || max_blocks <= 0)
+      return fail(GQA_AV_ERR_INVALID,
+                  "paged V: block_size=%d must be a positive multiple of 8, num_blocks=%d and "
+                  "max_blocks=%d positive", block_size, num_blocks, max_blocks);
+    if (static_cast<long long>(max_blocks) * block_size < Cmax)
+      return fail(GQA_AV_ERR_INVALID, "paged V: max_blocks x block_size = %lld < Cmax = %d",
+                  static_cast<long long>(max_blocks) * block_size, Cmax);
+    if (reinterpret_cast<uintptr_t>(block_table) & 3)
+      return fail(GQA_AV_ERR_INVALID, "block_table must be 4-byte aligned");
+  }
   if (!attn || !v || !out) return fail(GQA_AV_ERR_INVALID, "attn, v_cache and out must be non-NULL");
   if ((reinterpret_cast<uintptr_t>(attn) | reinterpret_cast<uintptr_t>(v) |
        reinterpret_cast<uintptr_t>(out)) & 15)
@@ -622,15 +660,25 @@ int run(const float* attn, const void* v, const int32_t* seq_lens, float* out, i
   int dev;
   if ((rc = current_device(&dev))) return rc;
   Plan pl;
-  if ((rc = make_plan(dev, B, Cmax, Hq, Hkv, D, v_dtype, mode, tuning, &pl))) return rc;
+  if ((rc = make_plan(dev, B, Cmax, Hq, Hkv, D, v_dtype, mode, tuning, &pl, block_table ? block_size : 0)))
+    return rc;
   Workspace ws;
   if ((rc = workspace(dev, kHeaderBytes + pl.ws_bytes, stream, &ws))) return rc;
 
   Params p;
   memset(&p, 0, sizeof p);
-  if ((rc = encode_v_map(&p.v_map, v, B, Cmax, Hkv, D, pl.dt, pl.R, pl.engine == kEngineTensor))) return rc;
+  if (block_table)
+    rc = encode_v_map(&p.v_map, v, num_blocks, block_size, Hkv, D, pl.dt, pl.chunk_rows,
+                      pl.engine == kEngineTensor);
+  else
+    rc = encode_v_map(&p.v_map, v, B, Cmax, Hkv, D, pl.dt, pl.R, pl.engine == kEngineTensor);
+  if (rc) return rc;
   char* wsb = static_cast<char*>(ws.base);
   fill_params(&p, pl, attn, seq_lens, out, wsb, wsb + kHeaderBytes, B, Cmax, Hq, Hkv, D);
+  p.block_table = block_table;
+  p.block_size = block_size;
+  p.max_blocks = max_blocks;
+  p.num_blocks = num_blocks;
   if (p.attn_tma && (rc = encode_attn_map(&p.a_map, attn, B, Cmax, Hq, pl.ap, pl.R))) return rc;
 
   Kernel kern;
@@ -685,6 +733,18 @@ int gqa_av_decode_tuned(const float* attn, const void* v_cache, const int32_t* s
                         const gqa_av_tuning* tuning, void* stream) {
   return run(attn, v_cache, seq_lens, out, B, Cmax, Hq, Hkv, D, v_dtype, mode, tuning,
              static_cast<cudaStream_t>(stream));
+}
+
+int gqa_av_decode_paged(const float* attn, const void* v_pool, const int32_t* block_table,
+                        const int32_t* seq_lens, float* out, int B, int Cmax, int Hq, int Hkv,
+                        int D, int v_dtype, int block_size, int num_blocks, int max_blocks,
+                        int mode, const gqa_av_tuning* tuning, void* stream) {
+  if (!block_table) {
+    g_last_error.clear();
+    return fail(GQA_AV_ERR_INVALID, "block_table must be non-NULL");
+  }
+  return run(attn, v_pool, seq_lens, out, B, Cmax, Hq, Hkv, D, v_dtype, mode, tuning,
+             static_cast<cudaStream_t>(stream), block_table, block_size, num_blocks, max_blocks);
 }
 
 int gqa_av_plan(int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode,

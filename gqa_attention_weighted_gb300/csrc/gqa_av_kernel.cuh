@@ -93,6 +93,13 @@ struct alignas(64) Params {
   int cvt_warps;                // weight-conversion warps (2 or 4)
   int split_units;              // CTAs the batch's context is spread over (length-balanced splits)
   int balanced;                 // splits balanced over the batch's lengths (else fixed)
+  // Paged V: the tensor map is over a pool of blocks {D, Hkv, block_size,
+  // num_blocks}; a stage's rows come as chunk_rows-row boxes from the blocks
+  // that hold them (block_table[b][c / block_size]). Contiguous V: null table,
+  // chunk_rows = R.
+  const int32_t* block_table;   // [B, max_blocks] or null
+  int block_size, max_blocks, num_blocks;
+  int chunk_rows;               // rows per V box
 };
 
 // The split combine: out[tile column] = sum over the tile's splits with
@@ -331,6 +338,17 @@ __device__ __forceinline__ void sum_strided(float4& s, const float4* src, size_t
   }
 }
 
+// TMA row and outermost coordinates of context row c of sequence b: (c, b)
+// for a contiguous cache, (c % block_size, block_table[b][c / block_size])
+// for a paged one. Rows at or past Cmax, and block indices outside the pool,
+// land outside the tensor map, which the TMA unit fills with zeros.
+__device__ __forceinline__ int2 v_row_coord(const Params& p, int b, int c) {
+  if (!p.block_table) return make_int2(c, b);
+  if (c >= p.Cmax) return make_int2(0, p.num_blocks);
+  const int j = c / p.block_size;
+  return make_int2(c - j * p.block_size, p.block_table[(size_t)b * p.max_blocks + j]);
+}
+
 // ---------------------------------------------------------------------------
 // Length-balanced splits (the tensor-core kernel and its combine).
 //
@@ -499,15 +517,25 @@ gqa_av_kernel(const __grid_constant__ Params p) {
 
   if (warp == kConsumerWarps) {
     // ----------------------------------------------------------------- producer
-    // V rows [c0, c0 + R) by TMA; their attn weights by a second TMA box, or
-    // (unaligned head groups) the weights of the first `rows` of them by cp.async.
+    // V rows [c0, c0 + R) by TMA (one box, or one box a block of a paged
+    // cache); their attn weights by a second TMA box, or (unaligned head
+    // groups) the weights of the first `rows` of them by cp.async.
+    auto load_v = [&](uint32_t dst, int c0, uint32_t full) {
+      if (!p.block_table) {
+        tma_load_4d(dst, &p.v_map, d0, kv_h, c0, b, full, policy);
+        return;
+      }
+      for (int r0 = 0; r0 < p.R; r0 += p.chunk_rows) {
+        const int2 rc = v_row_coord(p, b, c0 + r0);
+        tma_load_4d(dst + (uint32_t)r0 * p.dt * 2, &p.v_map, d0, kv_h, rc.x, rc.y, full, policy);
+      }
+    };
     auto issue = [&](int stage, int c0, int rows) {
       const uint32_t full = full0 + 8 * stage;
       if (p.attn_tma) {
         if (lane == 0) {
           mbar_arrive_expect_tx(full, p.v_stage_bytes + p.a_stage_bytes);
-          tma_load_4d(vring_s + (uint32_t)stage * p.v_stage_bytes, &p.v_map, d0, kv_h, c0, b, full,
-                      policy);
+          load_v(vring_s + (uint32_t)stage * p.v_stage_bytes, c0, full);
           tma_load_3d(aring_s + (uint32_t)stage * p.a_stage_bytes, &p.a_map, h0 - a_shift, c0, b,
                       full, policy);
         }
@@ -515,8 +543,7 @@ gqa_av_kernel(const __grid_constant__ Params p) {
       }
       if (lane == 0) {
         mbar_arrive_expect_tx(full, p.v_stage_bytes);
-        tma_load_4d(vring_s + (uint32_t)stage * p.v_stage_bytes, &p.v_map, d0, kv_h, c0, b, full,
-                    policy);
+        load_v(vring_s + (uint32_t)stage * p.v_stage_bytes, c0, full);
       }
       const float* src = attn_b + (size_t)c0 * p.Hq;
       const uint32_t dst = aring_s + 4u * (uint32_t)(stage * p.R * p.ap);

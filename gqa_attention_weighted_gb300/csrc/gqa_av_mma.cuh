@@ -349,9 +349,18 @@ __global__ void __launch_bounds__(kMmaMaxThreads, NB == 1 ? 3 : (NB == 2 ? 2 : 1
       if (lane == 0) {
         mbar_arrive_expect_tx(full, (uint32_t)p.v_halves * (p.v_stage_bytes / 2) +
                                         (p.attn_tma ? p.a_stage_bytes : 0u));
-        for (int h = 0; h < p.v_halves; ++h)
-          tma_load_4d(vdst + (uint32_t)h * p.v_stage_bytes / 2, &p.v_map, d0 + 64 * h, kv_h, c0, b,
-                      full, policy);
+        if (!p.block_table) {
+          for (int h = 0; h < p.v_halves; ++h)
+            tma_load_4d(vdst + (uint32_t)h * p.v_stage_bytes / 2, &p.v_map, d0 + 64 * h, kv_h, c0,
+                        b, full, policy);
+        } else {
+          for (int h = 0; h < p.v_halves; ++h)
+            for (int r0 = 0; r0 < p.R; r0 += p.chunk_rows) {  // one box a paged block
+              const int2 rc = v_row_coord(p, b, c0 + r0);
+              tma_load_4d(vdst + (uint32_t)h * p.v_stage_bytes / 2 + (uint32_t)r0 * 128, &p.v_map,
+                          d0 + 64 * h, kv_h, rc.x, rc.y, full, policy);
+            }
+        }
         if (p.attn_tma)
           tma_load_3d(aring_s + (uint32_t)stage * p.a_stage_bytes, &p.a_map, h0 - a_shift, c0, b,
                       full, policy);

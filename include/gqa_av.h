@@ -120,6 +120,21 @@ int gqa_av_decode_tuned(const float *attn, const void *v_cache, const int32_t *s
                         float *out, int B, int Cmax, int Hq, int Hkv, int D,
                         int v_dtype, int mode, const gqa_av_tuning *tuning, void *stream);
 
+/*
+ * Paged V cache (a block table, as serving engines keep their KV cache):
+ * the same reduction, with V row c of sequence b at
+ *     v_pool[block_table[b * max_blocks + c / block_size]][c % block_size][kv_h][:],
+ *     v_pool [num_blocks, block_size, Hkv, D] (bf16/fp16), block_table [B, max_blocks] int32.
+ * attn, seq_lens and out are as in gqa_av_decode, with Cmax <= max_blocks * block_size.
+ * block_size is a positive multiple of 8; a stage is whole blocks or a divisor of one.
+ * Table entries of blocks past a sequence's length are never used for the sum and may
+ * hold anything; an entry outside [0, num_blocks) reads zeros. tuning may be NULL.
+ */
+int gqa_av_decode_paged(const float *attn, const void *v_pool, const int32_t *block_table,
+                        const int32_t *seq_lens, float *out, int B, int Cmax, int Hq, int Hkv,
+                        int D, int v_dtype, int block_size, int num_blocks, int max_blocks,
+                        int mode, const gqa_av_tuning *tuning, void *stream);
+
 /* The launch shape a call with these arguments would use (no launch, no allocation). */
 typedef struct gqa_av_plan_info {
     int mode;            /* resolved mode: 0 per-head, 1 GQA-reuse */
