@@ -190,13 +190,19 @@ def run_gpu(args, rank, world, local):
     tuning = tuning or None
 
     def call(s, out):
-        if tuning is None:
+        if "table" in s:
+            gq.gqa_av_decode_paged(s["attn"], s["v"], s["table"], s["seq_lens"], out, mode=mode,
+                                   tuning=tuning)
+        elif tuning is None:
             gq.gqa_av_decode(s["attn"], s["v"], s["seq_lens"], out, mode=mode)
         else:
             gq.gqa_av_decode_tuned(s["attn"], s["v"], s["seq_lens"], out, mode=mode,
                                    tuning=tuning)
 
     x = W.generate(w, dev, pad="zero")
+    x_contig = x
+    if args.paged:
+        x = paged_inputs(x, args.paged, w.seed)
     lens = x["seq_lens"].cpu().tolist()
     cbytes = W.compulsory_bytes(w, lens)
     flops = W.flops(w, lens)
@@ -261,7 +267,7 @@ def run_gpu(args, rank, world, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = oracle_baseline(w, x, args.cpu_seconds)
+        cpu = oracle_baseline(w, x_contig, args.cpu_seconds)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -271,6 +277,7 @@ def run_gpu(args, rank, world, local):
         "config": {**w.describe(), "mode": args.mode, "resolved_mode": plan["mode"],
                    "engine": args.engine, "resolved_engine": plan["engine"],
                    "split_mode": args.split_mode, "resolved_split_mode": plan["split_mode"],
+                   "paged_block_size": args.paged or None,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "compulsory_bytes_per_call": cbytes, "flops_per_call": flops,
                    "l2": f"rotating {n_sets} input sets, {n_sets * set_bytes / 1e6:.0f} MB "
@@ -282,8 +289,8 @@ def run_gpu(args, rank, world, local):
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_kind": f"{peak_kind} hbm_gbs (copy)",
                      "frac_of_8tbs_nominal": round(achieved / 8000.0, 4),
-                     "traffic": committed_traffic(w.name, plan["mode"], plan["engine"],
-                                                  plan["split_mode"]),
+                     "traffic": None if args.paged else committed_traffic(
+                         w.name, plan["mode"], plan["engine"], plan["split_mode"]),
                      "kernel": KERNEL_NAMES[plan["engine"]], "kernel_hash": kernel_hash(),
                      "duration": "average time of one whole call (main kernel and, when the "
                                  "context is split, the split-combine kernel) over the timed "
@@ -296,6 +303,22 @@ def run_gpu(args, rank, world, local):
         line["cpu_baseline"] = cpu
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def paged_inputs(x, bs, seed):
+    """The workload's V as a paged cache: blocks of `bs` rows in a pool in a
+    seeded random order, and the block table that maps each sequence onto it."""
+    v = x["v"]
+    B, C, Hkv, D = v.shape
+    maxb = (C + bs - 1) // bs
+    g = torch.Generator(device="cpu").manual_seed(seed + 2)
+    perm = torch.randperm(B * maxb, generator=g).to(v.device)
+    pool = torch.zeros((B * maxb, bs, Hkv, D), dtype=v.dtype, device=v.device)
+    padded = torch.zeros((B, maxb * bs, Hkv, D), dtype=v.dtype, device=v.device)
+    padded[:, :C] = v
+    pool[perm] = padded.view(B * maxb, bs, Hkv, D)
+    table = perm.view(B, maxb).to(torch.int32).contiguous()
+    return {"attn": x["attn"], "v": pool, "table": table, "seq_lens": x["seq_lens"]}
 
 
 def run_gpu_qk(args, rank, world, local):
@@ -615,6 +638,9 @@ def main():
     ap.add_argument("--op", choices=["av", "qk"], default="av",
                     help="av: the AV reduction (the benchmark); qk: the decode score step "
                          "before it")
+    ap.add_argument("--paged", type=int, default=0, metavar="BLOCK_SIZE",
+                    help="run the AV call on a paged copy of V (blocks of this many rows in a "
+                         "shuffled pool, gqa_av_decode_paged)")
     ap.add_argument("--graph-len", type=int, default=500)
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
