@@ -520,30 +520,33 @@ gqa_av_kernel(const __grid_constant__ Params p) {
     // V rows [c0, c0 + R) by TMA (one box, or one box a block of a paged
     // cache); their attn weights by a second TMA box, or (unaligned head
     // groups) the weights of the first `rows` of them by cp.async.
+    // Paged: the stage's block indices are loaded by the warp's lanes together
+    // (lane j for box j), then lane 0 issues the boxes. Called by all lanes.
     auto load_v = [&](uint32_t dst, int c0, uint32_t full) {
       if (!p.block_table) {
-        tma_load_4d(dst, &p.v_map, d0, kv_h, c0, b, full, policy);
+        if (lane == 0) tma_load_4d(dst, &p.v_map, d0, kv_h, c0, b, full, policy);
         return;
       }
-      for (int r0 = 0; r0 < p.R; r0 += p.chunk_rows) {
-        const int2 rc = v_row_coord(p, b, c0 + r0);
-        tma_load_4d(dst + (uint32_t)r0 * p.dt * 2, &p.v_map, d0, kv_h, rc.x, rc.y, full, policy);
+      const int nbox = p.R / p.chunk_rows;  // <= 32
+      const int2 mine = lane < nbox ? v_row_coord(p, b, c0 + lane * p.chunk_rows) : make_int2(0, 0);
+      for (int j = 0; j < nbox; ++j) {
+        const int rx = __shfl_sync(0xffffffffu, mine.x, j);
+        const int ry = __shfl_sync(0xffffffffu, mine.y, j);
+        if (lane == 0)
+          tma_load_4d(dst + (uint32_t)(j * p.chunk_rows) * p.dt * 2, &p.v_map, d0, kv_h, rx, ry,
+                      full, policy);
       }
     };
     auto issue = [&](int stage, int c0, int rows) {
       const uint32_t full = full0 + 8 * stage;
+      if (lane == 0)
+        mbar_arrive_expect_tx(full, p.v_stage_bytes + (p.attn_tma ? p.a_stage_bytes : 0u));
+      load_v(vring_s + (uint32_t)stage * p.v_stage_bytes, c0, full);
       if (p.attn_tma) {
-        if (lane == 0) {
-          mbar_arrive_expect_tx(full, p.v_stage_bytes + p.a_stage_bytes);
-          load_v(vring_s + (uint32_t)stage * p.v_stage_bytes, c0, full);
+        if (lane == 0)
           tma_load_3d(aring_s + (uint32_t)stage * p.a_stage_bytes, &p.a_map, h0 - a_shift, c0, b,
                       full, policy);
-        }
         return;
-      }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(full, p.v_stage_bytes);
-        load_v(vring_s + (uint32_t)stage * p.v_stage_bytes, c0, full);
       }
       const float* src = attn_b + (size_t)c0 * p.Hq;
       const uint32_t dst = aring_s + 4u * (uint32_t)(stage * p.R * p.ap);

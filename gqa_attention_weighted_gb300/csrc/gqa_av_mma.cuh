@@ -346,20 +346,30 @@ __global__ void __launch_bounds__(kMmaMaxThreads, NB == 1 ? 3 : (NB == 2 ? 2 : 1
     auto issue = [&](int stage, int b, int c0, int rows) {
       const uint32_t full = full0 + 8 * stage;
       const uint32_t vdst = vring_s + (uint32_t)stage * p.v_stage_bytes;
+      if (p.block_table) {
+        // Paged: the stage's block indices loaded by the lanes together (lane
+        // j for box j), then lane 0 issues one box a block and V half.
+        const int nbox = p.R / p.chunk_rows;  // <= 32
+        const int2 mine = lane < nbox ? v_row_coord(p, b, c0 + lane * p.chunk_rows) : make_int2(0, 0);
+        if (lane == 0)
+          mbar_arrive_expect_tx(full, (uint32_t)p.v_halves * (p.v_stage_bytes / 2) +
+                                          (p.attn_tma ? p.a_stage_bytes : 0u));
+        for (int j = 0; j < nbox; ++j) {
+          const int rx = __shfl_sync(0xffffffffu, mine.x, j);
+          const int ry = __shfl_sync(0xffffffffu, mine.y, j);
+          if (lane == 0)
+            for (int h = 0; h < p.v_halves; ++h)
+              tma_load_4d(vdst + (uint32_t)h * p.v_stage_bytes / 2 + (uint32_t)(j * p.chunk_rows) * 128,
+                          &p.v_map, d0 + 64 * h, kv_h, rx, ry, full, policy);
+        }
+      }
       if (lane == 0) {
-        mbar_arrive_expect_tx(full, (uint32_t)p.v_halves * (p.v_stage_bytes / 2) +
-                                        (p.attn_tma ? p.a_stage_bytes : 0u));
         if (!p.block_table) {
+          mbar_arrive_expect_tx(full, (uint32_t)p.v_halves * (p.v_stage_bytes / 2) +
+                                          (p.attn_tma ? p.a_stage_bytes : 0u));
           for (int h = 0; h < p.v_halves; ++h)
             tma_load_4d(vdst + (uint32_t)h * p.v_stage_bytes / 2, &p.v_map, d0 + 64 * h, kv_h, c0,
                         b, full, policy);
-        } else {
-          for (int h = 0; h < p.v_halves; ++h)
-            for (int r0 = 0; r0 < p.R; r0 += p.chunk_rows) {  // one box a paged block
-              const int2 rc = v_row_coord(p, b, c0 + r0);
-              tma_load_4d(vdst + (uint32_t)h * p.v_stage_bytes / 2 + (uint32_t)r0 * 128, &p.v_map,
-                          d0 + 64 * h, kv_h, rc.x, rc.y, full, policy);
-            }
         }
         if (p.attn_tma)
           tma_load_3d(aring_s + (uint32_t)stage * p.a_stage_bytes, &p.a_map, h0 - a_shift, c0, b,
