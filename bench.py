@@ -44,6 +44,11 @@ QK_SOURCES = ["gqa_attention_weighted_gb300/csrc/gqa_qk_kernel.cuh",
               "gqa_attention_weighted_gb300/csrc/gqa_qk_mma.cuh",
               "gqa_attention_weighted_gb300/csrc/gqa_qk_api.cu",
               "gqa_attention_weighted_gb300/csrc/gqa_av_kernel.cuh"]
+METRIC_ATTN = ("GQA fused decode attention achieved HBM GB/s over compulsory bytes (K and V "
+               "read once), µs/call")
+ATTN_SOURCES = ["gqa_attention_weighted_gb300/csrc/gqa_attn_kernel.cuh",
+                "gqa_attention_weighted_gb300/csrc/gqa_attn_api.cu",
+                "gqa_attention_weighted_gb300/csrc/gqa_av_kernel.cuh"]
 DEFAULT_WORKLOAD = "llama"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["gqa_attention_weighted_gb300/csrc/gqa_av_kernel.cuh",
@@ -457,6 +462,187 @@ def run_gpu_qk(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+def run_gpu_attn(args, rank, world, local):
+    """Fused decode attention (include/gqa_attn.h) on the workload's shape: V and
+    seq_lens as for the AV call, K drawn the same way, q ~ N(0, logit_sigma^2)."""
+    import gqa_attention_weighted_gb300 as gq
+
+    w = W.get(args.workload)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    mode = {"auto": gq.MODE_AUTO, "gqa": gq.MODE_GQA, "per_head": gq.MODE_PER_HEAD}[args.mode]
+    x = W.generate_qkv(w, dev, pad="zero")
+    lens = x["seq_lens"].cpu().tolist()
+    cbytes = W.attention_compulsory_bytes(w, lens)
+    flops = W.attention_flops(w, lens)
+    scale = w.D ** -0.5
+    plan = gq.gqa_attn_plan(w.B, w.Cmax, w.Hq, w.Hkv, w.D, gq.native.v_dtype_code(x["k"].dtype),
+                            mode, args.attn_warps, args.attn_splits)
+
+    def call(st, out):
+        gq.gqa_attn_decode(st["q"], st["k"], st["v"], st["seq_lens"], out, mode=mode, scale=scale,
+                           consumer_warps=args.attn_warps, nsplit=args.attn_splits)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    set_bytes = sum(t.numel() * t.element_size() for t in x.values()) + w.B * w.Hq * w.D * 4
+    n_sets = max(1, math.ceil(3 * l2 / set_bytes)) if set_bytes < 3 * l2 else 1
+    sets = [x] + [{k: t.clone() for k, t in x.items()} for _ in range(n_sets - 1)]
+    outs = [torch.zeros((w.B, w.Hq, w.D), dtype=torch.float32, device=dev)
+            for _ in range(n_sets)]
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            call(sets[i % n_sets], outs[i % n_sets])
+        gq.gqa_attn_device_status(stream)
+        chunk = min(args.steps, args.graph_len)
+        reps, rem = divmod(args.steps, chunk)
+
+        def capture(n):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                for i in range(n):
+                    call(sets[i % n_sets], outs[i % n_sets])
+            return gr
+
+        g_main = capture(chunk)
+        g_rem = capture(rem) if rem else None
+        g_main.replay()
+        stream.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        with ClockSampler(local) as clk:
+            start.record(stream)
+            for _ in range(reps):
+                g_main.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            end.record(stream)
+            end.synchronize()
+        torch.cuda.synchronize()
+        barrier(world)
+        elapsed_ms = start.elapsed_time(end)
+        gq.gqa_attn_device_status(stream)
+    elapsed_ms = max_over_ranks(elapsed_ms, world)
+    ms_per_step = elapsed_ms / args.steps
+    value = cbytes * args.steps * world / (elapsed_ms * 1e-3) / 1e9
+    achieved = cbytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+
+    # End to end: pinned H2D of q, K, V and seq_lens, the call, D2H of out.
+    host = {k: t.cpu().pin_memory() for k, t in x.items()}
+    dbuf = {k: torch.empty_like(t) for k, t in x.items()}
+    out_d = torch.zeros((w.B, w.Hq, w.D), dtype=torch.float32, device=dev)
+    out_h = torch.empty_like(out_d, device="cpu").pin_memory()
+    e_steps = max(1, min(args.e2e_steps, args.steps))
+    with torch.cuda.stream(stream):
+        def step():
+            for k in host:
+                dbuf[k].copy_(host[k], non_blocking=True)
+            call(dbuf, out_d)
+            out_h.copy_(out_d, non_blocking=True)
+        for _ in range(3):
+            step()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        e0.record(stream)
+        for _ in range(e_steps):
+            step()
+        e1.record(stream)
+        e1.synchronize()
+        barrier(world)
+    e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e_steps
+    e2e = {"value": round(cbytes * world / (e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+           "ms_per_step": e_ms, "steps": e_steps,
+           "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host.values()),
+           "d2h_bytes_per_step": out_h.numel() * 4}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_baseline_attn(w, x, scale, args.cpu_seconds)
+    launches = 1 if plan["nsplit"] == 1 else 2
+    line = {
+        "metric": METRIC_ATTN, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "us_per_call": ms_per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {**w.describe(), "op": "attn", "mode": args.mode, "plan": plan,
+                   "scale": scale, "q": f"N(0, {w.logit_sigma}^2)",
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "compulsory_bytes_per_call": cbytes, "flops_per_call": flops,
+                   "l2": f"rotating {n_sets} input sets, {n_sets * set_bytes / 1e6:.0f} MB "
+                         f"(L2 {l2 / 1e6:.0f} MB)",
+                   "timing": f"CUDA graphs of {chunk} calls x {reps}"
+                             + (f" + {rem}" if rem else "") + ", events on the launch stream"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_kind": f"{peak_kind} hbm_gbs (copy)",
+                     "traffic": committed_traffic_attn(w.name, plan["mode"]),
+                     "kernel": "gqa_attn_kernel",
+                     "kernel_hash": kernel_hash(ATTN_SOURCES),
+                     "duration": "average time of one whole call (attention kernel and, with "
+                                 "several splits, the combine kernel) over the timed region"},
+        "e2e": e2e,
+        "gpu_launches": args.steps * launches,
+        "clocks": clk.summary(),
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def committed_traffic_attn(workload: str, mode: int):
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            entries = json.load(f)
+    except (OSError, ValueError):
+        return None
+    for e in entries:
+        if (e.get("op") == "attn" and e.get("kernel_hash") == kernel_hash(ATTN_SOURCES)
+                and e.get("workload") == workload and e.get("mode") == mode):
+            return e.get("traffic_bytes_per_launch")
+    return None
+
+
+def oracle_baseline_attn(w, x, scale, seconds):
+    """The fused-attention oracle, as it stands (numpy fp64), on a context prefix."""
+    import numpy as np
+    from oracle import gqa_attn
+    rows = w.Cmax
+    q = x["q"].cpu().numpy()
+
+    def inputs(n):
+        kb = x["k"][:, :n].contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+        vb = x["v"][:, :n].contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+        return kb, vb, x["seq_lens"].cpu().clamp(max=n).numpy().astype(np.int32)
+
+    kb, vb, lens = inputs(rows)
+    t0 = time.perf_counter()
+    gqa_attn.gqa_attention(q, kb, vb, w.v_dtype, lens, scale)
+    t1 = time.perf_counter() - t0
+    if t1 > seconds:
+        rows = max(1, int(rows * seconds / t1 / 2))
+        kb, vb, lens = inputs(rows)
+    sample_bytes = W.attention_compulsory_bytes(w, lens.tolist())
+    n, t_total = 0, 0.0
+    while t_total < seconds or n < 1:
+        t0 = time.perf_counter()
+        gqa_attn.gqa_attention(q, kb, vb, w.v_dtype, lens, scale)
+        t_total += time.perf_counter() - t0
+        n += 1
+    import oracle
+    return {"value": round(sample_bytes * n / t_total / 1e9, 4), "unit": UNIT,
+            "cores": oracle.host_cores(), "kind": "oracle",
+            "sample": f"{n} passes over context positions [0, {rows}) of {w.name} "
+                      f"({sample_bytes} compulsory bytes per pass), numpy fp64 (its BLAS "
+                      f"threads over the affinity mask), {t_total:.1f} s"}
+
+
 def committed_traffic_qk(workload: str, mode: int, engine: int):
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
@@ -635,9 +821,13 @@ def main():
     ap.add_argument("--split-mode", choices=list(SPLIT_MODES), default="auto",
                     help="context splits: the library's choice, fixed splits of each "
                          "sequence, or splits balanced over the batch's lengths")
-    ap.add_argument("--op", choices=["av", "qk"], default="av",
+    ap.add_argument("--op", choices=["av", "qk", "attn"], default="av",
                     help="av: the AV reduction (the benchmark); qk: the decode score step "
-                         "before it")
+                         "before it; attn: both fused in one pass over K and V")
+    ap.add_argument("--attn-warps", type=int, default=0,
+                    help="attn: consumer warps per CTA (0: the library's choice)")
+    ap.add_argument("--attn-splits", type=int, default=0,
+                    help="attn: context splits per tile (0: the library's choice)")
     ap.add_argument("--paged", type=int, default=0, metavar="BLOCK_SIZE",
                     help="run the AV call on a paged copy of V (blocks of this many rows in a "
                          "shuffled pool, gqa_av_decode_paged)")
@@ -656,7 +846,8 @@ def main():
         else:
             if not torch.cuda.is_available():
                 raise SystemExit("bench.py: the GB300 arm needs a CUDA GPU")
-            (run_gpu_qk if args.op == "qk" else run_gpu)(args, rank, world, local)
+            {"qk": run_gpu_qk, "attn": run_gpu_attn}.get(args.op, run_gpu)(args, rank, world,
+                                                                            local)
     finally:
         if world > 1:
             import torch.distributed as dist

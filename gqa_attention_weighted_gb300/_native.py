@@ -83,6 +83,14 @@ def _load() -> ctypes.CDLL:
     lib.gqa_qk_device_status.argtypes = [P, I]
     lib.gqa_qk_last_error.argtypes = []
     lib.gqa_qk_last_error.restype = ctypes.c_char_p
+    lib.gqa_attn_decode.argtypes = [P, P, P, P, P, *sizes, I, ctypes.c_float, I, P]
+    lib.gqa_attn_decode_tuned.argtypes = [P, P, P, P, P, *sizes, I, ctypes.c_float, I, I, I, P]
+    lib.gqa_attn_plan.argtypes = [*sizes, I, I, I, I, ctypes.POINTER(ctypes.c_int), I]
+    lib.gqa_attn_device_status.argtypes = [P, I]
+    lib.gqa_attn_last_error.argtypes = []
+    lib.gqa_attn_last_error.restype = ctypes.c_char_p
+    for f in ("gqa_attn_decode", "gqa_attn_decode_tuned", "gqa_attn_plan", "gqa_attn_device_status"):
+        getattr(lib, f).restype = I
     for f in ("gqa_av_decode", "gqa_av_decode_per_head", "gqa_av_decode_tuned", "gqa_av_decode_paged",
               "gqa_av_decode_noalloc", "gqa_av_plan",
               "gqa_av_set_workspace", "gqa_av_device_status", "gqa_av_version",
@@ -286,3 +294,54 @@ def gqa_qk_softmax_decode(q, k_cache, seq_lens, attn, mode: int = MODE_AUTO, sca
 
 def gqa_qk_device_status(stream=None, clear: bool = True) -> None:
     _check_qk(lib.gqa_qk_device_status(_stream_handle(stream), 1 if clear else 0))
+
+
+# ------------------------------------------------------- fused attention
+def _check_attn(status: int) -> None:
+    if status != GQA_AV_OK:
+        name = lib.gqa_av_status_string(status).decode()
+        raise GqaAvError(status, f"{name}: {lib.gqa_attn_last_error().decode()}")
+
+
+def gqa_attn_decode(q, k_cache, v_cache, seq_lens, out, mode: int = MODE_AUTO, scale=None,
+                    stream=None, consumer_warps: int = 0, nsplit: int = 0) -> torch.Tensor:
+    """out[b,q,:] = sum over c < L_b of softmax_c(scale * q[b,q,:] . k_cache[b,c,q//G,:])
+    * v_cache[b,c,q//G,:] (scale defaults to 1/sqrt(D)); writes and returns ``out``."""
+    if q.dim() != 3 or k_cache.dim() != 4 or v_cache.dim() != 4 or out.dim() != 3:
+        raise ValueError("q [B,Hq,D], k_cache and v_cache [B,Cmax,Hkv,D], out [B,Hq,D]")
+    B, Hq, D = q.shape
+    B2, Cmax, Hkv, D2 = k_cache.shape
+    if ((B2, D2) != (B, D) or tuple(v_cache.shape) != tuple(k_cache.shape)
+            or tuple(out.shape) != (B, Hq, D)):
+        raise ValueError(f"inconsistent shapes: q {tuple(q.shape)}, k {tuple(k_cache.shape)}, "
+                         f"v {tuple(v_cache.shape)}, out {tuple(out.shape)}")
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("out", out)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if q.dtype != torch.float32 or out.dtype != torch.float32:
+        raise ValueError("q and out must be float32")
+    if k_cache.dtype not in _V_DTYPE or v_cache.dtype != k_cache.dtype:
+        raise ValueError("k_cache and v_cache must both be bfloat16 or both float16")
+    if seq_lens is not None and (not seq_lens.is_cuda or seq_lens.dtype != torch.int32
+                                 or seq_lens.numel() != B or not seq_lens.is_contiguous()):
+        raise ValueError("seq_lens must be a contiguous CUDA int32 tensor of B elements")
+    sc = float(D) ** -0.5 if scale is None else float(scale)
+    _check_attn(lib.gqa_attn_decode_tuned(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
+                                          _ptr(out), B, Cmax, Hq, Hkv, D, _V_DTYPE[k_cache.dtype],
+                                          sc, int(mode), int(consumer_warps), int(nsplit),
+                                          _stream_handle(stream)))
+    return out
+
+
+def gqa_attn_plan(B, Cmax, Hq, Hkv, D, kv_dtype=GQA_AV_BF16, mode=MODE_AUTO, consumer_warps=0,
+                  nsplit=0) -> dict:
+    info = (ctypes.c_int * 8)()
+    _check_attn(lib.gqa_attn_plan(B, Cmax, Hq, Hkv, D, kv_dtype, mode, consumer_warps, nsplit,
+                                  info, 8))
+    keys = ("mode", "heads_per_cta", "consumer_warps", "stages", "rows_per_split", "nsplit",
+            "tiles", "smem_bytes")
+    return dict(zip(keys, list(info)))
+
+
+def gqa_attn_device_status(stream=None, clear: bool = True) -> None:
+    _check_attn(lib.gqa_attn_device_status(_stream_handle(stream), 1 if clear else 0))

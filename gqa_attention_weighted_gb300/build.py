@@ -18,7 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIBRARY = os.path.join(PKG, "libgqa_av.so")
 
-SOURCES = ["gqa_av_api.cu", "gqa_av_bf16.cu", "gqa_av_fp16.cu", "gqa_av_noalloc.cu", "gqa_qk_api.cu"]
+SOURCES = ["gqa_av_api.cu", "gqa_av_bf16.cu", "gqa_av_fp16.cu", "gqa_av_noalloc.cu", "gqa_qk_api.cu",
+           "gqa_attn_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                      "-diag-suppress", "1160", "-I", INCLUDE, "-I", CSRC]
@@ -32,7 +33,7 @@ def nvcc() -> str:
 
 def _inputs():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(INCLUDE, "gqa_av.h"))
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
     return files
 
 

@@ -157,6 +157,51 @@ def generate(w: Workload, device="cpu", pad: str = "zero",
     return {"attn": attn, "v": v, "seq_lens": seq_lens}
 
 
+def generate_qkv(w: Workload, device="cpu", pad: str = "zero",
+                 seed: Optional[int] = None) -> Dict[str, torch.Tensor]:
+    """Inputs of the fused decode attention for workload ``w``: (q, k, v, seq_lens).
+
+    ``seq_lens`` and ``v`` are those of ``generate`` with the same seed. A second
+    generator seeded with seed + 1 then draws, for b = 0..B-1, ``K[b]`` ~
+    N(0, v_sigma^2) in fp32 rounded to the cache type, and after that
+    ``q`` [B, Hq, D] ~ N(0, logit_sigma^2) in fp32, so that the scores
+    q . K / sqrt(D) spread like the workload's logits. K rows c >= L_b are
+    padding like V's.
+    """
+    x = generate(w, device, pad, seed)
+    del x["attn"]
+    device = torch.device(device)
+    g = torch.Generator(device=device)
+    g.manual_seed((w.seed if seed is None else seed) + 1)
+    B, C, Hkv, D = w.B, w.Cmax, w.Hkv, w.D
+    lens = x["seq_lens"].cpu().tolist()
+    padv = 0.0 if pad == "zero" else float("nan")
+    k = torch.empty((B, C, Hkv, D), dtype=V_DTYPES[w.v_dtype], device=device)
+    for b in range(B):
+        kb = torch.randn((C, Hkv, D), generator=g, device=device, dtype=torch.float32)
+        kb.mul_(w.v_sigma)
+        k[b].copy_(kb.to(k.dtype))
+        if lens[b] < C:
+            k[b, lens[b]:].fill_(padv)
+        del kb
+    q = torch.randn((B, w.Hq, D), generator=g, device=device, dtype=torch.float32)
+    q.mul_(w.logit_sigma)
+    return {"q": q, "k": k, "v": x["v"], "seq_lens": x["seq_lens"]}
+
+
+def attention_compulsory_bytes(w: Workload, seq_lens) -> int:
+    """Bytes the fused decode attention must move at least once: every in-range
+    K row and V row once, q once, out once, and seq_lens."""
+    total_L = int(sum(int(x) for x in seq_lens))
+    return total_L * w.Hkv * w.D * 2 * 2 + 2 * w.B * w.Hq * w.D * 4 + 4 * w.B
+
+
+def attention_flops(w: Workload, seq_lens) -> int:
+    """Multiply-adds x 2 of the two products (scores and the weighted sum)."""
+    total_L = int(sum(int(x) for x in seq_lens))
+    return 4 * total_L * w.Hq * w.D
+
+
 def compulsory_bytes(w: Workload, seq_lens) -> int:
     """Bytes the reduction must move at least once: every in-range V row once,
     every in-range attn weight once, out once, and seq_lens."""

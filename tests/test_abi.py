@@ -7,14 +7,14 @@ import re
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADERS = [os.path.join(ROOT, "include", h) for h in ("gqa_av.h", "gqa_qk.h")]
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("gqa_av.h", "gqa_qk.h", "gqa_attn.h")]
 
 
 def declared_functions():
     names = set()
     for h in HEADERS:
         text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
-        names |= set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(gqa_(?:av|qk)_\w+)\s*\(", text, re.M))
+        names |= set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(gqa_(?:av|qk|attn)_\w+)\s*\(", text, re.M))
     return sorted(names)
 
 
@@ -29,7 +29,9 @@ def native():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for f in ("gqa_av_decode", "gqa_av_decode_per_head", "gqa_av_status_string",
-              "gqa_av_workspace_bytes", "gqa_qk_softmax_decode", "gqa_qk_device_status"):
+              "gqa_av_workspace_bytes", "gqa_qk_softmax_decode", "gqa_qk_device_status",
+              "gqa_attn_decode", "gqa_attn_decode_tuned", "gqa_attn_plan",
+              "gqa_attn_device_status", "gqa_attn_last_error"):
         assert f in names
 
 
@@ -92,3 +94,30 @@ def test_score_step_host_checks_reject_before_launch(native, args, status):
     rc = native.lib.gqa_qk_softmax_decode(*args, None)
     assert rc == status, native.lib.gqa_qk_last_error()
     assert native.lib.gqa_qk_last_error() != b""
+
+
+# (q, k, v, seq_lens, out, B, Cmax, Hq, Hkv, D, kv_dtype, scale, mode)
+@pytest.mark.parametrize("args,status", [
+    ((FAKE, FAKE, FAKE, None, FAKE, 1, 8, 6, 4, 64, 0, 1.0, -1), 1),    # Hq % Hkv != 0
+    ((FAKE, FAKE, FAKE, None, FAKE, 0, 8, 4, 4, 64, 0, 1.0, -1), 1),    # B == 0
+    ((FAKE, FAKE, FAKE, None, FAKE, 1, 0, 4, 4, 64, 0, 1.0, -1), 1),    # Cmax == 0
+    ((FAKE, FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 64, 2, 1.0, -1), 1),    # unknown dtype
+    ((FAKE, FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 64, 0, 1.0, 3), 1),     # unknown mode
+    ((None, FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 64, 0, 1.0, -1), 1),    # NULL q
+    ((FAKE, FAKE, None, None, FAKE, 1, 8, 4, 4, 64, 0, 1.0, -1), 1),    # NULL v
+    ((FAKE, FAKE, FAKE, None, None, 1, 8, 4, 4, 64, 0, 1.0, 1), 1),     # NULL out
+    ((FAKE, FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 64, 0, float("inf"), 1), 1),  # scale not finite
+    ((FAKE, FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 96, 0, 1.0, 1), 2),     # D % 64 != 0
+    ((FAKE, FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 512, 0, 1.0, 1), 2),    # D > 256
+    ((FAKE, FAKE + 8, FAKE, None, FAKE, 1, 8, 4, 4, 64, 0, 1.0, 0), 2),  # misaligned k
+])
+def test_attention_host_checks_reject_before_launch(native, args, status):
+    rc = native.lib.gqa_attn_decode(*args, None)
+    assert rc == status, native.lib.gqa_attn_last_error()
+    assert native.lib.gqa_attn_last_error() != b""
+
+
+def test_attention_tuning_range_checked(native):
+    rc = native.lib.gqa_attn_decode_tuned(FAKE, FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 64, 0, 1.0,
+                                          -1, 9, 0, None)
+    assert rc == 1 and b"consumer_warps" in native.lib.gqa_attn_last_error()
