@@ -475,12 +475,14 @@ def run_gpu_attn(args, rank, world, local):
     cbytes = W.attention_compulsory_bytes(w, lens)
     flops = W.attention_flops(w, lens)
     scale = w.D ** -0.5
+    smode = SPLIT_MODES[args.split_mode]
     plan = gq.gqa_attn_plan(w.B, w.Cmax, w.Hq, w.Hkv, w.D, gq.native.v_dtype_code(x["k"].dtype),
-                            mode, args.attn_warps, args.attn_splits)
+                            mode, args.attn_warps, args.attn_splits, smode, True)
 
     def call(st, out):
         gq.gqa_attn_decode(st["q"], st["k"], st["v"], st["seq_lens"], out, mode=mode, scale=scale,
-                           consumer_warps=args.attn_warps, nsplit=args.attn_splits)
+                           consumer_warps=args.attn_warps, nsplit=args.attn_splits,
+                           split_mode=smode)
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     set_bytes = sum(t.numel() * t.element_size() for t in x.values()) + w.B * w.Hq * w.D * 4
@@ -563,7 +565,7 @@ def run_gpu_attn(args, rank, world, local):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_baseline_attn(w, x, scale, args.cpu_seconds)
-    launches = 1 if plan["nsplit"] == 1 else 2
+    launches = 1 if (plan["nsplit"] == 1 and plan["split_mode"] == 1) else 2
     line = {
         "metric": METRIC_ATTN, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,

@@ -22,7 +22,6 @@ namespace {
 constexpr size_t kAttnHeaderBytes = 256;             // device status word + padding
 constexpr long long kAttnTimeoutNs = 2000000000LL;   // 2 s bound on every mbarrier wait
 constexpr int kAttnMaxSplitRows = 8192;              // longest split of one CTA
-constexpr int kAttnCombineSmem = 48 * 1024;          // combine weights: heads x nsplit floats
 
 thread_local std::string g_at_error;
 std::mutex g_at_mu;
@@ -55,6 +54,7 @@ AttnKernel pick(int D) {
 
 struct AttnPlan {
   int mode, heads, hgroups, nw, stages, rows_per_split, nsplit, tiles;
+  int balanced, units, ctas, combine;
   int smem, q_off, qstride, bar_off, stage_bytes, merge_bytes;
   size_t ws_bytes;  // split partials only
 };
@@ -73,7 +73,7 @@ int check_args(int B, int Cmax, int Hq, int Hkv, int D, int kv_dtype, int mode) 
 }
 
 int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int kv_dtype, int mode, int want_nw,
-         int want_nsplit, AttnPlan* p) {
+         int want_nsplit, int split_mode, bool ragged, AttnPlan* p) {
   int rc = check_args(B, Cmax, Hq, Hkv, D, kv_dtype, mode);
   if (rc) return rc;
   const int G = Hq / Hkv;
@@ -90,13 +90,16 @@ int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int kv_dtype, int mod
   p->tiles = p->hgroups * B;
 
   // Consumer warps and ring: 32-row stages of K and V (128 * D bytes); the
-  // ring holds a whole number of stages per warp, about 128 KiB for D <= 128
-  // and 192 KiB for D = 256 (six warps of one 32 KiB stage each).
+  // ring holds a whole number of stages per warp, at most 192 KiB. Measured
+  // on GB300: 8 warps of 3 stages at D = 64, 6 warps of 2 at D = 128 and
+  // 3 warps of 2 at D = 256 (a warp overlaps its next stage's load with the
+  // current stage's products).
   p->stage_bytes = kAttnRows * D * 2 * 2;
-  p->nw = want_nw > 0 ? want_nw : (D == 256 ? 6 : 8);
-  if (p->nw < 1 || p->nw > kAttnMaxWarps)
-    return afail(GQA_AV_ERR_INVALID, "consumer warps %d outside 1..%d", p->nw, kAttnMaxWarps);
-  const int ring_budget = D == 256 ? 196608 : 131072;
+  p->nw = want_nw > 0 ? want_nw : (D == 256 ? 3 : D == 128 ? 6 : 8);
+  if (p->nw < 1 || p->nw > attn_max_warps(D))
+    return afail(GQA_AV_ERR_UNSUPPORTED, "consumer warps %d outside 1..%d for D=%d", p->nw,
+                 attn_max_warps(D), D);
+  const int ring_budget = 196608;
   const int per_warp = std::max(1, ring_budget / (p->stage_bytes * p->nw));
   p->stages = per_warp * p->nw;
   p->qstride = D * 2 + 16;
@@ -128,12 +131,17 @@ int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int kv_dtype, int mod
   p->nsplit = (Cmax + p->rows_per_split - 1) / p->rows_per_split;
   if (static_cast<long long>(p->tiles) * p->nsplit > 0x7fffffffLL)
     return afail(GQA_AV_ERR_UNSUPPORTED, "grid too large");
-  if (p->heads * p->nsplit * 4 > kAttnCombineSmem)
-    return afail(GQA_AV_ERR_UNSUPPORTED, "%d splits of %d heads: too many for the combine",
-                 p->nsplit, p->heads);
-  p->ws_bytes = p->nsplit > 1 ? static_cast<size_t>(p->tiles) * p->nsplit * p->heads *
-                                    (static_cast<size_t>(D) * 4 + 8)
-                              : 0;
+  // Balanced splits spread the batch's context rows evenly over the same
+  // number of CTAs, whatever the lengths: at most units + tiles CTAs have work.
+  p->balanced = split_mode == 2 || (split_mode == 0 && ragged && B > 1);
+  p->units = p->tiles * p->nsplit;
+  p->ctas = p->balanced ? p->units + p->tiles : p->units;
+  p->combine = p->balanced || p->nsplit > 1;
+  if (static_cast<long long>(p->units) + p->tiles > 0x7fffffffLL)
+    return afail(GQA_AV_ERR_UNSUPPORTED, "grid too large");
+  p->ws_bytes = p->combine ? static_cast<size_t>(p->ctas) * p->heads *
+                                 (static_cast<size_t>(D) * 4 + 8)
+                           : 0;
   return GQA_AV_OK;
 }
 
@@ -237,7 +245,8 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaS
 using namespace gqa_av;
 
 extern "C" int gqa_attn_plan(int B, int Cmax, int Hq, int Hkv, int D, int kv_dtype, int mode,
-                             int consumer_warps, int nsplit, int* info, int n_info) {
+                             int consumer_warps, int nsplit, int split_mode, int ragged, int* info,
+                             int n_info) {
   g_at_error.clear();
   int rc = check_args(B, Cmax, Hq, Hkv, D, kv_dtype, mode);
   if (rc) return rc;
@@ -245,10 +254,13 @@ extern "C" int gqa_attn_plan(int B, int Cmax, int Hq, int Hkv, int D, int kv_dty
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return afail_cuda(e, "cudaGetDevice");
   AttnPlan pl;
-  rc = plan(dev, B, Cmax, Hq, Hkv, D, kv_dtype, mode, consumer_warps, nsplit, &pl);
+  if (split_mode < 0 || split_mode > 2)
+    return afail(GQA_AV_ERR_INVALID, "split_mode=%d must be 0, 1 or 2", split_mode);
+  rc = plan(dev, B, Cmax, Hq, Hkv, D, kv_dtype, mode, consumer_warps, nsplit, split_mode,
+            ragged != 0, &pl);
   if (rc) return rc;
   const int vals[] = {pl.mode, pl.heads, pl.nw, pl.stages, pl.rows_per_split, pl.nsplit,
-                      pl.tiles, pl.smem};
+                      pl.tiles, pl.smem, pl.balanced ? 2 : 1, pl.ctas};
   if (info)
     for (int i = 0; i < n_info && i < static_cast<int>(sizeof vals / sizeof vals[0]); ++i)
       info[i] = vals[i];
@@ -258,7 +270,8 @@ extern "C" int gqa_attn_plan(int B, int Cmax, int Hq, int Hkv, int D, int kv_dty
 extern "C" int gqa_attn_decode_tuned(const float* q, const void* k_cache, const void* v_cache,
                                      const int32_t* seq_lens, float* out, int B, int Cmax, int Hq,
                                      int Hkv, int D, int kv_dtype, float scale, int mode,
-                                     int consumer_warps, int nsplit, void* stream_) {
+                                     int consumer_warps, int nsplit, int split_mode,
+                                     void* stream_) {
   g_at_error.clear();
   if (!q || !k_cache || !v_cache || !out)
     return afail(GQA_AV_ERR_INVALID, "q, k_cache, v_cache and out must be non-NULL");
@@ -268,14 +281,18 @@ extern "C" int gqa_attn_decode_tuned(const float* q, const void* k_cache, const 
   if (!std::isfinite(scale)) return afail(GQA_AV_ERR_INVALID, "scale must be finite");
   int rc = check_args(B, Cmax, Hq, Hkv, D, kv_dtype, mode);
   if (rc) return rc;
-  if (consumer_warps < 0 || consumer_warps > kAttnMaxWarps || nsplit < 0)
-    return afail(GQA_AV_ERR_INVALID, "consumer_warps=%d (0..%d) or nsplit=%d (>= 0) out of range",
-                 consumer_warps, kAttnMaxWarps, nsplit);
+  if (consumer_warps < 0 || consumer_warps > kAttnMaxWarps || nsplit < 0 || split_mode < 0 ||
+      split_mode > 2)
+    return afail(GQA_AV_ERR_INVALID,
+                 "consumer_warps=%d (0..%d), nsplit=%d (>= 0) or split_mode=%d (0..2) out of range",
+                 consumer_warps, kAttnMaxWarps, nsplit, split_mode);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return afail_cuda(e, "cudaGetDevice");
   AttnPlan pl;
-  if ((rc = plan(dev, B, Cmax, Hq, Hkv, D, kv_dtype, mode, consumer_warps, nsplit, &pl))) return rc;
+  if ((rc = plan(dev, B, Cmax, Hq, Hkv, D, kv_dtype, mode, consumer_warps, nsplit, split_mode,
+                 seq_lens != nullptr, &pl)))
+    return rc;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   Ws ws;
   if ((rc = workspace(dev, kAttnHeaderBytes + pl.ws_bytes, stream, &ws))) return rc;
@@ -289,12 +306,12 @@ extern "C" int gqa_attn_decode_tuned(const float* q, const void* k_cache, const 
   p.status = static_cast<unsigned int*>(ws.base);
   char* parts = static_cast<char*>(ws.base) + kAttnHeaderBytes;
   p.ws_o = reinterpret_cast<float*>(parts);
-  p.ws_ml = reinterpret_cast<float2*>(parts + static_cast<size_t>(pl.tiles) * pl.nsplit *
-                                                  pl.heads * D * 4);
+  p.ws_ml = reinterpret_cast<float2*>(parts + static_cast<size_t>(pl.ctas) * pl.heads * D * 4);
   p.qscale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);  // log2(e)
   p.B = B; p.Cmax = Cmax; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.G = Hq / Hkv;
   p.heads = pl.heads; p.hgroups = pl.hgroups; p.nw = pl.nw; p.stages = pl.stages;
   p.rows_per_split = pl.rows_per_split; p.nsplit = pl.nsplit;
+  p.balanced = pl.balanced; p.units = pl.units;
   p.stage_bytes = static_cast<uint32_t>(pl.stage_bytes);
   p.q_off = static_cast<uint32_t>(pl.q_off);
   p.qstride = static_cast<uint32_t>(pl.qstride);
@@ -306,10 +323,10 @@ extern "C" int gqa_attn_decode_tuned(const float* q, const void* k_cache, const 
   e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
   if (e != cudaSuccess) return afail_cuda(e, "cudaFuncSetAttribute");
   void* args1[] = {&p};
-  e = launch_pdl(reinterpret_cast<const void*>(k), dim3(pl.tiles * pl.nsplit),
+  e = launch_pdl(reinterpret_cast<const void*>(k), dim3(pl.ctas),
                  dim3(32 * (pl.nw + 1)), pl.smem, stream, args1);
   if (e != cudaSuccess) return afail_cuda(e, "attention kernel launch");
-  if (pl.nsplit == 1) return GQA_AV_OK;  // every tile wrote `out` itself
+  if (!pl.combine) return GQA_AV_OK;  // every tile wrote `out` itself
 
   AttnCombineParams c;
   c.ws_o = p.ws_o;
@@ -318,10 +335,10 @@ extern "C" int gqa_attn_decode_tuned(const float* q, const void* k_cache, const 
   c.out = out;
   c.B = B; c.Cmax = Cmax; c.Hq = Hq; c.D = D; c.heads = pl.heads; c.hgroups = pl.hgroups;
   c.rows_per_split = pl.rows_per_split; c.nsplit = pl.nsplit;
+  c.balanced = pl.balanced; c.units = pl.units;
   void* args2[] = {&c};
-  e = launch_pdl(reinterpret_cast<const void*>(gqa_attn_combine_kernel), dim3(pl.tiles),
-                 dim3(kAttnCombineThreads), static_cast<size_t>(pl.heads) * pl.nsplit * 4, stream,
-                 args2);
+  e = launch_pdl(reinterpret_cast<const void*>(gqa_attn_combine_kernel), dim3(pl.tiles * pl.heads),
+                 dim3(kAttnCombineThreads), 0, stream, args2);
   if (e != cudaSuccess) return afail_cuda(e, "combine kernel launch");
   return GQA_AV_OK;
 }
@@ -330,7 +347,7 @@ extern "C" int gqa_attn_decode(const float* q, const void* k_cache, const void* 
                                const int32_t* seq_lens, float* out, int B, int Cmax, int Hq,
                                int Hkv, int D, int kv_dtype, float scale, int mode, void* stream) {
   return gqa_attn_decode_tuned(q, k_cache, v_cache, seq_lens, out, B, Cmax, Hq, Hkv, D, kv_dtype,
-                               scale, mode, 0, 0, stream);
+                               scale, mode, 0, 0, 0, stream);
 }
 
 extern "C" int gqa_attn_device_status(void* stream_, int clear) {

@@ -42,8 +42,12 @@ namespace gqa_av {
 
 constexpr int kAttnRows = 32;          // context rows per stage
 constexpr int kAttnMaxWarps = 8;       // consumer warps at most
+// A thread holds D / 2 fp32 output sums. From D = 128 on, at most 6 consumer
+// warps (7 with the producer, two on a sub-partition) leave it 255 registers;
+// 9 warps would cap it at 168 and spill.
+__host__ __device__ constexpr int attn_max_warps(int D) { return D >= 128 ? 6 : kAttnMaxWarps; }
 constexpr int kAttnMaxHeads = 16;      // query heads per CTA (one m16 tile)
-constexpr int kAttnCombineThreads = 128;
+constexpr int kAttnCombineThreads = 128;  // 4 columns a thread, 2 to 8 parts of the splits
 
 struct alignas(64) AttnParams {
   CUtensorMap k_map;            // K as 4-D {D, Hkv, Cmax, B}; box {64, 1, 32, 1}, 128B swizzle
@@ -60,7 +64,9 @@ struct alignas(64) AttnParams {
   int hgroups;                  // Hq / heads
   int nw;                       // consumer warps
   int stages;                   // ring slots, a multiple of nw
-  int rows_per_split, nsplit;
+  int rows_per_split, nsplit;   // fixed splits
+  int balanced;                 // splits balanced over the batch's lengths
+  int units;                    // balanced: CTAs the batch's context is spread over
   uint32_t stage_bytes;         // 2 * 32 * D * 2: K rows, then V rows
   uint32_t q_off;               // shared-memory offset of q' hi and lo (16 rows each)
   uint32_t qstride;             // bytes per q' row in shared memory (D * 2 + 16)
@@ -74,6 +80,7 @@ struct AttnCombineParams {
   const int32_t* seq_lens;
   float* out;
   int B, Cmax, Hq, D, heads, hgroups, rows_per_split, nsplit;
+  int balanced, units;
 };
 
 // ---------------------------------------------------------------------------
@@ -161,7 +168,7 @@ __device__ __forceinline__ float exp2_fast(float x) { return exp2f(x); }
 // After the context loop the ring is reused for the warps' merge:
 //   [O: nw x heads x (D + 4) floats][(m, l): nw x heads float2]
 template <typename Tag, int D>
-__global__ void __launch_bounds__(32 * (kAttnMaxWarps + 1), 1)
+__global__ void __launch_bounds__(32 * (attn_max_warps(D) + 1), 1)
     gqa_attn_kernel(const __grid_constant__ AttnParams p) {
   constexpr int R = kAttnRows;
   constexpr int KS = D / 16;          // 16-column k-steps of the score product
@@ -177,14 +184,26 @@ __global__ void __launch_bounds__(32 * (kAttnMaxWarps + 1), 1)
   const int lane = tid & 31;
   const int nthreads = 32 * (p.nw + 1);
 
-  const int tile = blockIdx.x / p.nsplit;
-  const int split = blockIdx.x - tile * p.nsplit;
-  const int hg = tile / p.B;
-  const int b = tile - hg * p.B;
+  // Fixed splits: CTA (tile, split), tile = hg * B + b. Balanced splits: CTA u
+  // takes head group u % hgroups and batch split u / hgroups, found from the
+  // lengths after the dependency wait. Either way its partial is slot blockIdx.x.
+  int hg, b, split, c_begin, rps;
+  if (!p.balanced) {
+    const int tile = blockIdx.x / p.nsplit;
+    split = blockIdx.x - tile * p.nsplit;
+    hg = tile / p.B;
+    b = tile - hg * p.B;
+    rps = p.rows_per_split;
+    c_begin = split * rps;
+  } else {
+    hg = blockIdx.x % p.hgroups;
+    b = split = c_begin = rps = 0;
+  }
   const int h0 = hg * p.heads;
   const int kv_h = h0 / p.G;
-  const int c_begin = split * p.rows_per_split;
-  const int pre = min(min(p.stages, p.rows_per_split / R), (p.Cmax - c_begin + R - 1) / R);
+  // Fixed splits issue their first stages before the length is read.
+  const int pre =
+      p.balanced ? 0 : min(min(p.stages, rps / R), (p.Cmax - c_begin + R - 1) / R);
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.bar_off);
   volatile int* fail = reinterpret_cast<volatile int*>(bars + 2 * p.stages);
@@ -209,9 +228,29 @@ __global__ void __launch_bounds__(32 * (kAttnMaxWarps + 1), 1)
   grid_dependency_wait();
   grid_launch_dependents();
 
-  const int L = clamped_len(p.seq_lens, b, p.Cmax);
-  const int nsplit_b = L > 0 ? (L + p.rows_per_split - 1) / p.rows_per_split : 1;
-  const int c_end = min(c_begin + p.rows_per_split, L);
+  int L, nsplit_b;
+  if (!p.balanced) {
+    L = clamped_len(p.seq_lens, b, p.Cmax);
+    nsplit_b = L > 0 ? (L + rps - 1) / rps : 1;
+  } else {
+    // Warp-collective: every warp works the split out for itself.
+    const int sps = balanced_sps(p.seq_lens, p.B, p.Cmax, R, p.hgroups, p.units);
+    const BalancedSplit bs = balanced_find(p.seq_lens, p.B, p.Cmax, R, sps, blockIdx.x / p.hgroups);
+    if (bs.found) {
+      b = bs.b;
+      L = bs.L;
+      split = bs.split;
+      nsplit_b = bs.n;
+    } else {  // past the batch's splits: no work
+      b = 0;
+      L = 0;
+      split = 1;
+      nsplit_b = 1;
+    }
+    rps = sps * R;
+    c_begin = split * rps;
+  }
+  const int c_end = min(c_begin + rps, L);
   const int n_iters = split < nsplit_b && c_end > c_begin ? (c_end - c_begin + R - 1) / R : 0;
 
   if (warp == p.nw) {
@@ -262,17 +301,32 @@ __global__ void __launch_bounds__(32 * (kAttnMaxWarps + 1), 1)
     // q' = q * scale * log2(e) of the CTA's heads as 16-bit hi and lo rows;
     // rows past `heads` are zero.
     {
+      // Batches of kQv float4 loads a thread, all issued before any is used.
+      constexpr int kQv = 4;
       const uint32_t qs = p.qstride;
       uint8_t* qhi = smem + p.q_off;
       uint8_t* qlo = qhi + 16 * qs;
-      const float* src = p.q + ((size_t)b * p.Hq + h0) * D;
-      for (int i = tid; i < 16 * D; i += 32 * p.nw) {
-        const int h = i / D, d = i - (i / D) * D;
-        const float x = h < p.heads ? src[(size_t)h * D + d] * p.qscale : 0.0f;
-        uint16_t hi, lo;
-        split_one(Tag{}, x, hi, lo);
-        *reinterpret_cast<uint16_t*>(qhi + h * qs + d * 2) = hi;
-        *reinterpret_cast<uint16_t*>(qlo + h * qs + d * 2) = lo;
+      const float4* src = reinterpret_cast<const float4*>(p.q + ((size_t)b * p.Hq + h0) * D);
+      const int nthr = 32 * p.nw;
+      for (int i0 = tid; i0 < 16 * D / 4; i0 += kQv * nthr) {
+      float4 x[kQv];
+#pragma unroll
+      for (int u = 0; u < kQv; ++u) {
+        const int i = i0 + u * nthr;  // float4 index: head i / (D/4), columns 4 * (i % (D/4))
+        x[u] = (i < 16 * D / 4 && i / (D / 4) < p.heads) ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kQv; ++u) {
+        const int i = i0 + u * nthr;
+        if (i < 16 * D / 4) {
+          const int h = i / (D / 4), d = (i - h * (D / 4)) * 4;
+          uint32_t hi[2], lo[2];
+          split_pack(Tag{}, x[u].x * p.qscale, x[u].y * p.qscale, hi[0], lo[0]);
+          split_pack(Tag{}, x[u].z * p.qscale, x[u].w * p.qscale, hi[1], lo[1]);
+          *reinterpret_cast<uint2*>(qhi + h * qs + d * 2) = make_uint2(hi[0], hi[1]);
+          *reinterpret_cast<uint2*>(qlo + h * qs + d * 2) = make_uint2(lo[0], lo[1]);
+        }
+      }
       }
     }
     named_sync(1, 32 * p.nw);
@@ -303,6 +357,7 @@ __global__ void __launch_bounds__(32 * (kAttnMaxWarps + 1), 1)
       }
       const uint32_t k_s = base_s + (uint32_t)stage * p.stage_bytes;
       const uint32_t v_s = k_s + kHalf;
+
       const int c0 = c_begin + it * R;
       const int nvalid = min(R, c_end - c0);
 
@@ -487,7 +542,7 @@ __global__ void __launch_bounds__(32 * (kAttnMaxWarps + 1), 1)
       *reinterpret_cast<float4*>(p.out + ((size_t)b * p.Hq + h0 + h) * D + d) =
           make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     } else {
-      const size_t slot = ((size_t)tile * p.nsplit + split) * p.heads + h;
+      const size_t slot = (size_t)blockIdx.x * p.heads + h;
       __stcg(reinterpret_cast<float4*>(p.ws_o + slot * D + d), acc);
       if (d == 0) __stcg(p.ws_ml + slot, make_float2(M, l));
     }
@@ -495,68 +550,96 @@ __global__ void __launch_bounds__(32 * (kAttnMaxWarps + 1), 1)
 }
 
 // ---------------------------------------------------------------------------
-// CTA per tile: for each head, the splits' maxima give M, the weights
-// 2^(m_s - M) / sum_s 2^(m_s - M) l_s, and out = sum_s weight_s * O_s, all in
-// split order. Tiles whose sequence fits one split were written by the main
-// kernel and are skipped.
+// CTA per (tile, head): the splits' maxima give M and the normaliser
+// Z = sum_s 2^(m_s - M) l_s; then out = sum_s 2^(m_s - M) / Z * O_s. A thread
+// owns 4 output columns and the splits s = part, part + parts, ...; the
+// first batch of its partial loads goes out before M and Z are known, so the
+// call costs about one round trip to L2 after the dependency wait. The parts
+// are added in part order, so the result is deterministic. Tiles whose
+// sequence fits one split were written by the main kernel and are skipped.
+// Split s of a tile is slot tile * nsplit + s (fixed splits) or
+// (P_b + s) * hgroups + hg (balanced; P_b = splits of the sequences before b).
 __global__ void __launch_bounds__(kAttnCombineThreads)
     gqa_attn_combine_kernel(const __grid_constant__ AttnCombineParams p) {
-  extern __shared__ float wts[];  // [heads][nsplit]
-  const int tile = blockIdx.x;
+  constexpr int kBatch = 8;
+  __shared__ float2 mz;                                      // (M, 1 / Z) of the head
+  __shared__ float4 red[kAttnCombineThreads];                // per-part sums
+  const int tile = blockIdx.x / p.heads;
+  const int h = blockIdx.x - tile * p.heads;
   const int hg = tile / p.B;
   const int b = tile - hg * p.B;
-  const int L = clamped_len(p.seq_lens, b, p.Cmax);
-  const int nsplit_b = L > 0 ? (L + p.rows_per_split - 1) / p.rows_per_split : 1;
+  int nsplit_b;
+  size_t first, step;  // slot of split s: first + s * step
+  if (!p.balanced) {
+    const int L = clamped_len(p.seq_lens, b, p.Cmax);
+    nsplit_b = L > 0 ? (L + p.rows_per_split - 1) / p.rows_per_split : 1;
+    first = (size_t)tile * p.nsplit;
+    step = 1;
+  } else {
+    const int sps = balanced_sps(p.seq_lens, p.B, p.Cmax, kAttnRows, p.hgroups, p.units);
+    const int2 pn = balanced_prefix(p.seq_lens, p.Cmax, kAttnRows, sps, b);
+    nsplit_b = pn.y;
+    first = (size_t)pn.x * p.hgroups + hg;
+    step = p.hgroups;
+  }
   grid_dependency_wait();
   grid_launch_dependents();
   if (nsplit_b <= 1) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const float2* ml = p.ws_ml + (size_t)tile * p.nsplit * p.heads;
-  for (int h = warp; h < p.heads; h += kAttnCombineThreads / 32) {
+  const int cols = p.D / 4;
+  const int parts = kAttnCombineThreads / cols;
+  const int col = threadIdx.x % cols, part = threadIdx.x / cols;
+  const int d = 4 * col;
+  auto slot_of = [&](int s) { return (first + (size_t)s * step) * p.heads + h; };
+
+  float4 x[kBatch];
+  float em[kBatch];
+  auto load = [&](int s0) {
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int s = s0 + u * parts;
+      if (s < nsplit_b) {
+        const size_t slot = slot_of(s);
+        x[u] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + slot * p.D + d));
+        em[u] = __ldcg(p.ws_ml + slot).x;
+      }
+    }
+  };
+  load(part);
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
     float M = -INFINITY;
-    for (int s = lane; s < nsplit_b; s += 32) M = fmaxf(M, __ldcg(ml + (size_t)s * p.heads + h).x);
+    for (int s = lane; s < nsplit_b; s += 32) M = fmaxf(M, __ldcg(p.ws_ml + slot_of(s)).x);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float l = 0.0f;
+    float z = 0.0f;
     for (int s = lane; s < nsplit_b; s += 32) {
-      const float2 v = __ldcg(ml + (size_t)s * p.heads + h);
-      const float e = exp2_fast(v.x - M);
-      wts[h * p.nsplit + s] = e;
-      l = fmaf(v.y, e, l);
+      const float2 v = __ldcg(p.ws_ml + slot_of(s));
+      z = fmaf(v.y, exp2_fast(v.x - M), z);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-    const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-    __syncwarp();
-    for (int s = lane; s < nsplit_b; s += 32) wts[h * p.nsplit + s] *= inv;
+    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    if (lane == 0) mz = make_float2(M, z > 0.0f ? 1.0f / z : 0.0f);
   }
   __syncthreads();
-  const int h0 = hg * p.heads;
-  const int n4 = p.heads * (p.D / 4);
-  for (int i = threadIdx.x; i < n4; i += kAttnCombineThreads) {
-    const int h = i / (p.D / 4), d = (i - h * (p.D / 4)) * 4;
-    const float* w = wts + h * p.nsplit;
-    const float4* src = reinterpret_cast<const float4*>(
-        p.ws_o + ((size_t)tile * p.nsplit * p.heads + h) * p.D + d);
-    const size_t stride = (size_t)p.heads * p.D / 4;  // float4s between splits
-    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    constexpr int kBatch = 8;
-    for (int s0 = 0; s0 < nsplit_b; s0 += kBatch) {
-      float4 x[kBatch];
+  const float2 hz = mz;
+  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  for (int s0 = part; s0 < nsplit_b; s0 += kBatch * parts) {
+    if (s0 != part) load(s0);
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u)
-        if (s0 + u < nsplit_b) x[u] = __ldcg(src + (size_t)(s0 + u) * stride);
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u)
-        if (s0 + u < nsplit_b) {
-          const float e = w[s0 + u];
-          acc.x = fmaf(x[u].x, e, acc.x);
-          acc.y = fmaf(x[u].y, e, acc.y);
-          acc.z = fmaf(x[u].z, e, acc.z);
-          acc.w = fmaf(x[u].w, e, acc.w);
-        }
-    }
-    *reinterpret_cast<float4*>(p.out + ((size_t)b * p.Hq + h0 + h) * p.D + d) = acc;
+    for (int u = 0; u < kBatch; ++u)
+      if (s0 + u * parts < nsplit_b) {
+        const float wgt = exp2_fast(em[u] - hz.x) * hz.y;
+        acc.x = fmaf(x[u].x, wgt, acc.x);
+        acc.y = fmaf(x[u].y, wgt, acc.y);
+        acc.z = fmaf(x[u].z, wgt, acc.z);
+        acc.w = fmaf(x[u].w, wgt, acc.w);
+      }
+  }
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  if (part == 0) {
+    for (int q = 1; q < parts; ++q) add4(acc, red[q * cols + col]);
+    *reinterpret_cast<float4*>(p.out + ((size_t)b * p.Hq + hg * p.heads + h) * p.D + d) = acc;
   }
 }
 

@@ -60,19 +60,26 @@ int gqa_attn_decode(const float *q, const void *k_cache, const void *v_cache,
                     int kv_dtype, float scale, int mode, void *stream);
 
 /* The same with the launch shape chosen: consumer_warps (1..8) warps stream
- * the context in each CTA and nsplit is the number of context splits per
- * tile (rounded so each split is a whole number of 32-row stages); 0 lets the
- * library choose either. Any choice gives results within the stated bounds. */
+ * the context in each CTA; nsplit is the number of context splits per tile
+ * (rounded so each split is a whole number of 32-row stages); split_mode 1
+ * cuts each sequence into those fixed splits, 2 spreads the batch's context
+ * rows evenly over tiles x nsplit CTAs whatever the lengths (each CTA reads
+ * all of seq_lens to find its split). 0 lets the library choose any of
+ * them: balanced splits when seq_lens is given and B > 1. Any choice gives
+ * results within the stated bounds. */
 int gqa_attn_decode_tuned(const float *q, const void *k_cache, const void *v_cache,
                           const int32_t *seq_lens, float *out, int B, int Cmax, int Hq, int Hkv,
                           int D, int kv_dtype, float scale, int mode, int consumer_warps,
-                          int nsplit, void *stream);
+                          int nsplit, int split_mode, void *stream);
 
-/* The launch plan of a call without launching it: info[0..7] = resolved mode,
- * query heads per CTA, consumer warps, ring stages, rows per split, splits
- * per tile, tiles, dynamic shared memory bytes (the first n_info of them). */
+/* The launch plan of a call without launching it (ragged != 0: seq_lens will
+ * be given): info[0..9] = resolved mode, query heads per CTA, consumer warps,
+ * ring stages, rows per fixed split, splits per tile, tiles, dynamic shared
+ * memory bytes, split mode (1 fixed, 2 balanced), CTAs launched (the first
+ * n_info of them). */
 int gqa_attn_plan(int B, int Cmax, int Hq, int Hkv, int D, int kv_dtype, int mode,
-                  int consumer_warps, int nsplit, int *info, int n_info);
+                  int consumer_warps, int nsplit, int split_mode, int ragged, int *info,
+                  int n_info);
 
 /* Synchronise `stream`, then read the call's device status word (set when a
  * bounded wait inside a kernel runs out): GQA_AV_OK or

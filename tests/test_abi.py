@@ -118,6 +118,7 @@ def test_attention_host_checks_reject_before_launch(native, args, status):
 
 
 def test_attention_tuning_range_checked(native):
-    rc = native.lib.gqa_attn_decode_tuned(FAKE, FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 64, 0, 1.0,
-                                          -1, 9, 0, None)
-    assert rc == 1 and b"consumer_warps" in native.lib.gqa_attn_last_error()
+    for warps, splits, smode in ((9, 0, 0), (-1, 0, 0), (0, -2, 0), (0, 0, 3)):
+        rc = native.lib.gqa_attn_decode_tuned(FAKE, FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 64, 0, 1.0,
+                                              -1, warps, splits, smode, None)
+        assert rc == 1 and b"out of range" in native.lib.gqa_attn_last_error()

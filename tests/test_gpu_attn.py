@@ -39,12 +39,13 @@ def attn_case(rng, B, C, Hq, Hkv, D, kd, lens, q_sigma=1.0, pad_nan=True):
     return q, k, v, sl
 
 
-def run_attn(gq, q, k, v, sl, mode=-1, scale=None, warps=0, nsplit=0):
+def run_attn(gq, q, k, v, sl, mode=-1, scale=None, warps=0, nsplit=0, split_mode=0):
     dev = torch.device("cuda")
     B, Hq, D = q.shape
     out = torch.full((B, Hq, D), 7.0, dtype=torch.float32, device=dev)
     gq.gqa_attn_decode(q.to(dev), k.to(dev), v.to(dev), None if sl is None else sl.to(dev), out,
-                       mode=mode, scale=scale, consumer_warps=warps, nsplit=nsplit)
+                       mode=mode, scale=scale, consumer_warps=warps, nsplit=nsplit,
+                       split_mode=split_mode)
     gq.gqa_attn_device_status()
     return out.cpu().double().numpy()
 
@@ -77,21 +78,50 @@ def test_attention_shape_sweep(gq, G, D):
         ref = oracle_of(q, k, v, sl, kd, scale)
         assert np.all(ref[3] == 0.0)
         for mode in (0, 1):
-            for nsplit in (0, 1, 5):
-                got = run_attn(gq, q, k, v, sl, mode, scale, nsplit=nsplit)
-                check(got, ref, f"G={G} D={D} {kd} mode={mode} nsplit={nsplit}")
-                assert np.all(got[3] == 0.0), "an empty context must give out = 0"
+            for nsplit, smode in ((0, 0), (1, 1), (5, 1), (1, 2), (5, 2)):
+                got = run_attn(gq, q, k, v, sl, mode, scale, nsplit=nsplit, split_mode=smode)
+                what = f"G={G} D={D} {kd} mode={mode} nsplit={nsplit} split_mode={smode}"
+                check(got, ref, what)
+                assert np.all(got[3] == 0.0), f"{what}: an empty context must give out = 0"
 
 
 @pytest.mark.parametrize("warps", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_attention_consumer_warps(gq, warps):
-    """Every consumer-warp count (ring slots per warp, the warp merge) gives the same result."""
+    """Every consumer-warp count (ring slots per warp, the warp merge) gives the
+    same result; D >= 128 takes at most 6 consumer warps and refuses more."""
     rng = np.random.default_rng(7 + warps)
-    q, k, v, sl = attn_case(rng, 2, 1000, 8, 2, 128, "bf16", [1000, 333], q_sigma=2.0)
-    ref = oracle_of(q, k, v, sl, "bf16", 128 ** -0.5)
-    for nsplit in (0, 1, 3):
-        check(run_attn(gq, q, k, v, sl, 1, 128 ** -0.5, warps=warps, nsplit=nsplit), ref,
-              f"warps={warps} nsplit={nsplit}")
+    q, k, v, sl = attn_case(rng, 2, 1000, 8, 2, 64, "bf16", [1000, 333], q_sigma=2.0)
+    ref = oracle_of(q, k, v, sl, "bf16", 64 ** -0.5)
+    for nsplit, smode in ((0, 0), (1, 1), (3, 1), (3, 2)):
+        check(run_attn(gq, q, k, v, sl, 1, 64 ** -0.5, warps=warps, nsplit=nsplit,
+                       split_mode=smode), ref, f"warps={warps} nsplit={nsplit} split_mode={smode}")
+    for D, kd, G in ((128, "bf16", 6), (256, "fp16", 16)):
+        q, k, v, sl = attn_case(rng, 2, 700, 2 * G, 2, D, kd, [700, 90], q_sigma=2.0)
+        if warps > 6:
+            with pytest.raises(gq.GqaAvError):
+                run_attn(gq, q, k, v, sl, 1, D ** -0.5, warps=warps)
+            continue
+        ref = oracle_of(q, k, v, sl, kd, D ** -0.5)
+        for nsplit, smode in ((0, 0), (1, 1), (4, 2)):
+            check(run_attn(gq, q, k, v, sl, 1, D ** -0.5, warps=warps, nsplit=nsplit,
+                           split_mode=smode), ref, f"D={D} warps={warps} split_mode={smode}")
+
+
+def test_attention_balanced_splits_many_sequences(gq):
+    """Balanced splits over a batch of more sequences than a warp has lanes,
+    with empty, one-row, full and clamped lengths mixed."""
+    rng = np.random.default_rng(21)
+    B, C = 40, 300
+    lens = rng.integers(0, C + 1, size=B)
+    lens[:6] = [0, 1, C, 5000, -3, 33]
+    q, k, v, _ = attn_case(rng, B, C, 8, 2, 64, "bf16", np.clip(lens, 0, C), q_sigma=2.0)
+    sl = torch.tensor(lens, dtype=torch.int32)
+    ref = oracle_of(q, k, v, sl, "bf16", 0.125)
+    for nsplit in (0, 1, 2, 9):
+        check(run_attn(gq, q, k, v, sl, -1, 0.125, nsplit=nsplit, split_mode=2), ref,
+              f"balanced nsplit={nsplit}")
+        check(run_attn(gq, q, k, v, sl, -1, 0.125, nsplit=nsplit, split_mode=1), ref,
+              f"fixed nsplit={nsplit}")
 
 
 def test_attention_one_hot_scores_return_the_row(gq):
@@ -135,9 +165,10 @@ def test_attention_lengths_clamped(gq):
 def test_attention_deterministic(gq):
     rng = np.random.default_rng(8)
     q, k, v, sl = attn_case(rng, 3, 3000, 16, 4, 128, "bf16", [3000, 1777, 64])
-    a = run_attn(gq, q, k, v, sl, nsplit=7)
-    b = run_attn(gq, q, k, v, sl, nsplit=7)
-    assert np.array_equal(a, b)
+    for smode in (1, 2):
+        a = run_attn(gq, q, k, v, sl, nsplit=7, split_mode=smode)
+        b = run_attn(gq, q, k, v, sl, nsplit=7, split_mode=smode)
+        assert np.array_equal(a, b)
 
 
 def test_attention_matches_chained_score_and_av_calls(gq):
