@@ -42,12 +42,14 @@ int afail_cuda(cudaError_t e, const char* what) {
 
 using AttnKernel = void (*)(AttnParams);
 
+// The kernel compiled for at most MW consumer warps (6: 255 registers a
+// thread; 8: 168).
 template <typename Tag>
-AttnKernel pick(int D) {
+AttnKernel pick(int D, int nw) {
   switch (D) {
-    case 64: return gqa_attn_kernel<Tag, 64>;
-    case 128: return gqa_attn_kernel<Tag, 128>;
-    case 256: return gqa_attn_kernel<Tag, 256>;
+    case 64: return gqa_attn_kernel<Tag, 64, 8>;
+    case 128: return nw > 6 ? gqa_attn_kernel<Tag, 128, 8> : gqa_attn_kernel<Tag, 128, 6>;
+    case 256: return gqa_attn_kernel<Tag, 256, 6>;
     default: return nullptr;
   }
 }
@@ -89,13 +91,42 @@ int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int kv_dtype, int mod
   p->hgroups = Hq / p->heads;
   p->tiles = p->hgroups * B;
 
+  cudaDeviceProp prop;
+  cudaError_t e = cudaGetDeviceProperties(&prop, dev);
+  if (e != cudaSuccess) return afail_cuda(e, "cudaGetDeviceProperties");
+  const int sms = prop.multiProcessorCount;
+
+  // Splits: one CTA per SM over the tiles on few-tile shapes, and no split
+  // longer than kAttnMaxSplitRows rows (short waves on many-tile shapes).
+  const int max_splits = (Cmax + kAttnRows - 1) / kAttnRows;
+  long long want = want_nsplit > 0 ? want_nsplit
+                                   : std::max<long long>(p->tiles < sms ? sms / p->tiles : 1,
+                                                         (Cmax + kAttnMaxSplitRows - 1) /
+                                                             kAttnMaxSplitRows);
+  want = std::max<long long>(1, std::min<long long>(want, max_splits));
+  const int rps0 = static_cast<int>((Cmax + want - 1) / want);
+  p->rows_per_split = (rps0 + kAttnRows - 1) / kAttnRows * kAttnRows;
+  p->nsplit = (Cmax + p->rows_per_split - 1) / p->rows_per_split;
+  // Balanced splits spread the batch's context rows evenly over the same
+  // number of CTAs, whatever the lengths: at most units + tiles CTAs have work.
+  p->balanced = split_mode == 2 || (split_mode == 0 && ragged && B > 1);
+  if (static_cast<long long>(p->tiles) * (p->nsplit + 1) > 0x7fffffffLL)
+    return afail(GQA_AV_ERR_UNSUPPORTED, "grid too large");
+  p->units = p->tiles * p->nsplit;
+  p->ctas = p->balanced ? p->units + p->tiles : p->units;
+  p->combine = p->balanced || p->nsplit > 1;
+  p->ws_bytes = p->combine ? static_cast<size_t>(p->ctas) * p->heads *
+                                 (static_cast<size_t>(D) * 4 + 8)
+                           : 0;
+
   // Consumer warps and ring: 32-row stages of K and V (128 * D bytes); the
   // ring holds a whole number of stages per warp, at most 192 KiB. Measured
-  // on GB300: 8 warps of 3 stages at D = 64, 6 warps of 2 at D = 128 and
-  // 3 warps of 2 at D = 256 (a warp overlaps its next stage's load with the
-  // current stage's products).
+  // on GB300: 8 warps of 3 stages at D = 64, 6 warps of 2 stages at D = 128
+  // (a warp overlaps its next stage's load with the current stage's
+  // products; 8 warps of 1 stage measured 2-5 % slower on one-wave and
+  // many-wave grids alike), 3 warps of 2 stages at D = 256.
   p->stage_bytes = kAttnRows * D * 2 * 2;
-  p->nw = want_nw > 0 ? want_nw : (D == 256 ? 3 : D == 128 ? 6 : 8);
+  p->nw = want_nw > 0 ? want_nw : D == 256 ? 3 : D == 64 ? 8 : 6;
   if (p->nw < 1 || p->nw > attn_max_warps(D))
     return afail(GQA_AV_ERR_UNSUPPORTED, "consumer warps %d outside 1..%d for D=%d", p->nw,
                  attn_max_warps(D), D);
@@ -109,39 +140,9 @@ int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int kv_dtype, int mod
   p->merge_bytes = p->nw * p->heads * ((D + 4) * 4 + 8);
   if (p->merge_bytes > p->stages * p->stage_bytes)
     return afail(GQA_AV_ERR_UNSUPPORTED, "warp merge (%d B) larger than the ring", p->merge_bytes);
-
-  cudaDeviceProp prop;
-  cudaError_t e = cudaGetDeviceProperties(&prop, dev);
-  if (e != cudaSuccess) return afail_cuda(e, "cudaGetDeviceProperties");
-  const int sms = prop.multiProcessorCount;
   if (p->smem > static_cast<int>(prop.sharedMemPerBlockOptin))
     return afail(GQA_AV_ERR_UNSUPPORTED, "plan needs %d B of shared memory (limit %d)", p->smem,
                  static_cast<int>(prop.sharedMemPerBlockOptin));
-
-  // Splits: one CTA per SM over the tiles on few-tile shapes, and no split
-  // longer than kAttnMaxSplitRows rows (short waves on many-tile shapes).
-  const int max_splits = (Cmax + kAttnRows - 1) / kAttnRows;
-  long long want = want_nsplit > 0 ? want_nsplit
-                                   : std::max<long long>(p->tiles < sms ? sms / p->tiles : 1,
-                                                         (Cmax + kAttnMaxSplitRows - 1) /
-                                                             kAttnMaxSplitRows);
-  want = std::max<long long>(1, std::min<long long>(want, max_splits));
-  const int rps0 = static_cast<int>((Cmax + want - 1) / want);
-  p->rows_per_split = (rps0 + kAttnRows - 1) / kAttnRows * kAttnRows;
-  p->nsplit = (Cmax + p->rows_per_split - 1) / p->rows_per_split;
-  if (static_cast<long long>(p->tiles) * p->nsplit > 0x7fffffffLL)
-    return afail(GQA_AV_ERR_UNSUPPORTED, "grid too large");
-  // Balanced splits spread the batch's context rows evenly over the same
-  // number of CTAs, whatever the lengths: at most units + tiles CTAs have work.
-  p->balanced = split_mode == 2 || (split_mode == 0 && ragged && B > 1);
-  p->units = p->tiles * p->nsplit;
-  p->ctas = p->balanced ? p->units + p->tiles : p->units;
-  p->combine = p->balanced || p->nsplit > 1;
-  if (static_cast<long long>(p->units) + p->tiles > 0x7fffffffLL)
-    return afail(GQA_AV_ERR_UNSUPPORTED, "grid too large");
-  p->ws_bytes = p->combine ? static_cast<size_t>(p->ctas) * p->heads *
-                                 (static_cast<size_t>(D) * 4 + 8)
-                           : 0;
   return GQA_AV_OK;
 }
 
@@ -318,7 +319,7 @@ extern "C" int gqa_attn_decode_tuned(const float* q, const void* k_cache, const 
   p.bar_off = static_cast<uint32_t>(pl.bar_off);
   p.timeout_ns = kAttnTimeoutNs;
 
-  AttnKernel k = kv_dtype == GQA_AV_BF16 ? pick<Bf16Tag>(D) : pick<Fp16Tag>(D);
+  AttnKernel k = kv_dtype == GQA_AV_BF16 ? pick<Bf16Tag>(D, pl.nw) : pick<Fp16Tag>(D, pl.nw);
   if (!k) return afail(GQA_AV_ERR_UNSUPPORTED, "no attention kernel for D=%d", D);
   e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
   if (e != cudaSuccess) return afail_cuda(e, "cudaFuncSetAttribute");

@@ -42,10 +42,12 @@ namespace gqa_av {
 
 constexpr int kAttnRows = 32;          // context rows per stage
 constexpr int kAttnMaxWarps = 8;       // consumer warps at most
-// A thread holds D / 2 fp32 output sums. From D = 128 on, at most 6 consumer
-// warps (7 with the producer, two on a sub-partition) leave it 255 registers;
-// 9 warps would cap it at 168 and spill.
-__host__ __device__ constexpr int attn_max_warps(int D) { return D >= 128 ? 6 : kAttnMaxWarps; }
+// A thread holds D / 2 fp32 output sums. Up to 6 consumer warps (7 with the
+// producer, two on a sub-partition) leave it 255 registers; 8 (nine warps)
+// cap it at 168. The kernel is compiled for either bound (MW = 6 or 8):
+// D = 256 only for 6, D = 128 for both (8 warps spill a little but stream
+// faster on many-wave grids), D = 64 for 8.
+__host__ __device__ constexpr int attn_max_warps(int D) { return D == 256 ? 6 : kAttnMaxWarps; }
 constexpr int kAttnMaxHeads = 16;      // query heads per CTA (one m16 tile)
 constexpr int kAttnCombineThreads = 128;  // 4 columns a thread, 2 to 8 parts of the splits
 
@@ -100,10 +102,12 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
                : "memory");
 }
 
-// d += a (16x16, row-major) * b (16x8, column-major), fp32 accumulate.
+// d += a (16x16, row-major) * b (16x8, column-major), fp32 accumulate. Not
+// volatile: a pure function of its registers, so the compiler may interleave
+// independent products to hide the tensor pipe's latency.
 __device__ __forceinline__ void mma16816(Bf16Tag, float (&d)[4], const uint32_t (&a)[4],
                                          uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
       "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -112,7 +116,7 @@ __device__ __forceinline__ void mma16816(Bf16Tag, float (&d)[4], const uint32_t 
 
 __device__ __forceinline__ void mma16816(Fp16Tag, float (&d)[4], const uint32_t (&a)[4],
                                          uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
       "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -167,8 +171,8 @@ __device__ __forceinline__ float exp2_fast(float x) { return exp2f(x); }
 //   [mbarriers: full, empty (stages each)][fail flag]
 // After the context loop the ring is reused for the warps' merge:
 //   [O: nw x heads x (D + 4) floats][(m, l): nw x heads float2]
-template <typename Tag, int D>
-__global__ void __launch_bounds__(32 * (attn_max_warps(D) + 1), 1)
+template <typename Tag, int D, int MW>
+__global__ void __launch_bounds__(32 * (MW + 1), 1)
     gqa_attn_kernel(const __grid_constant__ AttnParams p) {
   constexpr int R = kAttnRows;
   constexpr int KS = D / 16;          // 16-column k-steps of the score product
@@ -373,17 +377,17 @@ __global__ void __launch_bounds__(32 * (attn_max_warps(D) + 1), 1)
         const int chunk = 2 * ks + (mi & 1);
         const uint32_t part_off = (uint32_t)(chunk >> 3) * R * 128;
         const uint32_t swz = (uint32_t)(((chunk & 7) ^ mr) << 4);
+        // K rows 16jp.. : matrix mi is (rows 16jp + 8*(mi>>1).., chunk 2ks + (mi&1)).
+        uint32_t kb[2][4];
 #pragma unroll
-        for (int jp = 0; jp < 2; ++jp) {
-          // K rows 16jp.. : matrix mi is (rows 16jp + 8*(mi>>1).., chunk 2ks + (mi&1)).
-          const int row = 16 * jp + 8 * (mi >> 1) + mr;
-          uint32_t kb[4];
-          ldsm_x4(k_s + part_off + (uint32_t)row * 128 + swz, kb);
-          mma16816(Tag{}, s[2 * jp], ahi, kb[0], kb[1]);
-          mma16816(Tag{}, s[2 * jp], alo, kb[0], kb[1]);
-          mma16816(Tag{}, s[2 * jp + 1], ahi, kb[2], kb[3]);
-          mma16816(Tag{}, s[2 * jp + 1], alo, kb[2], kb[3]);
-        }
+        for (int jp = 0; jp < 2; ++jp)
+          ldsm_x4(k_s + part_off + (uint32_t)(16 * jp + 8 * (mi >> 1) + mr) * 128 + swz, kb[jp]);
+        // The hi products of the four row tiles, then the lo ones: each
+        // accumulator is used again only four products later.
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mma16816(Tag{}, s[j], ahi, kb[j >> 1][2 * (j & 1)], kb[j >> 1][2 * (j & 1) + 1]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mma16816(Tag{}, s[j], alo, kb[j >> 1][2 * (j & 1)], kb[j >> 1][2 * (j & 1) + 1]);
       }
 
       if (nvalid < R) {
@@ -452,15 +456,19 @@ __global__ void __launch_bounds__(32 * (attn_max_warps(D) + 1), 1)
         const uint32_t part_off = (uint32_t)(chunk >> 3) * R * 128;
         const uint32_t swz = (uint32_t)(((chunk & 7) ^ mr) << 4);
         float d0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, d1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        uint32_t vb[2][4];
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+          ldsm_x4_trans(v_s + part_off + (uint32_t)(16 * kk + 8 * (mi & 1) + mr) * 128 + swz, vb[kk]);
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
-          const int row = 16 * kk + 8 * (mi & 1) + mr;
-          uint32_t vb[4];
-          ldsm_x4_trans(v_s + part_off + (uint32_t)row * 128 + swz, vb);
-          mma16816(Tag{}, d0, phi[kk], vb[0], vb[1]);
-          mma16816(Tag{}, d0, plo[kk], vb[0], vb[1]);
-          mma16816(Tag{}, d1, phi[kk], vb[2], vb[3]);
-          mma16816(Tag{}, d1, plo[kk], vb[2], vb[3]);
+          mma16816(Tag{}, d0, phi[kk], vb[kk][0], vb[kk][1]);
+          mma16816(Tag{}, d1, phi[kk], vb[kk][2], vb[kk][3]);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          mma16816(Tag{}, d0, plo[kk], vb[kk][0], vb[kk][1]);
+          mma16816(Tag{}, d1, plo[kk], vb[kk][2], vb[kk][3]);
         }
         o[2 * nj][0] = fmaf(o[2 * nj][0], a0, d0[0]);
         o[2 * nj][1] = fmaf(o[2 * nj][1], a0, d0[1]);

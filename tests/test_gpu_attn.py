@@ -87,8 +87,9 @@ def test_attention_shape_sweep(gq, G, D):
 
 @pytest.mark.parametrize("warps", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_attention_consumer_warps(gq, warps):
-    """Every consumer-warp count (ring slots per warp, the warp merge) gives the
-    same result; D >= 128 takes at most 6 consumer warps and refuses more."""
+    """Every consumer-warp count (ring slots per warp, the warp merge, both
+    compiled register bounds) gives the same result; D = 256 takes at most 6
+    consumer warps and refuses more."""
     rng = np.random.default_rng(7 + warps)
     q, k, v, sl = attn_case(rng, 2, 1000, 8, 2, 64, "bf16", [1000, 333], q_sigma=2.0)
     ref = oracle_of(q, k, v, sl, "bf16", 64 ** -0.5)
@@ -97,7 +98,7 @@ def test_attention_consumer_warps(gq, warps):
                        split_mode=smode), ref, f"warps={warps} nsplit={nsplit} split_mode={smode}")
     for D, kd, G in ((128, "bf16", 6), (256, "fp16", 16)):
         q, k, v, sl = attn_case(rng, 2, 700, 2 * G, 2, D, kd, [700, 90], q_sigma=2.0)
-        if warps > 6:
+        if warps > 6 and D == 256:
             with pytest.raises(gq.GqaAvError):
                 run_attn(gq, q, k, v, sl, 1, D ** -0.5, warps=warps)
             continue
