@@ -57,7 +57,7 @@ KERNEL_SOURCES = ["gqa_attention_weighted_gb300/csrc/gqa_av_kernel.cuh",
                   "gqa_attention_weighted_gb300/csrc/gqa_av_api.cu"]
 ENGINES = {"auto": 0, "fma": 1, "tensor": 2}
 SPLIT_MODES = {"auto": 0, "fixed": 1, "balanced": 2}
-KERNEL_NAMES = {1: "gqa_av_kernel", 2: "gqa_av_mma_kernel"}
+KERNEL_NAMES = {1: "gqa_av_kernel", 2: "gqa_av_mma_kernel", 3: "gqa_av_generic_kernel"}
 
 
 def kernel_hash(sources=None) -> str:

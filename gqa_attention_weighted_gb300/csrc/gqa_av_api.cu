@@ -18,6 +18,7 @@
 
 #include "gqa_av.h"
 #define GQA_AV_COMBINE_KERNEL  // the split combine kernel lives in this translation unit
+#include "gqa_av_generic.cuh"
 #include "gqa_av_kernel.cuh"
 #include "gqa_av_mma.cuh"
 
@@ -76,6 +77,7 @@ struct Kernel {
 
 constexpr int kEngineFma = 1;     // CUDA-core packed-FMA kernel
 constexpr int kEngineTensor = 2;  // tcgen05 tensor-core kernel
+constexpr int kEngineGeneric = 3; // any D, element-aligned pointers (plain loads)
 constexpr int kMaxMmaHeads = 64;  // N <= 64: B ring and tensor memory stay small
 
 template <typename Tag>
@@ -187,7 +189,17 @@ struct Plan {
   size_t ws_bytes;  // partials only
 };
 
+int check_shape_any_d(int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode);
+
 int check_shape(int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode) {
+  int rc = check_shape_any_d(B, Cmax, Hq, Hkv, D, v_dtype, mode);
+  if (rc) return rc;
+  if (D % 8 != 0) return fail(GQA_AV_ERR_UNSUPPORTED, "D=%d is not a multiple of 8", D);
+  return GQA_AV_OK;
+}
+
+// The checks that hold for every kernel, the generic one included.
+int check_shape_any_d(int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode) {
   if (B <= 0 || Cmax <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0)
     return fail(GQA_AV_ERR_INVALID, "sizes must be positive (B=%d Cmax=%d Hq=%d Hkv=%d D=%d)", B,
                 Cmax, Hq, Hkv, D);
@@ -197,7 +209,6 @@ int check_shape(int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode) 
     return fail(GQA_AV_ERR_INVALID, "unknown v_dtype %d", v_dtype);
   if (mode != GQA_AV_MODE_AUTO && mode != GQA_AV_MODE_PER_HEAD && mode != GQA_AV_MODE_GQA)
     return fail(GQA_AV_ERR_INVALID, "unknown mode %d", mode);
-  if (D % 8 != 0) return fail(GQA_AV_ERR_UNSUPPORTED, "D=%d is not a multiple of 8", D);
   return GQA_AV_OK;
 }
 
@@ -633,13 +644,101 @@ int current_device(int* dev) {
   return e == cudaSuccess ? GQA_AV_OK : fail_cuda(e, "cudaGetDevice");
 }
 
+// ------------------------------------------------------------ generic path
+struct GenPlan {
+  int mode, heads, hgroups, tiles, cw, row_par, rows_per_split, nsplit;
+  size_t ws_bytes;  // partials only
+};
+
+// Whether a tuning asks for anything (the generic kernel takes none).
+bool tuning_set(const gqa_av_tuning* t) {
+  return t && (t->nsplit || t->dtile || t->rows_per_stage || t->stages || t->early_stages ||
+               t->engine || t->split_mode);
+}
+
+int make_gen_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int mode, GenPlan* p) {
+  DeviceInfo di;
+  int rc = device_info(dev, &di);
+  if (rc) return rc;
+  const int G = Hq / Hkv;
+  p->mode = mode == GQA_AV_MODE_AUTO ? (G > 1 ? GQA_AV_MODE_GQA : GQA_AV_MODE_PER_HEAD) : mode;
+  p->heads = p->mode == GQA_AV_MODE_GQA ? G : 1;
+  p->hgroups = Hq / p->heads;
+  p->tiles = p->hgroups * B;
+  p->cw = D >= kGenThreads ? kGenThreads : (D + 31) / 32 * 32;
+  p->row_par = kGenThreads / p->cw;
+  // About eight CTAs per SM over the tiles (each thread has a few loads in
+  // flight; the kernel waits on memory latency), at least 32 rows a split.
+  long long want = p->tiles < 8 * di.sms ? (8LL * di.sms + p->tiles - 1) / p->tiles : 1;
+  want = std::max<long long>(1, std::min<long long>(want, (Cmax + 31) / 32));
+  p->rows_per_split = static_cast<int>((Cmax + want - 1) / want);
+  p->nsplit = (Cmax + p->rows_per_split - 1) / p->rows_per_split;
+  if (static_cast<long long>(p->tiles) * p->nsplit > 0x7fffffffLL)
+    return fail(GQA_AV_ERR_UNSUPPORTED, "grid too large");
+  p->ws_bytes = p->nsplit > 1
+                    ? static_cast<size_t>(p->tiles) * p->nsplit * p->heads * D * sizeof(float)
+                    : 0;
+  return GQA_AV_OK;
+}
+
+int run_generic(const float* attn, const void* v, const int32_t* seq_lens, float* out, int B,
+                int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode, cudaStream_t stream) {
+  if ((reinterpret_cast<uintptr_t>(attn) | reinterpret_cast<uintptr_t>(out)) & 3)
+    return fail(GQA_AV_ERR_INVALID, "attn and out must be 4-byte aligned (float)");
+  if (reinterpret_cast<uintptr_t>(v) & 1)
+    return fail(GQA_AV_ERR_INVALID, "v_cache must be 2-byte aligned (bf16 / fp16)");
+  int dev, rc;
+  if ((rc = current_device(&dev))) return rc;
+  GenPlan gp;
+  if ((rc = make_gen_plan(dev, B, Cmax, Hq, Hkv, D, mode, &gp))) return rc;
+  Workspace ws;
+  if ((rc = workspace(dev, kHeaderBytes + gp.ws_bytes, stream, &ws))) return rc;
+  GenericParams p;
+  p.attn = attn;
+  p.v = static_cast<const uint16_t*>(v);
+  p.seq_lens = seq_lens;
+  p.out = out;
+  p.ws = reinterpret_cast<float*>(static_cast<char*>(ws.base) + kHeaderBytes);
+  p.B = B; p.Cmax = Cmax; p.Hq = Hq; p.Hkv = Hkv; p.D = D; p.G = Hq / Hkv;
+  p.heads = gp.heads; p.hgroups = gp.hgroups; p.cw = gp.cw; p.row_par = gp.row_par;
+  p.rows_per_split = gp.rows_per_split; p.nsplit = gp.nsplit;
+  const dim3 grid(static_cast<unsigned>(gp.tiles * gp.nsplit));
+  if (v_dtype == GQA_AV_BF16)
+    gqa_av_generic_kernel<Bf16Tag><<<grid, kGenThreads, 0, stream>>>(p);
+  else
+    gqa_av_generic_kernel<Fp16Tag><<<grid, kGenThreads, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_cuda(e, "generic kernel launch");
+  if (gp.nsplit > 1) {
+    const int chunks = (gp.heads * D + kGenCombineOut - 1) / kGenCombineOut;
+    gqa_av_generic_combine<<<gp.tiles * chunks, kGenThreads, 0, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return fail_cuda(e, "generic combine launch");
+  }
+  return GQA_AV_OK;
+}
+
 int run(const float* attn, const void* v, const int32_t* seq_lens, float* out, int B, int Cmax,
         int Hq, int Hkv, int D, int v_dtype, int mode, const gqa_av_tuning* tuning,
         cudaStream_t stream, const int32_t* block_table = nullptr, int block_size = 0,
         int num_blocks = 0, int max_blocks = 0) {
   g_last_error.clear();
-  int rc = check_shape(B, Cmax, Hq, Hkv, D, v_dtype, mode);
+  int rc = check_shape_any_d(B, Cmax, Hq, Hkv, D, v_dtype, mode);
   if (rc) return rc;
+  // Contiguous calls that the TMA kernels cannot take (D % 8 != 0, or attn,
+  // V or out not 16-byte aligned) run the generic kernel.
+  if (!block_table && attn && v && out &&
+      (D % 8 != 0 || ((reinterpret_cast<uintptr_t>(attn) | reinterpret_cast<uintptr_t>(v) |
+                       reinterpret_cast<uintptr_t>(out)) & 15))) {
+    if (tuning_set(tuning))
+      return fail(GQA_AV_ERR_UNSUPPORTED,
+                  "launch-shape tunings apply to the TMA kernels, which need D %% 8 == 0 and "
+                  "16-byte aligned attn, v_cache and out");
+    if (reinterpret_cast<uintptr_t>(seq_lens) & 3)
+      return fail(GQA_AV_ERR_INVALID, "seq_lens must be 4-byte aligned");
+    return run_generic(attn, v, seq_lens, out, B, Cmax, Hq, Hkv, D, v_dtype, mode, stream);
+  }
+  if ((rc = check_shape(B, Cmax, Hq, Hkv, D, v_dtype, mode))) return rc;
   if (block_table) {
     if (block_size <= 0 || block_size % 8 || num_blocks <= 0 || max_blocks <= 0)
       return fail(GQA_AV_ERR_INVALID,
@@ -752,7 +851,32 @@ int gqa_av_plan(int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode,
   g_last_error.clear();
   if (!info) return fail(GQA_AV_ERR_INVALID, "info must be non-NULL");
   int dev, rc;
+  if ((rc = check_shape_any_d(B, Cmax, Hq, Hkv, D, v_dtype, mode))) return rc;
   if ((rc = current_device(&dev))) return rc;
+  if (D % 8 != 0 && !tuning_set(tuning)) {
+    // The generic kernel (the plan cannot see pointers: misaligned ones also
+    // take it, with this launch).
+    GenPlan g;
+    if ((rc = make_gen_plan(dev, B, Cmax, Hq, Hkv, D, mode, &g))) return rc;
+    memset(info, 0, sizeof *info);
+    info->mode = g.mode;
+    info->heads_per_cta = g.heads;
+    info->head_chunk = std::min(g.heads, kGenHeads);
+    info->dtile = g.cw;
+    info->rows_per_stage = g.row_par;
+    info->nsplit = g.nsplit;
+    info->combine_ctas =
+        g.nsplit > 1 ? g.tiles * ((g.heads * D + kGenCombineOut - 1) / kGenCombineOut) : 0;
+    info->rows_per_split = g.rows_per_split;
+    info->tiles = g.tiles;
+    info->ctas = g.tiles * g.nsplit;
+    info->threads_per_cta = kGenThreads;
+    info->engine = kEngineGeneric;
+    info->split_mode = 1;
+    info->smem_bytes = kGenHeads * kGenThreads * 4;
+    info->workspace_bytes = kHeaderBytes + g.ws_bytes;
+    return GQA_AV_OK;
+  }
   Plan p;
   if ((rc = make_plan(dev, B, Cmax, Hq, Hkv, D, v_dtype, mode, tuning, &p))) return rc;
   info->mode = p.mode;

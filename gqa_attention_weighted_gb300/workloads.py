@@ -89,6 +89,9 @@ WORKLOADS: Dict[str, Workload] = {w.name: w for w in [
     # in [C/4, C]): the same 256 tiles and split rule, small enough to profile.
     Workload("ragged_b32_c16384_hq64_hkv8_d128", 32, 16384, 64, 8, 128, "bf16",
              1.0, 2.0, 4096, 16384),
+    # The Llama-style shape with a head dimension of 100 (a multiple of the
+    # page's 4-wide texel, not of 8): the calls the TMA kernels cannot take.
+    Workload("odd_b1_c8192_hq32_hkv8_d100", 1, 8192, 32, 8, 100, "bf16", 1.0, 2.0),
 ]}
 
 # Short aliases, in the order above.
@@ -100,6 +103,7 @@ ALIASES = {
     "large": "large_b32_c131072_hq64_hkv8_d128_ragged",
     "traffic": "traffic_b8_c32768_hq32_hkv8_d128",
     "ragged": "ragged_b32_c16384_hq64_hkv8_d128",
+    "odd": "odd_b1_c8192_hq32_hkv8_d100",
 }
 
 

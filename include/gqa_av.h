@@ -52,7 +52,7 @@ extern "C" {
 /* Status codes. */
 #define GQA_AV_OK                  0
 #define GQA_AV_ERR_INVALID         1 /* NULL pointer, size <= 0, Hq % Hkv != 0, bad mode or dtype */
-#define GQA_AV_ERR_UNSUPPORTED     2 /* D % 8 != 0, pointer not 16-byte aligned, shape too large */
+#define GQA_AV_ERR_UNSUPPORTED     2 /* outside a variant's limits (see each call), shape too large */
 #define GQA_AV_ERR_CUDA            3 /* a CUDA runtime/driver call or a launch failed */
 #define GQA_AV_ERR_NOMEM           4 /* workspace could not be allocated (or not during capture) */
 #define GQA_AV_ERR_DEVICE_TIMEOUT  5 /* a bounded wait inside a kernel ran out (device status word) */
@@ -68,9 +68,14 @@ extern "C" {
 
 /*
  * The reduction. Arguments as in the layouts above; B, Cmax, Hq, Hkv, D > 0,
- * Hq % Hkv == 0, D % 8 == 0; attn, v_cache and out 16-byte aligned.
- * Forcing a mode on a shape it cannot run is an error (never a silent
- * fallback): with Hq % Hkv != 0 every mode returns GQA_AV_ERR_INVALID.
+ * Hq % Hkv == 0; attn and out 4-byte aligned, v_cache 2-byte aligned (their
+ * element types), seq_lens 4-byte aligned. With D % 8 == 0 and attn, v_cache
+ * and out 16-byte aligned the TMA kernels run (the FMA or the tensor-core
+ * engine); any other D or alignment runs the generic kernel (plain loads, any
+ * D >= 1; the page's 4-wide texel granularity and below), with the same
+ * results within the stated gate and the same determinism. Forcing a mode on
+ * a shape it cannot run is an error (never a silent fallback): with
+ * Hq % Hkv != 0 every mode returns GQA_AV_ERR_INVALID.
  */
 int gqa_av_decode(const float *attn, const void *v_cache, const int32_t *seq_lens,
                   float *out, int B, int Cmax, int Hq, int Hkv, int D,
@@ -104,7 +109,11 @@ int gqa_av_decode_per_head(const float *attn, const void *v_cache, const int32_t
  * to its length), 0 lets the library pick (balanced for the tensor-core
  * engine on shapes with at least as many tiles as SMs, else fixed). Results
  * stay within the stated tolerance for every choice, and are bitwise
- * reproducible for a fixed choice and fixed lengths.
+ * reproducible for a fixed choice and fixed lengths. Tunings apply to the TMA
+ * kernels only: a call that would run the generic kernel (D % 8 != 0 or a
+ * pointer not 16-byte aligned) with any field set returns
+ * GQA_AV_ERR_UNSUPPORTED. The paged and no-allocation variants keep the TMA
+ * kernels' limits (D % 8 == 0, 16-byte aligned attn, V and out).
  */
 typedef struct gqa_av_tuning {
     int nsplit;
@@ -144,7 +153,8 @@ typedef struct gqa_av_plan_info {
     int rows_per_stage;
     int stages;
     int early_stages;    /* stages issued before the sequence length is read (0: none) */
-    int engine;          /* 1 CUDA-core packed FMA, 2 tcgen05 tensor cores */
+    int engine;          /* 1 CUDA-core packed FMA, 2 tcgen05 tensor cores, 3 generic
+                            (D % 8 != 0; a call with misaligned pointers also runs it) */
     int split_mode;      /* 1 fixed splits, 2 balanced over the batch's lengths */
     int nsplit;          /* context splits per tile (of a full-length sequence) */
     int combine_ctas;    /* CTAs of the split-combine kernel (0: not launched) */

@@ -62,14 +62,23 @@ FAKE = 1 << 20
     ((FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 8, 0, 3), 1),    # unknown mode
     ((None, FAKE, None, FAKE, 1, 8, 4, 4, 8, 0, -1), 1),   # NULL attn
     ((FAKE, FAKE, None, None, 1, 8, 4, 4, 8, 0, 1), 1),    # NULL out
-    ((FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 12, 0, 1), 2),   # D % 8 != 0
-    ((FAKE + 4, FAKE, None, FAKE, 1, 8, 4, 4, 8, 0, 0), 2),  # misaligned attn
+    ((FAKE, FAKE + 1, None, FAKE, 1, 8, 4, 4, 12, 0, 1), 1),  # v not 2-byte aligned
+    ((FAKE + 2, FAKE, None, FAKE, 1, 8, 4, 4, 8, 0, 0), 1),  # attn not 4-byte aligned
+    ((FAKE, FAKE, None, FAKE + 2, 1, 8, 4, 4, 8, 0, 0), 1),  # out not 4-byte aligned
     ((FAKE, FAKE, FAKE + 2, FAKE, 1, 8, 4, 4, 8, 0, 0), 1),  # misaligned seq_lens
 ])
 def test_host_checks_reject_before_launch(native, args, status):
     rc = native.lib.gqa_av_decode(*args, None)
     assert rc == status, native.gqa_av_last_error()
     assert native.gqa_av_last_error() != ""
+
+
+def test_tunings_need_the_tma_kernels(native):
+    # D % 8 != 0 runs the generic kernel, which takes no launch-shape tuning.
+    t = native.Tuning(3, 0, 0, 0, 0, 0, 0)
+    rc = native.lib.gqa_av_decode_tuned(FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 12, 0, -1,
+                                        ctypes.byref(t), None)
+    assert rc == 2 and "TMA" in native.gqa_av_last_error()
 
 
 def test_per_head_entry_checks(native):
