@@ -477,12 +477,13 @@ def run_gpu_attn(args, rank, world, local):
     scale = w.D ** -0.5
     smode = SPLIT_MODES[args.split_mode]
     plan = gq.gqa_attn_plan(w.B, w.Cmax, w.Hq, w.Hkv, w.D, gq.native.v_dtype_code(x["k"].dtype),
-                            mode, args.attn_warps, args.attn_splits, smode, True)
+                            mode, args.attn_warps, args.attn_splits, smode, True,
+                            args.attn_column_blocks)
 
     def call(st, out):
         gq.gqa_attn_decode(st["q"], st["k"], st["v"], st["seq_lens"], out, mode=mode, scale=scale,
                            consumer_warps=args.attn_warps, nsplit=args.attn_splits,
-                           split_mode=smode)
+                           split_mode=smode, column_blocks=args.attn_column_blocks)
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     set_bytes = sum(t.numel() * t.element_size() for t in x.values()) + w.B * w.Hq * w.D * 4
@@ -830,6 +831,8 @@ def main():
                     help="attn: consumer warps per CTA (0: the library's choice)")
     ap.add_argument("--attn-splits", type=int, default=0,
                     help="attn: context splits per tile (0: the library's choice)")
+    ap.add_argument("--attn-column-blocks", type=int, default=0,
+                    help="attn: output column blocks per head group (0: the library's choice)")
     ap.add_argument("--paged", type=int, default=0, metavar="BLOCK_SIZE",
                     help="run the AV call on a paged copy of V (blocks of this many rows in a "
                          "shuffled pool, gqa_av_decode_paged)")

@@ -84,8 +84,9 @@ def _load() -> ctypes.CDLL:
     lib.gqa_qk_last_error.argtypes = []
     lib.gqa_qk_last_error.restype = ctypes.c_char_p
     lib.gqa_attn_decode.argtypes = [P, P, P, P, P, *sizes, I, ctypes.c_float, I, P]
-    lib.gqa_attn_decode_tuned.argtypes = [P, P, P, P, P, *sizes, I, ctypes.c_float, I, I, I, I, P]
-    lib.gqa_attn_plan.argtypes = [*sizes, I, I, I, I, I, I, ctypes.POINTER(ctypes.c_int), I]
+    lib.gqa_attn_decode_tuned.argtypes = [P, P, P, P, P, *sizes, I, ctypes.c_float, I, I, I, I, I,
+                                          P]
+    lib.gqa_attn_plan.argtypes = [*sizes, I, I, I, I, I, I, I, ctypes.POINTER(ctypes.c_int), I]
     lib.gqa_attn_device_status.argtypes = [P, I]
     lib.gqa_attn_last_error.argtypes = []
     lib.gqa_attn_last_error.restype = ctypes.c_char_p
@@ -305,7 +306,7 @@ def _check_attn(status: int) -> None:
 
 def gqa_attn_decode(q, k_cache, v_cache, seq_lens, out, mode: int = MODE_AUTO, scale=None,
                     stream=None, consumer_warps: int = 0, nsplit: int = 0,
-                    split_mode: int = 0) -> torch.Tensor:
+                    split_mode: int = 0, column_blocks: int = 0) -> torch.Tensor:
     """out[b,q,:] = sum over c < L_b of softmax_c(scale * q[b,q,:] . k_cache[b,c,q//G,:])
     * v_cache[b,c,q//G,:] (scale defaults to 1/sqrt(D)); writes and returns ``out``."""
     if q.dim() != 3 or k_cache.dim() != 4 or v_cache.dim() != 4 or out.dim() != 3:
@@ -330,17 +331,18 @@ def gqa_attn_decode(q, k_cache, v_cache, seq_lens, out, mode: int = MODE_AUTO, s
     _check_attn(lib.gqa_attn_decode_tuned(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens),
                                           _ptr(out), B, Cmax, Hq, Hkv, D, _V_DTYPE[k_cache.dtype],
                                           sc, int(mode), int(consumer_warps), int(nsplit),
-                                          int(split_mode), _stream_handle(stream)))
+                                          int(split_mode), int(column_blocks),
+                                          _stream_handle(stream)))
     return out
 
 
 def gqa_attn_plan(B, Cmax, Hq, Hkv, D, kv_dtype=GQA_AV_BF16, mode=MODE_AUTO, consumer_warps=0,
-                  nsplit=0, split_mode=0, ragged=True) -> dict:
-    info = (ctypes.c_int * 10)()
+                  nsplit=0, split_mode=0, ragged=True, column_blocks=0) -> dict:
+    info = (ctypes.c_int * 11)()
     _check_attn(lib.gqa_attn_plan(B, Cmax, Hq, Hkv, D, kv_dtype, mode, consumer_warps, nsplit,
-                                  split_mode, 1 if ragged else 0, info, 10))
+                                  split_mode, column_blocks, 1 if ragged else 0, info, 11))
     keys = ("mode", "heads_per_cta", "consumer_warps", "stages", "rows_per_split", "nsplit",
-            "tiles", "smem_bytes", "split_mode", "ctas")
+            "tiles", "smem_bytes", "split_mode", "ctas", "column_blocks")
     return dict(zip(keys, list(info)))
 
 

@@ -27,6 +27,11 @@
 //     stage's products made by the tensor core from zero and added to the
 //     fp32 register accumulator with one FMA, so the tensor core never sums
 //     more than one stage. P's fragments are the score fragments themselves.
+// At D = 256 the output columns can be cut into two blocks of 128 owned by
+// two CTAs (each computes all the scores and half of the weighted sum): a
+// thread then holds 64 output sums instead of 128, and the two CTAs, adjacent
+// in the grid, read the same K rows at about the same time (the second read
+// is an L2 hit).
 // Rows past the split or the sequence get score -inf and their V rows are
 // zeroed in shared memory (they may hold NaN). At the end the warps' (m, l,
 // O) are merged through shared memory in warp order; a tile whose context
@@ -64,12 +69,14 @@ struct alignas(64) AttnParams {
   int B, Cmax, Hq, Hkv, D, G;
   int heads;                    // query heads per CTA (<= 16)
   int hgroups;                  // Hq / heads
+  int ncol;                     // column blocks of the output (1, or 2 at D = 256)
+  int kt;                       // tiles of one sequence: hgroups * ncol
   int nw;                       // consumer warps
   int stages;                   // ring slots, a multiple of nw
   int rows_per_split, nsplit;   // fixed splits
   int balanced;                 // splits balanced over the batch's lengths
   int units;                    // balanced: CTAs the batch's context is spread over
-  uint32_t stage_bytes;         // 2 * 32 * D * 2: K rows, then V rows
+  uint32_t stage_bytes;         // 32 * (D + D / ncol) * 2: K rows, then the block's V columns
   uint32_t q_off;               // shared-memory offset of q' hi and lo (16 rows each)
   uint32_t qstride;             // bytes per q' row in shared memory (D * 2 + 16)
   uint32_t bar_off;             // shared-memory offset of the mbarriers and the fail flag
@@ -83,6 +90,7 @@ struct AttnCombineParams {
   float* out;
   int B, Cmax, Hq, D, heads, hgroups, rows_per_split, nsplit;
   int balanced, units;
+  int ncol, kt;                 // column blocks, tiles of one sequence
 };
 
 // ---------------------------------------------------------------------------
@@ -171,12 +179,12 @@ __device__ __forceinline__ float exp2_fast(float x) { return exp2f(x); }
 //   [mbarriers: full, empty (stages each)][fail flag]
 // After the context loop the ring is reused for the warps' merge:
 //   [O: nw x heads x (D + 4) floats][(m, l): nw x heads float2]
-template <typename Tag, int D, int MW>
+template <typename Tag, int D, int DV, int MW>
 __global__ void __launch_bounds__(32 * (MW + 1), 1)
     gqa_attn_kernel(const __grid_constant__ AttnParams p) {
   constexpr int R = kAttnRows;
   constexpr int KS = D / 16;          // 16-column k-steps of the score product
-  constexpr int NT = D / 8;           // 8-column n-tiles of the output
+  constexpr int NT = DV / 8;          // 8-column n-tiles of the CTA's output columns
   constexpr uint32_t kHalf = R * D * 2;  // K bytes of a stage; V follows
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_addr(smem_raw);
@@ -188,21 +196,24 @@ __global__ void __launch_bounds__(32 * (MW + 1), 1)
   const int lane = tid & 31;
   const int nthreads = 32 * (p.nw + 1);
 
-  // Fixed splits: CTA (tile, split), tile = hg * B + b. Balanced splits: CTA u
-  // takes head group u % hgroups and batch split u / hgroups, found from the
-  // lengths after the dependency wait. Either way its partial is slot blockIdx.x.
-  int hg, b, split, c_begin, rps;
+  // A tile is (head group hg, column block cb, b); hgv = hg * ncol + cb.
+  // Fixed splits: CTA (tile, split), tile = hgv * B + b. Balanced splits: CTA
+  // u takes hgv = u % kt and batch split u / kt, found from the lengths after
+  // the dependency wait. Either way its partial is slot blockIdx.x.
+  int hgv, b, split, c_begin, rps;
   if (!p.balanced) {
     const int tile = blockIdx.x / p.nsplit;
     split = blockIdx.x - tile * p.nsplit;
-    hg = tile / p.B;
-    b = tile - hg * p.B;
+    hgv = tile / p.B;
+    b = tile - hgv * p.B;
     rps = p.rows_per_split;
     c_begin = split * rps;
   } else {
-    hg = blockIdx.x % p.hgroups;
+    hgv = blockIdx.x % p.kt;
     b = split = c_begin = rps = 0;
   }
+  const int hg = hgv / p.ncol;
+  const int dv0 = (hgv - hg * p.ncol) * DV;  // first output column of the CTA
   const int h0 = hg * p.heads;
   const int kv_h = h0 / p.G;
   // Fixed splits issue their first stages before the length is read.
@@ -238,8 +249,8 @@ __global__ void __launch_bounds__(32 * (MW + 1), 1)
     nsplit_b = L > 0 ? (L + rps - 1) / rps : 1;
   } else {
     // Warp-collective: every warp works the split out for itself.
-    const int sps = balanced_sps(p.seq_lens, p.B, p.Cmax, R, p.hgroups, p.units);
-    const BalancedSplit bs = balanced_find(p.seq_lens, p.B, p.Cmax, R, sps, blockIdx.x / p.hgroups);
+    const int sps = balanced_sps(p.seq_lens, p.B, p.Cmax, R, p.kt, p.units);
+    const BalancedSplit bs = balanced_find(p.seq_lens, p.B, p.Cmax, R, sps, blockIdx.x / p.kt);
     if (bs.found) {
       b = bs.b;
       L = bs.L;
@@ -265,12 +276,13 @@ __global__ void __launch_bounds__(32 * (MW + 1), 1)
         mbar_arrive_expect_tx(full, p.stage_bytes);
         const uint32_t dst = base_s + (uint32_t)stage * p.stage_bytes;
 #pragma unroll
-        for (int part = 0; part < D / 64; ++part) {
+        for (int part = 0; part < D / 64; ++part)
           tma_load_4d(dst + (uint32_t)part * R * 128, &p.k_map, 64 * part, kv_h, c0, b, full,
                       policy);
-          tma_load_4d(dst + kHalf + (uint32_t)part * R * 128, &p.v_map, 64 * part, kv_h, c0, b,
-                      full, policy);
-        }
+#pragma unroll
+        for (int part = 0; part < DV / 64; ++part)
+          tma_load_4d(dst + kHalf + (uint32_t)part * R * 128, &p.v_map, dv0 + 64 * part, kv_h, c0,
+                      b, full, policy);
       }
     };
     for (int it = 0; it < pre; ++it) issue(it, c_begin + it * R);  // before the length is known
@@ -398,10 +410,10 @@ __global__ void __launch_bounds__(32 * (MW + 1), 1)
           if (r >= nvalid) s[j][0] = s[j][2] = -INFINITY;
           if (r + 1 >= nvalid) s[j][1] = s[j][3] = -INFINITY;
         }
-        const int lines = (R - nvalid) * (D / 64);  // 128-byte lines to clear
+        const int lines = (R - nvalid) * (DV / 64);  // 128-byte lines to clear
         for (int i = lane; i < lines * 8; i += 32) {
           const int line = i >> 3, q16 = i & 7;
-          const int r = nvalid + line / (D / 64), part = line % (D / 64);
+          const int r = nvalid + line / (DV / 64), part = line % (DV / 64);
           *reinterpret_cast<uint4*>(smem + (v_s - base_s) + part * R * 128 + r * 128 + q16 * 16) =
               make_uint4(0u, 0u, 0u, 0u);
         }
@@ -494,7 +506,7 @@ __global__ void __launch_bounds__(32 * (MW + 1), 1)
     // into it (the producer joins after its early stages have landed).
     named_sync(2, nthreads);
     if (*fail) return;
-    const int ostride = D + 4;  // floats; keeps the float2 stores conflict-free
+    const int ostride = DV + 4;  // floats; keeps the float2 stores conflict-free
     float* mo = reinterpret_cast<float*>(smem);
     float2* mml = reinterpret_cast<float2*>(smem + (size_t)p.nw * p.heads * ostride * 4);
     const float inv_gain = 1.0f / gain;
@@ -523,12 +535,12 @@ __global__ void __launch_bounds__(32 * (MW + 1), 1)
   if (split >= nsplit_b) return;  // a split past the sequence: nothing to write
 
   // ---- merge the warps in warp order, then write out or this split's partial.
-  const int ostride = D + 4;
+  const int ostride = DV + 4;
   const float* mo = reinterpret_cast<const float*>(smem);
   const float2* mml = reinterpret_cast<const float2*>(smem + (size_t)p.nw * p.heads * ostride * 4);
-  const int n4 = p.heads * (D / 4);
+  const int n4 = p.heads * (DV / 4);
   for (int i = tid; i < n4; i += nthreads) {
-    const int h = i / (D / 4), d = (i - h * (D / 4)) * 4;
+    const int h = i / (DV / 4), d = (i - h * (DV / 4)) * 4;
     float M = -INFINITY;
     for (int w = 0; w < p.nw; ++w) M = fmaxf(M, mml[w * p.heads + h].x);
     float l = 0.0f;
@@ -547,11 +559,11 @@ __global__ void __launch_bounds__(32 * (MW + 1), 1)
     }
     if (nsplit_b == 1) {
       const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-      *reinterpret_cast<float4*>(p.out + ((size_t)b * p.Hq + h0 + h) * D + d) =
+      *reinterpret_cast<float4*>(p.out + ((size_t)b * p.Hq + h0 + h) * D + dv0 + d) =
           make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     } else {
       const size_t slot = (size_t)blockIdx.x * p.heads + h;
-      __stcg(reinterpret_cast<float4*>(p.ws_o + slot * D + d), acc);
+      __stcg(reinterpret_cast<float4*>(p.ws_o + slot * DV + d), acc);
       if (d == 0) __stcg(p.ws_ml + slot, make_float2(M, l));
     }
   }
@@ -566,7 +578,8 @@ __global__ void __launch_bounds__(32 * (MW + 1), 1)
 // are added in part order, so the result is deterministic. Tiles whose
 // sequence fits one split were written by the main kernel and are skipped.
 // Split s of a tile is slot tile * nsplit + s (fixed splits) or
-// (P_b + s) * hgroups + hg (balanced; P_b = splits of the sequences before b).
+// (P_b + s) * kt + hgv (balanced; P_b = splits of the sequences before b).
+// A tile covers the output columns of its column block.
 __global__ void __launch_bounds__(kAttnCombineThreads)
     gqa_attn_combine_kernel(const __grid_constant__ AttnCombineParams p) {
   constexpr int kBatch = 8;
@@ -574,8 +587,11 @@ __global__ void __launch_bounds__(kAttnCombineThreads)
   __shared__ float4 red[kAttnCombineThreads];                // per-part sums
   const int tile = blockIdx.x / p.heads;
   const int h = blockIdx.x - tile * p.heads;
-  const int hg = tile / p.B;
-  const int b = tile - hg * p.B;
+  const int hgv = tile / p.B;
+  const int b = tile - hgv * p.B;
+  const int hg = hgv / p.ncol;
+  const int DV = p.D / p.ncol;
+  const int dv0 = (hgv - hg * p.ncol) * DV;
   int nsplit_b;
   size_t first, step;  // slot of split s: first + s * step
   if (!p.balanced) {
@@ -584,16 +600,16 @@ __global__ void __launch_bounds__(kAttnCombineThreads)
     first = (size_t)tile * p.nsplit;
     step = 1;
   } else {
-    const int sps = balanced_sps(p.seq_lens, p.B, p.Cmax, kAttnRows, p.hgroups, p.units);
+    const int sps = balanced_sps(p.seq_lens, p.B, p.Cmax, kAttnRows, p.kt, p.units);
     const int2 pn = balanced_prefix(p.seq_lens, p.Cmax, kAttnRows, sps, b);
     nsplit_b = pn.y;
-    first = (size_t)pn.x * p.hgroups + hg;
-    step = p.hgroups;
+    first = (size_t)pn.x * p.kt + hgv;
+    step = p.kt;
   }
   grid_dependency_wait();
   grid_launch_dependents();
   if (nsplit_b <= 1) return;
-  const int cols = p.D / 4;
+  const int cols = DV / 4;
   const int parts = kAttnCombineThreads / cols;
   const int col = threadIdx.x % cols, part = threadIdx.x / cols;
   const int d = 4 * col;
@@ -607,7 +623,7 @@ __global__ void __launch_bounds__(kAttnCombineThreads)
       const int s = s0 + u * parts;
       if (s < nsplit_b) {
         const size_t slot = slot_of(s);
-        x[u] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + slot * p.D + d));
+        x[u] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + slot * DV + d));
         em[u] = __ldcg(p.ws_ml + slot).x;
       }
     }
@@ -647,7 +663,8 @@ __global__ void __launch_bounds__(kAttnCombineThreads)
   __syncthreads();
   if (part == 0) {
     for (int q = 1; q < parts; ++q) add4(acc, red[q * cols + col]);
-    *reinterpret_cast<float4*>(p.out + ((size_t)b * p.Hq + hg * p.heads + h) * p.D + d) = acc;
+    *reinterpret_cast<float4*>(p.out + ((size_t)b * p.Hq + hg * p.heads + h) * p.D + dv0 + d) =
+        acc;
   }
 }
 

@@ -59,27 +59,30 @@ int gqa_attn_decode(const float *q, const void *k_cache, const void *v_cache,
                     const int32_t *seq_lens, float *out, int B, int Cmax, int Hq, int Hkv, int D,
                     int kv_dtype, float scale, int mode, void *stream);
 
-/* The same with the launch shape chosen: consumer_warps (1..8) warps stream
- * the context in each CTA; nsplit is the number of context splits per tile
- * (rounded so each split is a whole number of 32-row stages); split_mode 1
- * cuts each sequence into those fixed splits, 2 spreads the batch's context
- * rows evenly over tiles x nsplit CTAs whatever the lengths (each CTA reads
- * all of seq_lens to find its split). 0 lets the library choose any of
- * them: balanced splits when seq_lens is given and B > 1. Any choice gives
- * results within the stated bounds. */
+/* The same with the launch shape chosen: consumer_warps (1..8; 1..6 at
+ * D = 256) warps stream the context in each CTA; nsplit is the number of
+ * context splits per tile (rounded so each split is a whole number of 32-row
+ * stages); split_mode 1 cuts each sequence into those fixed splits, 2 spreads
+ * the batch's context rows evenly over tiles x nsplit CTAs whatever the
+ * lengths (each CTA reads all of seq_lens to find its split); column_blocks
+ * 1 lets one CTA write all D output columns of its heads, 2 (D = 256 only)
+ * gives each of two CTAs 128 of them (both compute all the scores). 0 lets
+ * the library choose any of them: balanced splits when seq_lens is given and
+ * B > 1, two column blocks at D = 256. Any choice gives results within the
+ * stated bounds. */
 int gqa_attn_decode_tuned(const float *q, const void *k_cache, const void *v_cache,
                           const int32_t *seq_lens, float *out, int B, int Cmax, int Hq, int Hkv,
                           int D, int kv_dtype, float scale, int mode, int consumer_warps,
-                          int nsplit, int split_mode, void *stream);
+                          int nsplit, int split_mode, int column_blocks, void *stream);
 
 /* The launch plan of a call without launching it (ragged != 0: seq_lens will
- * be given): info[0..9] = resolved mode, query heads per CTA, consumer warps,
- * ring stages, rows per fixed split, splits per tile, tiles, dynamic shared
- * memory bytes, split mode (1 fixed, 2 balanced), CTAs launched (the first
- * n_info of them). */
+ * be given): info[0..10] = resolved mode, query heads per CTA, consumer
+ * warps, ring stages, rows per fixed split, splits per tile, tiles, dynamic
+ * shared memory bytes, split mode (1 fixed, 2 balanced), CTAs launched,
+ * column blocks (the first n_info of them). */
 int gqa_attn_plan(int B, int Cmax, int Hq, int Hkv, int D, int kv_dtype, int mode,
-                  int consumer_warps, int nsplit, int split_mode, int ragged, int *info,
-                  int n_info);
+                  int consumer_warps, int nsplit, int split_mode, int column_blocks, int ragged,
+                  int *info, int n_info);
 
 /* Synchronise `stream`, then read the call's device status word (set when a
  * bounded wait inside a kernel runs out): GQA_AV_OK or

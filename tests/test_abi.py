@@ -127,7 +127,8 @@ def test_attention_host_checks_reject_before_launch(native, args, status):
 
 
 def test_attention_tuning_range_checked(native):
-    for warps, splits, smode in ((9, 0, 0), (-1, 0, 0), (0, -2, 0), (0, 0, 3)):
+    for warps, splits, smode, ncol in ((9, 0, 0, 0), (-1, 0, 0, 0), (0, -2, 0, 0), (0, 0, 3, 0),
+                                       (0, 0, 0, -1)):
         rc = native.lib.gqa_attn_decode_tuned(FAKE, FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 64, 0, 1.0,
-                                              -1, warps, splits, smode, None)
+                                              -1, warps, splits, smode, ncol, None)
         assert rc == 1 and b"out of range" in native.lib.gqa_attn_last_error()

@@ -39,13 +39,13 @@ def attn_case(rng, B, C, Hq, Hkv, D, kd, lens, q_sigma=1.0, pad_nan=True):
     return q, k, v, sl
 
 
-def run_attn(gq, q, k, v, sl, mode=-1, scale=None, warps=0, nsplit=0, split_mode=0):
+def run_attn(gq, q, k, v, sl, mode=-1, scale=None, warps=0, nsplit=0, split_mode=0, ncol=0):
     dev = torch.device("cuda")
     B, Hq, D = q.shape
     out = torch.full((B, Hq, D), 7.0, dtype=torch.float32, device=dev)
     gq.gqa_attn_decode(q.to(dev), k.to(dev), v.to(dev), None if sl is None else sl.to(dev), out,
                        mode=mode, scale=scale, consumer_warps=warps, nsplit=nsplit,
-                       split_mode=split_mode)
+                       split_mode=split_mode, column_blocks=ncol)
     gq.gqa_attn_device_status()
     return out.cpu().double().numpy()
 
@@ -79,10 +79,13 @@ def test_attention_shape_sweep(gq, G, D):
         assert np.all(ref[3] == 0.0)
         for mode in (0, 1):
             for nsplit, smode in ((0, 0), (1, 1), (5, 1), (1, 2), (5, 2)):
-                got = run_attn(gq, q, k, v, sl, mode, scale, nsplit=nsplit, split_mode=smode)
-                what = f"G={G} D={D} {kd} mode={mode} nsplit={nsplit} split_mode={smode}"
-                check(got, ref, what)
-                assert np.all(got[3] == 0.0), f"{what}: an empty context must give out = 0"
+                for ncol in ((0, 1, 2) if D == 256 else (0,)):
+                    got = run_attn(gq, q, k, v, sl, mode, scale, nsplit=nsplit, split_mode=smode,
+                                   ncol=ncol)
+                    what = (f"G={G} D={D} {kd} mode={mode} nsplit={nsplit} split_mode={smode} "
+                            f"column_blocks={ncol}")
+                    check(got, ref, what)
+                    assert np.all(got[3] == 0.0), f"{what}: an empty context must give out = 0"
 
 
 @pytest.mark.parametrize("warps", [1, 2, 3, 4, 5, 6, 7, 8])
@@ -104,8 +107,13 @@ def test_attention_consumer_warps(gq, warps):
             continue
         ref = oracle_of(q, k, v, sl, kd, D ** -0.5)
         for nsplit, smode in ((0, 0), (1, 1), (4, 2)):
-            check(run_attn(gq, q, k, v, sl, 1, D ** -0.5, warps=warps, nsplit=nsplit,
-                           split_mode=smode), ref, f"D={D} warps={warps} split_mode={smode}")
+            for ncol in ((1, 2) if D == 256 else (0,)):
+                check(run_attn(gq, q, k, v, sl, 1, D ** -0.5, warps=warps, nsplit=nsplit,
+                               split_mode=smode, ncol=ncol), ref,
+                      f"D={D} warps={warps} split_mode={smode} column_blocks={ncol}")
+    with pytest.raises(gq.GqaAvError):  # two column blocks need D = 256
+        run_attn(gq, q[:, :, :64].contiguous(), k[..., :64].contiguous(), v[..., :64].contiguous(),
+                 sl, ncol=2)
 
 
 def test_attention_balanced_splits_many_sequences(gq):
