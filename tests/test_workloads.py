@@ -56,3 +56,38 @@ def test_compulsory_bytes_of_the_two_dense_shapes():
     assert W.compulsory_bytes(small, [512]) == 149_508
     assert W.compulsory_bytes(llama, [8192]) == 17_842_180
     assert W.flops(llama, [8192]) == 2 * 8192 * 32 * 128
+
+
+@pytest.mark.parametrize("pad", ["zero", "nan"])
+def test_fused_attention_inputs(pad):
+    """generate_qkv: V and lengths as generate() draws them, K of the same
+    shape and type from the next seed with the same padding, q spread like the
+    workload's logits; deterministic."""
+    w = W.custom(3, 80, 8, 2, 16, v_dtype="bf16", logit_sigma=3.0, len_lo=0, len_hi=80)
+    x = W.generate_qkv(w, pad=pad)
+    g = W.generate(w, pad=pad)
+    assert set(x) == {"q", "k", "v", "seq_lens"}
+    assert torch.equal(x["seq_lens"], g["seq_lens"])
+    assert torch.equal(x["v"].view(torch.int16), g["v"].view(torch.int16))
+    assert x["k"].shape == x["v"].shape and x["k"].dtype == x["v"].dtype
+    assert not torch.equal(x["k"].view(torch.int16), x["v"].view(torch.int16))
+    assert x["q"].shape == (3, 8, 16) and x["q"].dtype == torch.float32
+    for b, L in enumerate(x["seq_lens"].tolist()):
+        tail = x["k"][b, L:].float()
+        assert torch.all(tail == 0) if pad == "zero" else torch.all(torch.isnan(tail))
+        assert not torch.isnan(x["k"][b, :L].float()).any()
+    y = W.generate_qkv(w, pad=pad)
+    for k in ("q", "k", "v", "seq_lens"):
+        a, b = x[k], y[k]
+        if a.is_floating_point():
+            a, b = a.view(torch.uint8), b.view(torch.uint8)
+        assert torch.equal(a, b)
+    big = W.generate_qkv(W.custom(1, 2048, 16, 1, 64, logit_sigma=2.0))
+    assert abs(big["q"].std().item() - 2.0) < 0.1
+
+
+def test_fused_attention_compulsory_bytes():
+    llama = W.get("llama")
+    # K and V rows once (2 x 8192 x 8 x 128 x 2 B), q and out (2 x 32 x 128 x 4 B), seq_lens.
+    assert W.attention_compulsory_bytes(llama, [8192]) == 33_587_204
+    assert W.attention_flops(llama, [8192]) == 4 * 8192 * 32 * 128
