@@ -239,3 +239,18 @@ def test_attention_large_batch_sampled(gq):
         ref = oracle_of(q[b:b + 1, heads].cpu(), k[b:b + 1, :L, kv_h:kv_h + 1].cpu(),
                         v[b:b + 1, :L, kv_h:kv_h + 1].cpu(), None, w.v_dtype, w.D ** -0.5)
         check(got[b:b + 1, heads], ref, f"large b={b} kv_h={kv_h}")
+
+
+@pytest.mark.parametrize("D,kd", [(64, "bf16"), (128, "bf16"), (256, "fp16")])
+def test_attention_many_splits(gq, D, kd):
+    """More splits per sequence than a warp has lanes and than one batch of
+    combine loads covers, on fixed and balanced splits."""
+    rng = np.random.default_rng(300 + D)
+    q, k, v, sl = attn_case(rng, 2, 6000, 8, 2, D, kd, [6000, 2500], q_sigma=2.0)
+    ref = oracle_of(q, k, v, sl, kd, D ** -0.5)
+    for nsplit, smode in ((150, 1), (150, 2)):
+        plan = gq.gqa_attn_plan(2, 6000, 8, 2, D, gq.native.v_dtype_code(k.dtype), -1, 0,
+                                nsplit, smode)
+        assert plan["nsplit"] > 64
+        check(run_attn(gq, q, k, v, sl, -1, D ** -0.5, nsplit=nsplit, split_mode=smode), ref,
+              f"D={D} nsplit={nsplit} split_mode={smode}")
