@@ -1,8 +1,11 @@
 """GPU parity of the decode score step (through the C ABI) against its fp64 oracle.
 
-Gate: max|gpu - oracle| <= 1e-4 * max(1, max|oracle|) over the written rows
-(c < L_b); rows c >= L_b must keep the value they had. K rows past a length
-hold NaN, so a kernel that uses an out-of-range row fails.
+Gate (tests/helpers.py, qk_gate): every written probability (c < L_b) within
+1e-4 of the oracle's value relative to that value (plus 1e-12), and every row
+summing to 1 within 1e-5. Softmax probabilities at workload lengths are of
+order 1/L, so an absolute bound would not check them. Rows c >= L_b must keep
+the value they had. K rows past a length hold NaN, so a kernel that uses an
+out-of-range row fails.
 """
 import numpy as np
 import pytest
@@ -10,7 +13,7 @@ import torch
 
 import oracle
 from oracle import gqa_qk
-from helpers import TORCH_V, bits
+from helpers import TORCH_V, bits, qk_gate
 
 pytestmark = pytest.mark.gpu
 
@@ -49,11 +52,9 @@ def run_qk(gq, q, k, sl, mode=-1, scale=None, engine=0):
 
 def check(got, ref, lens, what):
     B, C, _ = got.shape
+    qk_gate(got, ref, lens, what)
     for b in range(B):
         L = max(0, min(int(lens[b]), C)) if lens is not None else C
-        assert np.all(np.isfinite(got[b, :L])), f"{what}: non-finite at b={b}"
-        err = float(np.abs(got[b, :L] - ref[b, :L]).max()) if L else 0.0
-        assert err <= TOL, f"{what}: b={b} max|gpu-oracle| = {err:.3e}"
         assert np.all(got[b, L:] == SENTINEL), f"{what}: rows past L_b={L} were written"
 
 
