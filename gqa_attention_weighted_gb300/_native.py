@@ -69,6 +69,7 @@ def _load() -> ctypes.CDLL:
     lib.gqa_av_decode_paged.argtypes = [P, P, P, P, P, *sizes, I, I, I, I, I,
                                         ctypes.POINTER(Tuning), P]
     lib.gqa_av_plan.argtypes = [*sizes, I, I, ctypes.POINTER(Tuning), ctypes.POINTER(PlanInfo)]
+    lib.gqa_av_selftest_wait_timeout.argtypes = [P, P, P, P, *sizes, I, ctypes.c_longlong, I, P]
     lib.gqa_av_workspace_bytes.argtypes = [*sizes, I, I]
     lib.gqa_av_workspace_bytes.restype = S
     lib.gqa_av_set_workspace.argtypes = [P, S]
@@ -93,7 +94,7 @@ def _load() -> ctypes.CDLL:
     for f in ("gqa_attn_decode", "gqa_attn_decode_tuned", "gqa_attn_plan", "gqa_attn_device_status"):
         getattr(lib, f).restype = I
     for f in ("gqa_av_decode", "gqa_av_decode_per_head", "gqa_av_decode_tuned", "gqa_av_decode_paged",
-              "gqa_av_decode_noalloc", "gqa_av_plan",
+              "gqa_av_decode_noalloc", "gqa_av_plan", "gqa_av_selftest_wait_timeout",
               "gqa_av_set_workspace", "gqa_av_device_status", "gqa_av_version",
               "gqa_qk_softmax_decode", "gqa_qk_softmax_decode_tuned", "gqa_qk_device_status"):
         getattr(lib, f).restype = I

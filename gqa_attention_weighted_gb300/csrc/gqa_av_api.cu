@@ -501,6 +501,8 @@ void fill_params(Params* p, const Plan& pl, const float* attn, const int32_t* se
   p->a_stage_bytes = static_cast<uint32_t>(pl.R) * pl.ap * 4;
   p->v_stage_bytes = pl.v_stage_bytes; p->a_off = pl.a_off; p->bar_off = pl.bar_off;
   p->timeout_ns = kWaitTimeoutNs;
+  p->full_wait_ns = kWaitTimeoutNs;
+  p->withhold_last = 0;
   p->v_halves = pl.v_halves; p->b_off = pl.b_off; p->tmem_cols = static_cast<uint32_t>(pl.tmem_cols);
   p->cvt_warps = pl.cvt_warps;
   p->split_units = pl.split_units;
@@ -537,6 +539,9 @@ struct Workspace {
   bool user = false;
 };
 std::map<int, Workspace> g_ws;
+// Device -> status word of the no-allocation call's fixed array (registered
+// by that call's per-device set-up).
+std::map<int, void*> g_noalloc_status;
 
 // Returns the workspace of `dev` with at least `need` bytes; grows outside capture.
 int workspace(int dev, size_t need, cudaStream_t stream, Workspace* out) {
@@ -937,22 +942,30 @@ int gqa_av_device_status(void* stream, int clear) {
   if ((rc = current_device(&dev))) return rc;
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
-  Workspace w;
+  // The workspace's word and, once the no-allocation call has run on this
+  // device, the word in its fixed array.
+  void* words[2] = {nullptr, nullptr};
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    w = g_ws[dev];
+    words[0] = g_ws[dev].base;
+    auto it = g_noalloc_status.find(dev);
+    if (it != g_noalloc_status.end()) words[1] = it->second;
   }
-  if (!w.base) return GQA_AV_OK;
-  unsigned word = 0;
-  e = cudaMemcpy(&word, w.base, sizeof word, cudaMemcpyDeviceToHost);
-  if (e != cudaSuccess) return fail_cuda(e, "reading the device status word");
-  if (clear && word) {
-    e = cudaMemset(w.base, 0, kHeaderBytes);
-    if (e == cudaSuccess) e = cudaDeviceSynchronize();
-    if (e != cudaSuccess) return fail_cuda(e, "clearing the device status word");
+  unsigned any = 0;
+  for (void* w : words) {
+    if (!w) continue;
+    unsigned word = 0;
+    e = cudaMemcpy(&word, w, sizeof word, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return fail_cuda(e, "reading the device status word");
+    if (clear && word) {
+      e = cudaMemset(w, 0, sizeof word);
+      if (e == cudaSuccess) e = cudaDeviceSynchronize();
+      if (e != cudaSuccess) return fail_cuda(e, "clearing the device status word");
+    }
+    any |= word;
   }
-  if (word)
-    return fail(GQA_AV_ERR_DEVICE_TIMEOUT, "a bounded wait ran out on the device (status 0x%x)", word);
+  if (any)
+    return fail(GQA_AV_ERR_DEVICE_TIMEOUT, "a bounded wait ran out on the device (status 0x%x)", any);
   return GQA_AV_OK;
 }
 
@@ -983,10 +996,15 @@ namespace gqa_av {
 
 int record_error(int status, const char* msg) { return fail(status, "%s", msg); }
 
+void register_noalloc_status(int dev, void* status_word) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_noalloc_status[dev] = status_word;
+}
+
 // One call of the reduction in the default launch shape, with the status
 // word and split partials placed in caller-given device scratch laid out as
-// [status_bytes][partials]. Clears the status word on `stream` before the
-// launch; allocates nothing.
+// [status_bytes][partials]. Leaves the status word as it is (only
+// gqa_av_device_status clears it); allocates nothing.
 int run_in_scratch(const float* attn, const void* v, const int32_t* seq_lens, float* out, int B,
                    int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode, cudaStream_t stream,
                    void* scratch, size_t status_bytes, size_t scratch_bytes) {
@@ -1010,8 +1028,7 @@ int run_in_scratch(const float* attn, const void* v, const int32_t* seq_lens, fl
                 "holds %zu B (use gqa_av_decode)",
                 pl.ws_bytes, partial_cap);
   char* base = static_cast<char*>(scratch);
-  cudaError_t e = cudaMemsetAsync(base, 0, status_bytes, stream);
-  if (e != cudaSuccess) return fail_cuda(e, "clearing the no-allocation scratch");
+  cudaError_t e;
 
   Params p;
   memset(&p, 0, sizeof p);
@@ -1026,4 +1043,83 @@ int run_in_scratch(const float* attn, const void* v, const int32_t* seq_lens, fl
   return GQA_AV_OK;
 }
 
+int noalloc_scratch(int dev, void** ptr, size_t* status_bytes, size_t* bytes);  // gqa_av_noalloc.cu
+
+// Self-test of the failure path: the FMA kernel in its default launch shape
+// for this call, with the producer withholding every full split's last stage
+// (nothing of it is ever issued, so no copy is in flight when the CTA leaves)
+// and the consumers' wait for a stage bounded by `wait_ns`. The consumers'
+// wait for the withheld stage runs out: they set the status word (in the
+// workspace, or in the no-allocation call's fixed array) and return through
+// the same barriers as on any other timeout. `out` is left unspecified.
+int selftest_wait_timeout(const float* attn, const void* v, const int32_t* seq_lens, float* out,
+                          int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, long long wait_ns,
+                          int scratch_kind, cudaStream_t stream) {
+  g_last_error.clear();
+  int rc = check_shape(B, Cmax, Hq, Hkv, D, v_dtype, GQA_AV_MODE_AUTO);
+  if (rc) return rc;
+  if (!attn || !v || !out) return fail(GQA_AV_ERR_INVALID, "attn, v_cache and out must be non-NULL");
+  if ((reinterpret_cast<uintptr_t>(attn) | reinterpret_cast<uintptr_t>(v) |
+       reinterpret_cast<uintptr_t>(out)) & 15)
+    return fail(GQA_AV_ERR_UNSUPPORTED, "attn, v_cache and out must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(seq_lens) & 3)
+    return fail(GQA_AV_ERR_INVALID, "seq_lens must be 4-byte aligned");
+  if (wait_ns < 1000 || wait_ns > kWaitTimeoutNs)
+    return fail(GQA_AV_ERR_INVALID, "wait_ns=%lld must be in [1000, %lld]", wait_ns,
+                kWaitTimeoutNs);
+  if (scratch_kind != 0 && scratch_kind != 1)
+    return fail(GQA_AV_ERR_INVALID, "scratch=%d must be 0 (workspace) or 1 (fixed array)",
+                scratch_kind);
+  int dev;
+  if ((rc = current_device(&dev))) return rc;
+  gqa_av_tuning t;
+  memset(&t, 0, sizeof t);
+  t.engine = kEngineFma;
+  Plan pl;
+  if ((rc = make_plan(dev, B, Cmax, Hq, Hkv, D, v_dtype, GQA_AV_MODE_AUTO, &t, &pl))) return rc;
+  // Every full split must have a stage after the one issued before the length
+  // is read, or nothing would be withheld.
+  if (pl.early != 1 || pl.rows_per_split < 2 * pl.R)
+    return fail(GQA_AV_ERR_UNSUPPORTED,
+                "self-test needs splits of at least two stages (rows_per_split %d, R %d)",
+                pl.rows_per_split, pl.R);
+  char* base = nullptr;
+  size_t status_bytes = kHeaderBytes;
+  if (scratch_kind == 1) {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+    if ((rc = noalloc_scratch(dev, &ptr, &status_bytes, &bytes))) return rc;
+    if (pl.ws_bytes > bytes - status_bytes)
+      return fail(GQA_AV_ERR_UNSUPPORTED, "self-test shape needs %zu B of split partials",
+                  pl.ws_bytes);
+    base = static_cast<char*>(ptr);
+  } else {
+    Workspace ws;
+    if ((rc = workspace(dev, kHeaderBytes + pl.ws_bytes, stream, &ws))) return rc;
+    base = static_cast<char*>(ws.base);
+  }
+  Params p;
+  memset(&p, 0, sizeof p);
+  if ((rc = encode_v_map(&p.v_map, v, B, Cmax, Hkv, D, pl.dt, pl.R, false))) return rc;
+  fill_params(&p, pl, attn, seq_lens, out, base, base + status_bytes, B, Cmax, Hq, Hkv, D);
+  if (p.attn_tma && (rc = encode_attn_map(&p.a_map, attn, B, Cmax, Hq, pl.ap, pl.R))) return rc;
+  p.full_wait_ns = wait_ns;
+  p.withhold_last = 1;
+  Kernel kern;
+  if (!pick_kernel(v_dtype, pl.engine, kernel_sel(pl), &kern))
+    return fail(GQA_AV_ERR_UNSUPPORTED, "no kernel");
+  cudaError_t e = launch_call(kern, pl, p, stream);
+  if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
+  return GQA_AV_OK;
+}
+
 }  // namespace gqa_av
+
+extern "C" int gqa_av_selftest_wait_timeout(const float* attn, const void* v_cache,
+                                            const int32_t* seq_lens, float* out, int B, int Cmax,
+                                            int Hq, int Hkv, int D, int v_dtype,
+                                            long long wait_ns, int scratch, void* stream) {
+  return gqa_av::selftest_wait_timeout(attn, v_cache, seq_lens, out, B, Cmax, Hq, Hkv, D,
+                                       v_dtype, wait_ns, scratch,
+                                       static_cast<cudaStream_t>(stream));
+}

@@ -85,7 +85,11 @@ struct alignas(64) Params {
   uint32_t a_off;               // shared-memory offset of the attn ring
   uint32_t bar_off;             // shared-memory offset of the mbarriers
   int early_stages;             // stages issued before the sequence length is read (>= 1)
-  long long timeout_ns;         // bound on every mbarrier wait
+  long long timeout_ns;         // bound on every mbarrier wait but the one below
+  long long full_wait_ns;       // FMA kernel: bound on the consumers' waits for a stage
+  int withhold_last;            // self-test of the failure path (FMA kernel): the producer
+                                // issues no copy for a split's last stage, so the
+                                // consumers' wait for it runs out (0 in every normal call)
   // Tensor-core kernel only.
   int v_halves;                 // 64-column V boxes per stage (1 or 2)
   uint32_t b_off;               // shared-memory offset of the B (weights) ring
@@ -264,10 +268,12 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-// Named barrier of the consumer warps only (the producer warp does not join).
+// Named barrier 1 of the consumer warps only (the producer warp does not
+// join). Reconverges the warp first (named_sync): on the path where a bounded
+// wait ran out, lanes leave their wait loops at different times.
 template <int kConsumerThreads>
 __device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+  named_sync(1, kConsumerThreads);
 }
 
 // ---------------------------------------------------------------------------
@@ -582,6 +588,9 @@ gqa_av_kernel(const __grid_constant__ Params p) {
     int issued = pre;
     bool ok = true;
     for (int it = pre; it < n_iters; ++it) {
+      // Self-test: the last stage is never issued (nothing of it is in flight),
+      // so the consumers' bounded wait for it runs out.
+      if (p.withhold_last && it == n_iters - 1) break;
       const int stage = it % p.stages;
       const uint32_t parity = ((it / p.stages) & 1) ^ 1;
       if (!mbar_wait(empty0 + 8 * stage, parity, p.timeout_ns)) {
@@ -631,7 +640,7 @@ gqa_av_kernel(const __grid_constant__ Params p) {
   bool ok = true;
   for (int it = 0; it < n_stages; ++it) {
     const int stage = it % p.stages;
-    if (!mbar_wait(full0 + 8 * stage, (it / p.stages) & 1, p.timeout_ns)) {
+    if (!mbar_wait(full0 + 8 * stage, (it / p.stages) & 1, p.full_wait_ns)) {
       atomicOr(p.status, kErrFullWait);
       ok = false;
       break;

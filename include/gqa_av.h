@@ -24,9 +24,25 @@
  * Entries at c >= L_b are never used. Values outside [0, Cmax] in seq_lens
  * are clamped to that range on the device.
  *
- * Numerics: products and sums in fp32 (bf16/fp16 -> fp32 widening is exact),
- * context splits combined in a fixed order, so repeated calls with the same
- * shape give bitwise-identical out.
+ * Numerics. V is widened exactly (bf16/fp16 -> fp32); which arithmetic runs
+ * depends on the kernel the plan picks (gqa_av_plan_info.engine):
+ *   - CUDA-core FMA kernel (engine 1: the default for D % 8 == 0 calls with
+ *     fewer than 8 heads per CTA that stream fewer than 2^18 tile rows) and
+ *     the generic kernel (engine 3: D % 8 != 0 or misaligned pointers):
+ *     fp32 products and sums, every multiply-add rounded like fmaf.
+ *   - tcgen05 tensor-core kernel (engine 2: the default where it applies --
+ *     head groups of at most 64 heads, D >= 64 with D <= 128 or D % 128 == 0
+ *     -- and the CTA has 8 or more heads or the call streams 2^18 tile rows
+ *     or more): each fp32 weight w is split into two 16-bit values of V's
+ *     type, hi = round(w) and lo = round(w - hi) (fp16 weights scaled by 2^12
+ *     first, exactly, and unscaled at the end), so the weights keep about 16
+ *     (bf16) or 22 (fp16) significant bits; V x hi and V x lo are exact in
+ *     fp32; the tensor core accumulates them in fp32 over one pipeline stage
+ *     (at most R / 16 products a value), and stages are added in fp32
+ *     registers.
+ * Both stay within max|out - exact| <= 1e-4 * max(1, max|exact|) on the
+ * tested workloads. Context splits are combined in a fixed order, so repeated
+ * calls with the same shape and lengths give bitwise-identical out.
  *
  * Execution: every call is asynchronous on `stream` (a cudaStream_t; NULL is
  * the legacy default stream) and performs no host synchronisation. Calls
@@ -184,9 +200,13 @@ size_t gqa_av_workspace_bytes(int B, int Cmax, int Hq, int Hkv, int D, int v_dty
 int gqa_av_set_workspace(void *ptr, size_t bytes);
 
 /*
- * Synchronise `stream`, then read the current device's status word, which
- * kernels set when a bounded wait runs out. Returns GQA_AV_OK or
- * GQA_AV_ERR_DEVICE_TIMEOUT; with clear != 0 the word is reset.
+ * Synchronise `stream`, then read the current device's status words, which
+ * kernels set when a bounded wait runs out: the one in the workspace of
+ * gqa_av_decode and its variants, and the one in the fixed array of
+ * gqa_av_decode_noalloc (once that call has run on the device). A word stays
+ * set until it is cleared here, so a timeout in any earlier call is reported.
+ * Returns GQA_AV_OK or GQA_AV_ERR_DEVICE_TIMEOUT; with clear != 0 both words
+ * are reset.
  */
 int gqa_av_device_status(void *stream, int clear);
 
@@ -197,25 +217,49 @@ int gqa_av_device_status(void *stream, int clear);
  * critical loops that must not risk the implicit synchronisation of
  * cudaMalloc/cudaFree, processes with a fixed up-front memory budget.
  *
- * Same arguments, layouts, launch shape and results as gqa_av_decode, but the
- * scratch it needs (status word, split partials) lives in one
- * fixed array of GQA_AV_NOALLOC_SCRATCH_BYTES in this library's device
- * globals, held on every GPU that loads the library until the process exits.
- * No call allocates or frees memory. Set-up: the first call on each device
- * looks up that array's device address (cudaGetSymbolAddress), so make that
- * first call before any stream capture. A shape whose split partials need more
- * than the array holds (8 MiB less its 256-byte status word) is rejected with
- * GQA_AV_ERR_UNSUPPORTED and a message; gqa_av_decode handles it. All calls on
- * a device share the array, which keeps the last call's contents: each call
- * clears the status word on its stream, and every partial is written before
- * it is read. Calls that may overlap on the GPU (unordered streams) race on
- * the array and must not be issued.
+ * Same arguments, layouts, launch shape and results as gqa_av_decode on the
+ * calls the TMA kernels take: D % 8 == 0 and 16-byte aligned attn, v_cache
+ * and out (anything else returns GQA_AV_ERR_UNSUPPORTED; gqa_av_decode runs
+ * it on the generic kernel). The scratch it needs (status word, split
+ * partials) lives in one fixed array of GQA_AV_NOALLOC_SCRATCH_BYTES in this
+ * library's device globals, held on every GPU that loads the library until
+ * the process exits. No call allocates or frees memory. Set-up: the first
+ * call on each device looks up that array's device address
+ * (cudaGetSymbolAddress) and zeroes its status word (synchronously), so make
+ * that first call before any stream capture. A shape whose split partials
+ * need more than the array holds (8 MiB less its 256-byte status word) is
+ * rejected with GQA_AV_ERR_UNSUPPORTED and a message; gqa_av_decode handles
+ * it. All calls on a device share the array, which keeps the last call's
+ * contents: every partial is written before it is read, and the status word
+ * stays set until gqa_av_device_status reads and clears it (that call reports
+ * this array's word together with gqa_av_decode's). Calls that may overlap on
+ * the GPU (unordered streams) race on the array and must not be issued.
  */
 #define GQA_AV_NOALLOC_SCRATCH_BYTES (8u << 20) /* 8 MiB */
 
 int gqa_av_decode_noalloc(const float *attn, const void *v_cache, const int32_t *seq_lens,
                           float *out, int B, int Cmax, int Hq, int Hkv, int D,
                           int v_dtype, int mode, void *stream);
+
+/*
+ * Self-test of the failure path (the pages have no counterpart: it checks
+ * this library's bounded waits). Runs the CUDA-core FMA kernel on the given
+ * call (same arguments and limits as gqa_av_decode's TMA kernels, mode auto)
+ * with the producer withholding the last pipeline stage of every context
+ * split of at least two stages -- nothing of that stage is ever issued, so no
+ * copy is in flight when a CTA leaves -- and the consumers' wait for a stage
+ * bounded by wait_ns (1 us to 2 s) instead of 2 s. Their wait for the
+ * withheld stage runs out, they set the device status word and leave through
+ * the same barriers as on any timeout; no GPU fault, trap or hang is caused.
+ * scratch 0 puts the status word and partials in gqa_av_decode's workspace,
+ * 1 in gqa_av_decode_noalloc's fixed array. Returns GQA_AV_OK once launched;
+ * gqa_av_device_status then reports GQA_AV_ERR_DEVICE_TIMEOUT. `out` is left
+ * unspecified. GQA_AV_ERR_UNSUPPORTED when the call's splits are shorter than
+ * two stages.
+ */
+int gqa_av_selftest_wait_timeout(const float *attn, const void *v_cache, const int32_t *seq_lens,
+                                 float *out, int B, int Cmax, int Hq, int Hkv, int D,
+                                 int v_dtype, long long wait_ns, int scratch, void *stream);
 
 /* Name of a status code; never NULL. */
 const char *gqa_av_status_string(int status);

@@ -132,3 +132,15 @@ def test_attention_tuning_range_checked(native):
         rc = native.lib.gqa_attn_decode_tuned(FAKE, FAKE, FAKE, None, FAKE, 1, 8, 4, 4, 64, 0, 1.0,
                                               -1, warps, splits, smode, ncol, None)
         assert rc == 1 and b"out of range" in native.lib.gqa_attn_last_error()
+
+
+@pytest.mark.parametrize("wait_ns,scratch,D,status", [
+    (10, 0, 64, 1),              # wait limit below 1 us
+    (3_000_000_000, 0, 64, 1),   # above the 2 s every other wait has
+    (200_000, 2, 64, 1),         # unknown scratch
+    (200_000, 0, 12, 2),         # the self-test runs the TMA kernels only (D % 8 == 0)
+])
+def test_wait_timeout_selftest_checks_arguments(native, wait_ns, scratch, D, status):
+    rc = native.lib.gqa_av_selftest_wait_timeout(FAKE, FAKE, None, FAKE, 1, 64, 8, 2, D, 0,
+                                                 wait_ns, scratch, None)
+    assert rc == status, native.gqa_av_last_error()

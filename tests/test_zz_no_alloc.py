@@ -2,11 +2,12 @@
 device memory (engine plug-ins whose host owns all device memory, loops that
 must not risk an allocation's implicit synchronisation, fixed memory budgets).
 
-It is called through the C ABI and must match gqa_av_decode, the allocating
-entry point, within the parity tolerance on two calls in a row (the second
-with different inputs, so stale scratch contents would show). This file is
-collected last so a stop-at-first-failure run has already run everything else;
-it also passes on its own in a fresh process.
+It is called through the C ABI and must match the fp64 oracle, and gqa_av_decode
+(the allocating entry point), within the parity tolerance on two calls in a row
+(the second with different inputs, so stale scratch contents would show). Its
+status word must be reported by gqa_av_device_status. This file is collected
+last so a stop-at-first-failure run has already run everything else; it also
+passes on its own in a fresh process.
 """
 import ctypes
 
@@ -14,7 +15,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from gqa_attention_weighted_gb300 import workloads as W
+from helpers import bits
 
 pytestmark = pytest.mark.gpu
 
@@ -31,7 +34,9 @@ def native():
 
 def _inputs(w, seed):
     x = W.generate(w, "cpu", pad="nan", seed=seed)
-    return {k: t.cuda() for k, t in x.items()}
+    ref = oracle.gqa_av(x["attn"].numpy(), bits(x["v"]), w.v_dtype, x["seq_lens"].numpy(),
+                        nthreads=oracle.host_cores())
+    return {k: t.cuda() for k, t in x.items()}, ref
 
 
 def _call_noalloc(native, x, out, w, mode):
@@ -53,17 +58,20 @@ SHAPES = [
 @pytest.mark.parametrize("mode", [-1, 0])
 def test_noalloc_matches_allocating_entry_point(native, w, mode):
     for seed in (11, 12):  # two calls in a row, different inputs
-        x = _inputs(w, seed)
+        x, exact = _inputs(w, seed)
         ref = torch.empty((w.B, w.Hq, w.D), device="cuda")
         native.gqa_av_decode(x["attn"], x["v"], x["seq_lens"], ref, mode=mode)
         out = torch.full((w.B, w.Hq, w.D), float("nan"), device="cuda")
         rc = _call_noalloc(native, x, out, w, mode)
         assert rc == 0, native.gqa_av_last_error()
         torch.cuda.synchronize()
+        assert native.lib.gqa_av_device_status(None, 0) == 0, "a bounded wait ran out"
         r, o = ref.double().cpu().numpy(), out.double().cpu().numpy()
-        tol = TOL * max(1.0, float(np.abs(r).max()))
+        tol = TOL * max(1.0, float(np.abs(exact).max()))
         assert np.all(np.isfinite(o))
-        assert float(np.abs(o - r).max()) <= tol
+        assert float(np.abs(o - exact).max()) <= tol, "no-allocation call vs the oracle"
+        assert float(np.abs(r - exact).max()) <= tol, "gqa_av_decode vs the oracle"
+        assert float(np.abs(o - r).max()) <= tol, "no-allocation call vs gqa_av_decode"
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(native):
