@@ -940,11 +940,11 @@ def run_e2e(gq, w, x, call, dev, args, world):
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_host.numel() * 4
     steps = max(1, min(args.e2e_steps, args.steps))
-    # Chunks of at most 256 MB, dealt to the copy streams in turn.
+    # Chunks of at most 1 GiB, dealt to the copy streams in turn.
     chunks = []
     for k, h in host.items():
         hf, df = h.view(-1), dbuf[k].view(-1)
-        per = max(1, (256 << 20) // h.element_size())
+        per = max(1, (1 << 30) // h.element_size())
         for i in range(0, hf.numel(), per):
             chunks.append((df[i:i + per], hf[i:i + per]))
 

@@ -21,6 +21,7 @@
 #include "gqa_av_generic.cuh"
 #include "gqa_av_kernel.cuh"
 #include "gqa_av_mma.cuh"
+#include "gqa_av_stream.cuh"
 
 namespace gqa_av {
 
@@ -41,6 +42,14 @@ GQA_AV_DECLARE_ALL(Fp16Tag)
   GQA_AV_DECLARE_MMA(TAG, 1) GQA_AV_DECLARE_MMA(TAG, 2) GQA_AV_DECLARE_MMA(TAG, 3) GQA_AV_DECLARE_MMA(TAG, 4)
 GQA_AV_DECLARE_MMA_ALL(Bf16Tag)
 GQA_AV_DECLARE_MMA_ALL(Fp16Tag)
+#define GQA_AV_DECLARE_STREAM(TAG, NB)                                                      \
+  extern template cudaError_t launch_stream<TAG, NB>(const Params&, int, int, cudaStream_t); \
+  extern template cudaError_t occupancy_stream<TAG, NB>(int, int, int*);
+#define GQA_AV_DECLARE_STREAM_ALL(TAG)                                                    \
+  GQA_AV_DECLARE_STREAM(TAG, 1) GQA_AV_DECLARE_STREAM(TAG, 2) GQA_AV_DECLARE_STREAM(TAG, 3) \
+  GQA_AV_DECLARE_STREAM(TAG, 4)
+GQA_AV_DECLARE_STREAM_ALL(Bf16Tag)
+GQA_AV_DECLARE_STREAM_ALL(Fp16Tag)
 
 namespace {
 
@@ -92,6 +101,17 @@ bool pick_mma(int nb, Kernel* k) {
 }
 
 template <typename Tag>
+bool pick_stream(int nb, Kernel* k) {
+  switch (nb) {
+    case 1: *k = {launch_stream<Tag, 1>, occupancy_stream<Tag, 1>}; return true;
+    case 2: *k = {launch_stream<Tag, 2>, occupancy_stream<Tag, 2>}; return true;
+    case 3: *k = {launch_stream<Tag, 3>, occupancy_stream<Tag, 3>}; return true;
+    case 4: *k = {launch_stream<Tag, 4>, occupancy_stream<Tag, 4>}; return true;
+    default: return false;
+  }
+}
+
+template <typename Tag>
 bool pick(int gc, Kernel* k) {
   switch (gc) {
 #define GQA_AV_CASE(GC)                          \
@@ -106,8 +126,13 @@ bool pick(int gc, Kernel* k) {
   }
 }
 
-// `sel` is the head chunk (FMA kernel) or N / 16 (tensor-core kernel).
+// `sel` is the head chunk (FMA kernel) or N / 16 (tensor-core kernels);
+// kEngineStream is the streamed tensor-core kernel.
+constexpr int kEngineStream = 4;
+
 bool pick_kernel(int v_dtype, int engine, int sel, Kernel* k) {
+  if (engine == kEngineStream)
+    return v_dtype == GQA_AV_BF16 ? pick_stream<Bf16Tag>(sel, k) : pick_stream<Fp16Tag>(sel, k);
   if (engine == kEngineTensor)
     return v_dtype == GQA_AV_BF16 ? pick_mma<Bf16Tag>(sel, k) : pick_mma<Fp16Tag>(sel, k);
   return v_dtype == GQA_AV_BF16 ? pick<Bf16Tag>(sel, k) : pick<Fp16Tag>(sel, k);
@@ -175,6 +200,8 @@ struct Plan {
   int grid;                                // CTAs of the main kernel
   int split_units;                         // tensor core: CTAs the context is balanced over
   int balanced;                            // tensor core: splits balanced over the batch's lengths
+  int stream;                              // tensor core: the streamed kernel (split_mode 3)
+  uint32_t lens_off;                       // streamed kernel: shared-memory offset of the lengths
   int chunk_rows;                          // rows per V box (R, or a paged block)
   int one_per_sm;                          // shared memory padded so one CTA fits per SM
   int early;                               // stages issued before the length is read
@@ -215,6 +242,10 @@ int check_shape_any_d(int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int 
 // Kernel instantiation of a plan: head chunk (FMA) or N / 16 (tensor core).
 int kernel_sel(const Plan& p) { return p.engine == kEngineTensor ? p.nmma / 16 : p.gc; }
 
+// The engine code of the kernel that runs a plan (the streamed kernel is a
+// schedule of the tensor-core engine).
+int kernel_engine(const Plan& p) { return p.stream ? kEngineStream : p.engine; }
+
 // Shared memory of a tensor-core plan, from a 1024-byte-aligned base (1 KiB of
 // slack lets the kernel align the dynamic allocation): [V ring, stages x R x
 // 256 B] [attn ring] [B ring, stages x (hi, lo) x N x R x 2 B] [mbarriers,
@@ -240,6 +271,109 @@ void layout(Plan* p, int min_smem = 0) {
   const size_t aring = static_cast<size_t>(p->stages) * p->R * p->ap * 4;
   p->bar_off = static_cast<uint32_t>(align_up(p->a_off + aring, 16));
   p->smem = std::max(static_cast<int>(p->bar_off + 2 * kMaxStages * 8 + 16), min_smem);
+}
+
+// attn weights of a stage. By TMA when attn rows are 16-byte multiples
+// (Hq % 4 == 0): the box starts at the 4-aligned head at or below the CTA's
+// first head (a TMA box must start 16-byte aligned) and is wide enough for
+// every CTA's heads; otherwise by cp.async, `avec` floats a copy.
+void attn_layout(Plan* p, int Hq) {
+  const int max_off = p->heads % 4 == 0 ? 0 : (p->heads % 2 == 0 ? 2 : 3);
+  const int aw = static_cast<int>(align_up(p->heads + max_off, 4));
+  p->attn_tma = Hq % 4 == 0 && aw <= 256;
+  p->ap = p->attn_tma ? aw : static_cast<int>(align_up(p->heads, 4));
+  p->avec = 1;
+  if (Hq % 4 == 0 && p->heads % 4 == 0) p->avec = 4;
+  else if (Hq % 2 == 0 && p->heads % 2 == 0) p->avec = 2;
+}
+
+// Split-combine launch shape: `parts` threads per float4 column (a power of
+// two <= 16), as many as keep its grid within about one CTA per SM. Its CTAs
+// are small enough to start next to the main kernel's while that runs, so
+// they are all waiting when the partials are complete (measured faster than
+// a grid that only starts as the main kernel's CTAs leave).
+void combine_layout(Plan* p, int sms) {
+  const int ncol4 = p->heads * p->dt / 4;
+  const long long cols = static_cast<long long>(p->tiles) * ncol4;
+  p->parts = 1;
+  while (p->parts < 16 && (p->balanced || p->stream || p->parts < p->nsplit) &&
+         cols * p->parts * 2 <= static_cast<long long>(sms) * kCombineThreads)
+    p->parts *= 2;
+  p->cols_per_cta = kCombineThreads / p->parts;
+  p->ctas_per_tile = (ncol4 + p->cols_per_cta - 1) / p->cols_per_cta;
+}
+
+// The streamed tensor-core kernel (split_mode 3): about SMs x ctas_per_sm
+// persistent CTAs (tuning nsplit: CTAs per SM, 1 to 4; default 2) in groups
+// of one CTA per tile of a sequence, each CTA taking an equal run of its tile
+// column's R-row stages (tuning rows_per_stage, a multiple of 16; default 64)
+// through a ring of `stages` slots (default: as many as fit the CTA's share
+// of the SM's shared memory, 2 to 8).
+int plan_stream(Plan* p, const gqa_av_tuning* t, const DeviceInfo& di, int B, int Cmax, int dev,
+                int v_dtype, int Hq) {
+  const int per_sm = t && t->nsplit > 0 ? t->nsplit : 2;
+  if (per_sm > 4) return fail(GQA_AV_ERR_INVALID, "streamed splits: nsplit=%d CTAs per SM, at most 4", per_sm);
+  p->stream = 1;
+  p->balanced = 0;
+  p->early = 0;
+  p->cvt_warps = 4;  // one CTA streams for the whole call: the widest conversion
+  if (t && t->rows_per_stage > 0) {
+    if (t->rows_per_stage % 16 || t->rows_per_stage > 256)
+      return fail(GQA_AV_ERR_INVALID, "rows_per_stage=%d must be a multiple of 16, <= 256",
+                  t->rows_per_stage);
+    p->R = t->rows_per_stage;
+  } else {
+    // 64-row stages on shapes with at least as many tiles as SMs, 96-row
+    // stages on the others (each measured faster in its regime).
+    p->R = static_cast<long long>(B) * p->hgroups * p->ndt >= di.sms ? 64 : 96;
+  }
+  p->chunk_rows = p->R;
+  p->rows_per_split = p->R;
+  // K CTAs a group, one per tile of a sequence; as many groups as fit
+  // per_sm CTAs on every SM (at least one).
+  const int K = p->hgroups * p->ndt;
+  p->split_units = K * std::max(1, di.sms * per_sm / K);
+  p->grid = p->split_units;
+  p->nsplit = per_sm;
+  p->combine = 1;
+  attn_layout(p, Hq);
+  const int budget = std::min(di.smem_optin, di.smem_per_sm / per_sm - 1024);
+  auto lay = [&] {
+    layout_mma(p, 0);
+    p->lens_off = static_cast<uint32_t>(align_up(p->smem - 1024, 16));
+    p->smem = static_cast<int>(p->lens_off + (B + 1) * 4 + 1024);
+  };
+  if (t && t->stages > 0) {
+    if (t->stages < 2 || t->stages > kMaxStages)
+      return fail(GQA_AV_ERR_INVALID, "stages=%d must be in [2, %d]", t->stages, kMaxStages);
+    p->stages = t->stages;
+    lay();
+  } else {
+    // About 64 KiB of V in flight a CTA (4 stages of 64 rows, 3 of 96 or
+    // more, 2 of 128 or more), fewer if the CTA's share of shared memory is
+    // smaller, at least 2.
+    const int pref = std::max(2, std::min(kMaxStages, 65536 / (p->R * 256) + (p->R == 96)));
+    for (p->stages = pref; p->stages > 2; --p->stages) {
+      lay();
+      if (p->smem <= budget) break;
+    }
+    lay();
+  }
+  if (p->smem > di.smem_optin)
+    return fail(GQA_AV_ERR_UNSUPPORTED, "plan needs %d B of shared memory (limit %d)", p->smem,
+                di.smem_optin);
+  if (t && t->early_stages > p->stages)
+    return fail(GQA_AV_ERR_INVALID, "early_stages=%d must be in [1, stages=%d]", t->early_stages,
+                p->stages);
+  int rc;
+  if ((rc = ctas_per_sm(dev, di.smem_optin, v_dtype, kEngineStream, p->nmma / 16, p->smem, &p->occ)))
+    return rc;
+  if (p->occ < 1) return fail(GQA_AV_ERR_UNSUPPORTED, "kernel does not fit on an SM");
+  p->one_per_sm = 0;
+  p->ws_bytes = static_cast<size_t>(2) * p->split_units * p->heads * p->dt * sizeof(float);
+  combine_layout(p, di.sms);
+  (void)Cmax;
+  return GQA_AV_OK;
 }
 
 int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode,
@@ -402,11 +536,28 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
   // With fewer tiles than SMs the grid is one wave and fixed splits are
   // faster: a CTA issues its first stage before it reads any length.
   const int want_split = t && t->split_mode > 0 ? t->split_mode : 0;
-  if (want_split > 2)
-    return fail(GQA_AV_ERR_INVALID, "split_mode=%d must be 0 (auto), 1 (fixed) or 2 (balanced)",
+  if (want_split > 3)
+    return fail(GQA_AV_ERR_INVALID,
+                "split_mode=%d must be 0 (auto), 1 (fixed), 2 (balanced) or 3 (streamed)",
                 want_split);
-  if (want_split == 2 && !tensor)
-    return fail(GQA_AV_ERR_UNSUPPORTED, "balanced splits need the tensor-core engine");
+  if (want_split >= 2 && !tensor)
+    return fail(GQA_AV_ERR_UNSUPPORTED, "balanced and streamed splits need the tensor-core engine");
+  p->stream = 0;
+  p->lens_off = 0;
+  if (want_split == 3) {
+    if (block_size > 0)
+      return fail(GQA_AV_ERR_UNSUPPORTED, "streamed splits take a contiguous V cache");
+    if (B > kStreamMaxB)
+      return fail(GQA_AV_ERR_UNSUPPORTED, "streamed splits take at most %d sequences", kStreamMaxB);
+    return plan_stream(p, t, di, B, Cmax, dev, v_dtype, Hq);
+  }
+  // The tensor-core engine streams by default (contiguous V, at most
+  // kStreamMaxB sequences): measured faster than fixed or balanced splits on
+  // every tensor-core workload (large batch 827 vs 882 us, its 1/8-context
+  // twin 105 vs 117 us, MQA 19.5 vs 20.7 us, Phi 20.4 vs 21.3 us).
+  if (want_split == 0 && tensor && block_size == 0 && B <= kStreamMaxB &&
+      !(t && (t->nsplit > 0 || t->early_stages > 0)))
+    return plan_stream(p, t, di, B, Cmax, dev, v_dtype, Hq);
   p->balanced = tensor && (want_split == 2 || (want_split == 0 && p->tiles >= di.sms));
   const long long grid =
       static_cast<long long>(p->tiles) * (p->balanced ? p->nsplit + 1 : p->nsplit);
@@ -422,17 +573,7 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
   } else {
     p->stages = std::max(2, std::min(3, iters));
   }
-  // attn weights of a stage. By TMA when attn rows are 16-byte multiples
-  // (Hq % 4 == 0): the box starts at the 4-aligned head at or below the CTA's
-  // first head (a TMA box must start 16-byte aligned) and is wide enough for
-  // every CTA's heads; otherwise by cp.async, `avec` floats a copy.
-  const int max_off = p->heads % 4 == 0 ? 0 : (p->heads % 2 == 0 ? 2 : 3);
-  const int aw = static_cast<int>(align_up(p->heads + max_off, 4));
-  p->attn_tma = Hq % 4 == 0 && aw <= 256;
-  p->ap = p->attn_tma ? aw : static_cast<int>(align_up(p->heads, 4));
-  p->avec = 1;
-  if (Hq % 4 == 0 && p->heads % 4 == 0) p->avec = 4;
-  else if (Hq % 2 == 0 && p->heads % 2 == 0) p->avec = 2;
+  attn_layout(p, Hq);
   p->one_per_sm = one_wave && static_cast<long long>(p->tiles) * p->nsplit <= di.sms;
   const int min_smem = p->one_per_sm ? di.smem_per_sm / 2 + 1024 : 0;
   auto lay = [&] { if (tensor) layout_mma(p, min_smem); else layout(p, min_smem); };
@@ -459,7 +600,7 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
   // nothing before it has read them.
   if (p->balanced) p->early = 0;
 
-  if ((rc = ctas_per_sm(dev, di.smem_optin, v_dtype, p->engine, kernel_sel(*p), p->smem,
+  if ((rc = ctas_per_sm(dev, di.smem_optin, v_dtype, kernel_engine(*p), kernel_sel(*p), p->smem,
                         &p->occ)))
     return rc;
   if (p->occ < 1) return fail(GQA_AV_ERR_UNSUPPORTED, "kernel does not fit on an SM");
@@ -467,19 +608,7 @@ int make_plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int
   p->ws_bytes = p->combine
                     ? static_cast<size_t>(p->grid) * p->heads * p->dt * sizeof(float)
                     : 0;  // one partial slot a CTA
-  // Split combine: `parts` threads per float4 column (a power of two <= 16),
-  // as many as keep its grid within about one CTA per SM. Its CTAs are small
-  // enough to start next to the main kernel's while that runs, so they are
-  // all waiting when the partials are complete (measured faster than a grid
-  // that only starts as the main kernel's CTAs leave).
-  const int ncol4 = p->heads * p->dt / 4;
-  const long long cols = static_cast<long long>(p->tiles) * ncol4;
-  p->parts = 1;
-  while (p->parts < 16 && (p->balanced || p->parts < p->nsplit) &&
-         cols * p->parts * 2 <= static_cast<long long>(di.sms) * kCombineThreads)
-    p->parts *= 2;
-  p->cols_per_cta = kCombineThreads / p->parts;
-  p->ctas_per_tile = (ncol4 + p->cols_per_cta - 1) / p->cols_per_cta;
+  combine_layout(p, di.sms);
   return GQA_AV_OK;
 }
 
@@ -507,6 +636,7 @@ void fill_params(Params* p, const Plan& pl, const float* attn, const int32_t* se
   p->cvt_warps = pl.cvt_warps;
   p->split_units = pl.split_units;
   p->balanced = pl.balanced;
+  p->lens_off = pl.lens_off;
   p->chunk_rows = pl.chunk_rows;
   // attn is 16-byte aligned (checked before planning): a TMA source or a
   // cp.async of up to 16 bytes can start at any 4-head boundary of it.
@@ -526,7 +656,7 @@ cudaError_t launch_call(const Kernel& kern, const Plan& pl, const Params& p, cud
   c.rows_per_split = pl.rows_per_split; c.nsplit = pl.nsplit;
   c.tile_elems = pl.heads * pl.dt;
   c.parts = pl.parts; c.cols_per_cta = pl.cols_per_cta; c.ctas_per_tile = pl.ctas_per_tile;
-  c.balanced = pl.balanced;
+  c.balanced = pl.stream ? kCombineStream : (pl.balanced ? kCombineBalanced : kCombineFixed);
   c.R = pl.R; c.hgroups = pl.hgroups; c.split_units = pl.split_units;
   return launch_combine(c, pl.tiles * pl.ctas_per_tile, stream);
 }
@@ -786,7 +916,7 @@ int run(const float* attn, const void* v, const int32_t* seq_lens, float* out, i
   if (p.attn_tma && (rc = encode_attn_map(&p.a_map, attn, B, Cmax, Hq, pl.ap, pl.R))) return rc;
 
   Kernel kern;
-  if (!pick_kernel(v_dtype, pl.engine, kernel_sel(pl), &kern)) return fail(GQA_AV_ERR_UNSUPPORTED, "no kernel");
+  if (!pick_kernel(v_dtype, kernel_engine(pl), kernel_sel(pl), &kern)) return fail(GQA_AV_ERR_UNSUPPORTED, "no kernel");
   cudaError_t e = launch_call(kern, pl, p, stream);
   if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
   return GQA_AV_OK;
@@ -808,8 +938,12 @@ cudaError_t launch_combine(const CombineParams& p, int grid, cudaStream_t stream
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = p.balanced ? cudaLaunchKernelEx(&cfg, gqa_av_combine_kernel<true>, p)
-                             : cudaLaunchKernelEx(&cfg, gqa_av_combine_kernel<false>, p);
+  cudaError_t e =
+      p.balanced == kCombineStream
+          ? cudaLaunchKernelEx(&cfg, gqa_av_combine_kernel<kCombineStream>, p)
+          : (p.balanced == kCombineBalanced
+                 ? cudaLaunchKernelEx(&cfg, gqa_av_combine_kernel<kCombineBalanced>, p)
+                 : cudaLaunchKernelEx(&cfg, gqa_av_combine_kernel<kCombineFixed>, p));
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -898,7 +1032,7 @@ int gqa_av_plan(int B, int Cmax, int Hq, int Hkv, int D, int v_dtype, int mode,
   info->ctas = p.grid;
   info->threads_per_cta = p.engine == kEngineTensor ? mma_threads(p.cvt_warps) : cta_threads(p.gc);
   info->engine = p.engine;
-  info->split_mode = p.balanced ? 2 : 1;
+  info->split_mode = p.stream ? 3 : (p.balanced ? 2 : 1);
   info->smem_bytes = p.smem;
   info->ctas_per_sm = p.occ;
   info->workspace_bytes = kHeaderBytes + p.ws_bytes;
@@ -1037,7 +1171,7 @@ int run_in_scratch(const float* attn, const void* v, const int32_t* seq_lens, fl
   if (p.attn_tma && (rc = encode_attn_map(&p.a_map, attn, B, Cmax, Hq, pl.ap, pl.R))) return rc;
 
   Kernel kern;
-  if (!pick_kernel(v_dtype, pl.engine, kernel_sel(pl), &kern)) return fail(GQA_AV_ERR_UNSUPPORTED, "no kernel");
+  if (!pick_kernel(v_dtype, kernel_engine(pl), kernel_sel(pl), &kern)) return fail(GQA_AV_ERR_UNSUPPORTED, "no kernel");
   e = launch_call(kern, pl, p, stream);
   if (e != cudaSuccess) return fail_cuda(e, "kernel launch");
   return GQA_AV_OK;

@@ -4,6 +4,7 @@
 #pragma once
 #include "gqa_av_kernel.cuh"
 #include "gqa_av_mma.cuh"
+#include "gqa_av_stream.cuh"
 
 namespace gqa_av {
 
@@ -63,6 +64,36 @@ cudaError_t occupancy_mma(int smem_limit, int smem_bytes, int* ctas_per_sm) {
                                                        kMmaMaxThreads, smem_bytes);
 }
 
+// The streamed tensor-core kernel: one persistent CTA per SM (or more).
+template <typename Tag, int NB>
+cudaError_t launch_stream(const Params& p, int grid, int smem_bytes, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(mma_threads(p.cvt_warps));
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem_bytes);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gqa_av_stream_kernel<Tag, NB>, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <typename Tag, int NB>
+cudaError_t occupancy_stream(int smem_limit, int smem_bytes, int* ctas_per_sm) {
+  cudaError_t e = cudaFuncSetAttribute(gqa_av_stream_kernel<Tag, NB>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_limit);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, gqa_av_stream_kernel<Tag, NB>,
+                                                       kMmaMaxThreads, smem_bytes);
+}
+
+#define GQA_AV_INSTANTIATE_STREAM(TAG, NB)                                               \
+  template cudaError_t launch_stream<TAG, NB>(const Params&, int, int, cudaStream_t);    \
+  template cudaError_t occupancy_stream<TAG, NB>(int, int, int*);
+
 #define GQA_AV_INSTANTIATE_MMA(TAG, NB)                                                  \
   template cudaError_t launch_mma<TAG, NB>(const Params&, int, int, cudaStream_t);       \
   template cudaError_t occupancy_mma<TAG, NB>(int, int, int*);
@@ -84,6 +115,10 @@ cudaError_t occupancy_mma(int smem_limit, int smem_bytes, int* ctas_per_sm) {
   GQA_AV_INSTANTIATE_MMA(TAG, 1)    \
   GQA_AV_INSTANTIATE_MMA(TAG, 2)    \
   GQA_AV_INSTANTIATE_MMA(TAG, 3)    \
-  GQA_AV_INSTANTIATE_MMA(TAG, 4)
+  GQA_AV_INSTANTIATE_MMA(TAG, 4)    \
+  GQA_AV_INSTANTIATE_STREAM(TAG, 1) \
+  GQA_AV_INSTANTIATE_STREAM(TAG, 2) \
+  GQA_AV_INSTANTIATE_STREAM(TAG, 3) \
+  GQA_AV_INSTANTIATE_STREAM(TAG, 4)
 
 }  // namespace gqa_av

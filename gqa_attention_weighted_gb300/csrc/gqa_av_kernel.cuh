@@ -95,8 +95,9 @@ struct alignas(64) Params {
   uint32_t b_off;               // shared-memory offset of the B (weights) ring
   uint32_t tmem_cols;           // tensor-memory columns allocated (4 x N, power of 2 >= 32)
   int cvt_warps;                // weight-conversion warps (2 or 4)
-  int split_units;              // CTAs the batch's context is spread over (length-balanced splits)
+  int split_units;              // CTAs the batch's context is spread over (balanced, streamed)
   int balanced;                 // splits balanced over the batch's lengths (else fixed)
+  uint32_t lens_off;            // streamed kernel: shared-memory offset of the lengths
   // Paged V: the tensor map is over a pool of blocks {D, Hkv, block_size,
   // num_blocks}; a stage's rows come as chunk_rows-row boxes from the blocks
   // that hold them (block_table[b][c / block_size]). Contiguous V: null table,
@@ -119,7 +120,7 @@ struct CombineParams {
   int parts;                    // threads per column (fixed chunks of splits)
   int cols_per_cta;             // float4 columns per CTA (kCombineThreads / parts)
   int ctas_per_tile;
-  int balanced;                 // length-balanced splits of the tensor-core kernel
+  int balanced;                 // 0 fixed splits, 1 length-balanced, 2 streamed
   int R, hgroups, split_units;  // their stage rows, head groups and CTA count
 };
 
@@ -373,6 +374,15 @@ __device__ __forceinline__ int clamped_len(const int32_t* seq_lens, int b, int C
   return L < 0 ? 0 : (L > Cmax ? Cmax : L);
 }
 
+// The same through the read-only data path: the lengths are read by every CTA
+// of a call, so CTAs on one SM share them in L1 instead of queueing on one L2
+// line. Only for reads after the grid-dependency wait (nothing of them can be
+// cached from before it) of lengths no kernel writes while this one runs.
+__device__ __forceinline__ int clamped_len_ro(const int32_t* seq_lens, int b, int Cmax) {
+  const int L = seq_lens ? __ldg(seq_lens + b) : Cmax;
+  return L < 0 ? 0 : (L > Cmax ? Cmax : L);
+}
+
 __device__ __forceinline__ int balanced_splits_of(int L, int R, int sps) {
   const int n = ((L + R - 1) / R + sps - 1) / sps;
   return n > 1 ? n : 1;
@@ -437,6 +447,44 @@ __device__ __forceinline__ int2 balanced_prefix(const int32_t* seq_lens, int Cma
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   return make_int2(s, balanced_splits_of(clamped_len(seq_lens, b, Cmax), R, sps));
+}
+
+// ---------------------------------------------------------------------------
+// Streamed schedule (the streamed tensor-core kernel, gqa_av_stream.cuh, and
+// its combine): sequence b has stream_stages(L_b, R) stages in each of its K
+// tiles; tile column k lists them sequence after sequence, T = sum_b of them;
+// group g of Ug takes stages [stream_first(T, g, Ug), stream_first(T, g + 1,
+// Ug)) of every column (CTA u = g * K + k takes column k).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int stream_stages(int L, int R) {
+  const int n = (L + R - 1) / R;
+  return n > 1 ? n : 1;
+}
+
+__device__ __forceinline__ long long stream_first(long long T, int g, int Ug) {
+  return T * g / Ug;
+}
+
+// The group whose range holds stage x: the largest g with stream_first(T, g, Ug) <= x.
+__device__ __forceinline__ int stream_owner(long long T, long long x, int Ug) {
+  return static_cast<int>(((x + 1) * Ug - 1) / T);
+}
+
+// Stages a column holds in all (x) and before sequence b (y). Warp-collective.
+__device__ __forceinline__ longlong2 stream_prefix(const int32_t* seq_lens, int B, int Cmax, int R,
+                                                   int b) {
+  long long tot = 0, pre = 0;
+  for (int i = threadIdx.x & 31; i < B; i += 32) {
+    const int n = stream_stages(clamped_len(seq_lens, i, Cmax), R);
+    tot += n;
+    if (i < b) pre += n;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    pre += __shfl_xor_sync(0xffffffffu, pre, o);
+  }
+  return make_longlong2(tot, pre);
 }
 
 // Two fp32 lanes in one 64-bit register pair, and the packed FMA on them:
@@ -718,10 +766,17 @@ gqa_av_kernel(const __grid_constant__ Params p) {
 // ---------------------------------------------------------------------------
 // The split combine. CTA (tile, column block): `parts` threads per float4
 // column each sum a fixed chunk of the splits (their loads in flight
-// together), then the chunks are added in chunk order. kBalanced: the
-// partials of length-balanced splits (one slot a CTA of the main kernel).
+// together), then the chunks are added in chunk order. kMode: the partials
+// of fixed splits ([tile][split]), of length-balanced splits (one slot a CTA
+// of the main kernel), or of the streamed kernel (two slots a CTA: its first
+// and its last segment; the tile's partials are those of the CTAs whose
+// ranges hold its stages, in CTA order).
 // ---------------------------------------------------------------------------
-template <bool kBalanced>
+constexpr int kCombineFixed = 0;
+constexpr int kCombineBalanced = 1;
+constexpr int kCombineStream = 2;
+
+template <int kMode>
 __global__ void __launch_bounds__(kCombineThreads)
 gqa_av_combine_kernel(const __grid_constant__ CombineParams p) {
   __shared__ float4 chunk_sum[kCombineThreads];
@@ -740,7 +795,33 @@ gqa_av_combine_kernel(const __grid_constant__ CombineParams p) {
   const int ncol4 = p.tile_elems >> 2;
   int nunit;              // splits of the tile
   size_t first, stride;   // float4 offsets of its split 0 and between its splits
-  if constexpr (kBalanced) {
+  size_t adj0 = 0;        // added to split 0's offset (streamed: a CTA's second slot)
+  if constexpr (kMode == kCombineStream) {
+    // Tile (b, k): stages [P_b, P_b + n_b) of column k, held by groups g0..g1;
+    // group g's CTA is g * K + k, its partial slot 2 (g K + k), except that
+    // g0's is its second slot when the tile does not start its range.
+    __shared__ longlong2 span;  // (first group, group count)
+    __shared__ int first_slot_adj;
+    const int K = p.hgroups * p.ndt;
+    if (threadIdx.x < 32) {
+      const longlong2 r = stream_prefix(p.seq_lens, p.B, p.Cmax, p.R, b);
+      const int nb = stream_stages(clamped_len(p.seq_lens, b, p.Cmax), p.R);
+      const int Ug0 = p.split_units / K;
+      const int Ug = static_cast<int>(r.x < Ug0 ? r.x : Ug0);  // groups that stream
+      const int g0 = stream_owner(r.x, r.y, Ug);
+      const int g1 = stream_owner(r.x, r.y + nb - 1, Ug);
+      if (threadIdx.x == 0) {
+        span = make_longlong2(g0, g1 - g0 + 1);
+        first_slot_adj = stream_first(r.x, g0, Ug) == r.y ? 0 : 1;
+      }
+    }
+    __syncthreads();
+    const size_t k = (size_t)hg * p.ndt + dti;
+    nunit = static_cast<int>(span.y);
+    first = (size_t)(2 * (span.x * K + k)) * ncol4;
+    stride = (size_t)2 * K * ncol4;
+    adj0 = (size_t)first_slot_adj * ncol4;
+  } else if constexpr (kMode == kCombineBalanced) {
     __shared__ int2 prefix;
     if (threadIdx.x < 32) {
       const int K = p.hgroups * p.ndt;
@@ -772,7 +853,7 @@ gqa_av_combine_kernel(const __grid_constant__ CombineParams p) {
   const float4* base = reinterpret_cast<const float4*>(p.ws) + first;
   float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
   if (col < ncol4 && lo < hi) {
-    sum = __ldcg(base + (size_t)lo * stride + col);
+    sum = __ldcg(base + (size_t)lo * stride + (lo == 0 ? adj0 : 0) + col);
     sum_strided<true>(sum, base + col, stride, lo + 1, hi);
   }
   chunk_sum[t] = sum;

@@ -103,7 +103,15 @@ def tensor_engine_preferred(B, C, Hq, heads, D):
     return tensor_engine_applies(heads, D) and (heads >= 8 or tile_rows >= 1 << 18)
 
 
-@pytest.mark.parametrize("engine", [0, 1, 2], ids=["auto", "fma", "tensor"])
+def engine_tuning(engine):
+    """Tuning of a test's engine code: 0 the library's choice, 1 the FMA
+    kernel, 2 the tensor-core kernel, 3 the streamed tensor-core kernel."""
+    if engine == 3:
+        return dict(engine=2, split_mode=3)
+    return dict(engine=engine) if engine else None
+
+
+@pytest.mark.parametrize("engine", [0, 1, 2, 3], ids=["auto", "fma", "tensor", "stream"])
 @pytest.mark.parametrize("G,D", SWEEP, ids=[f"G{g}-D{d}" for g, d in SWEEP])
 def test_shape_sweep(gq, G, D, engine):
     rng = np.random.default_rng(1000 * G + D)
@@ -115,17 +123,17 @@ def test_shape_sweep(gq, G, D, engine):
         ref = run_oracle(attn, v, sl, vd)
         for mode in (0, 1):
             heads = G if mode == 1 else 1
-            if engine == 2 and not tensor_engine_applies(heads, D):
+            if engine >= 2 and not tensor_engine_applies(heads, D):
                 continue
             if engine == 0:
                 want = 2 if tensor_engine_preferred(B, C, G * Hkv, heads, D) else 1
                 plan = gq.gqa_av_plan(B, C, G * Hkv, Hkv, D, 0 if vd == "bf16" else 1, mode)
                 assert plan["engine"] == want, (G, D, mode, plan["engine"])
-            out = run_gpu(gq, attn, v, sl, mode, dict(engine=engine) if engine else None)
+            out = run_gpu(gq, attn, v, sl, mode, engine_tuning(engine))
             assert_close(out, ref, f"G={G} D={D} {vd} mode={mode} engine={engine}")
 
 
-@pytest.mark.parametrize("engine", [0, 2], ids=["auto", "tensor"])
+@pytest.mark.parametrize("engine", [0, 2, 3], ids=["auto", "tensor", "stream"])
 @pytest.mark.parametrize("L", [0, 1, 2, 7, 8, 9, 31, 32, 33, 63, 64, 65, 255, 256, 257, 1000])
 def test_lengths_and_ragged_tails(gq, L, engine):
     rng = np.random.default_rng(L + 7)
@@ -133,17 +141,17 @@ def test_lengths_and_ragged_tails(gq, L, engine):
     attn, v, sl = rand_case(rng, B, C, Hq, Hkv, D, "bf16", [L, max(0, 1024 - L)])
     ref = run_oracle(attn, v, sl, "bf16")
     for mode in (0, 1):
-        out = run_gpu(gq, attn, v, sl, mode, dict(engine=engine) if engine else None)
+        out = run_gpu(gq, attn, v, sl, mode, engine_tuning(engine))
         assert_close(out, ref, f"L={L} mode={mode}")
         if L == 0:
             assert np.array_equal(out[0], np.zeros_like(out[0]))
 
 
-@pytest.mark.parametrize("engine", [0, 1, 2], ids=["auto", "fma", "tensor"])
+@pytest.mark.parametrize("engine", [0, 1, 2, 3], ids=["auto", "fma", "tensor", "stream"])
 def test_lengths_are_clamped_and_null_means_full(gq, engine):
     rng = np.random.default_rng(5)
     B, C, Hq, Hkv, D = 3, 300, 8, 2, 64
-    tun = dict(engine=engine) if engine else None
+    tun = engine_tuning(engine)
     attn, v, _ = rand_case(rng, B, C, Hq, Hkv, D, "bf16", [300, 300, 300], pad_nan=False)
     full = run_oracle(attn, v, None, "bf16")
     assert_close(run_gpu(gq, attn, v, None, -1, tun), full, "seq_lens=NULL")
@@ -191,6 +199,40 @@ def test_balanced_splits_over_the_batch(gq, B, kind, nsplit, split_mode):
             assert np.array_equal(out[b], np.zeros_like(out[b])), b
 
 
+# The streamed tensor-core kernel: every CTA takes an equal run of the call's
+# stages across tile and sequence boundaries (its first stage found by a warp
+# scan over the lengths in chunks of 32), cut tiles are combined from two
+# partial slots a CTA. The same batches as above, with 1 to 4 CTAs per SM and
+# stages of 16 to 128 rows (more CTAs than stages included).
+@pytest.mark.parametrize("R", [16, 64, 128])
+@pytest.mark.parametrize("per_sm", [0, 1, 3, 4])
+@pytest.mark.parametrize("B,kind", BALANCED, ids=[f"B{b}-{k if isinstance(k, str) else 'mix'}"
+                                                  for b, k in BALANCED])
+def test_streamed_splits_over_the_batch(gq, B, kind, per_sm, R):
+    rng = np.random.default_rng(B * 10 + per_sm + R)
+    C, Hq, Hkv, D = 300, 16, 2, 64
+    if kind == "one_long":
+        lens = [3] * B
+        lens[B // 2] = C
+    elif kind == "all_empty":
+        lens = [0] * B
+    else:
+        lens = list(rng.integers(0, C + 1, size=B))
+        for i, L in enumerate(x for x in kind if x is not None):
+            lens[(7 * i + 3) % B] = L
+    attn, v, sl = rand_case(rng, B, C, Hq, Hkv, D, "bf16", lens)
+    ref = run_oracle(attn, v, sl, "bf16")
+    tun = dict(engine=2, nsplit=per_sm, split_mode=3, rows_per_stage=R)
+    assert gq.gqa_av_plan(B, C, Hq, Hkv, D, 0, 1, tun)["split_mode"] == 3
+    for mode in (0, 1):
+        out = run_gpu(gq, attn, v, sl, mode, tun)
+        assert_close(out, ref, f"B={B} {kind} per_sm={per_sm} R={R} mode={mode}")
+        assert np.array_equal(run_gpu(gq, attn, v, sl, mode, tun), out), "not reproducible"
+        for b, L in enumerate(lens):
+            if L == 0:
+                assert np.array_equal(out[b], np.zeros_like(out[b])), b
+
+
 # ------------------------------------------------------ launch-shape sweep
 TUNINGS = [dict(nsplit=1), dict(nsplit=2), dict(nsplit=7), dict(nsplit=1000),
            dict(dtile=64), dict(dtile=32, rows_per_stage=8), dict(stages=2),
@@ -204,7 +246,10 @@ TUNINGS = [dict(nsplit=1), dict(nsplit=2), dict(nsplit=7), dict(nsplit=1000),
            dict(nsplit=7, stages=4, early_stages=4), dict(nsplit=16, early_stages=2),
            dict(nsplit=2, rows_per_stage=64, stages=8, early_stages=8),
            dict(split_mode=1), dict(split_mode=2), dict(nsplit=7, split_mode=2),
-           dict(nsplit=1, split_mode=2), dict(rows_per_stage=32, stages=2, split_mode=2)]
+           dict(nsplit=1, split_mode=2), dict(rows_per_stage=32, stages=2, split_mode=2),
+           dict(split_mode=3), dict(nsplit=1, split_mode=3), dict(nsplit=4, split_mode=3),
+           dict(split_mode=3, rows_per_stage=128, stages=3),
+           dict(split_mode=3, rows_per_stage=16, stages=8)]
 
 
 def tensor_tuning_applies(t):
@@ -217,8 +262,8 @@ def tensor_tuning_applies(t):
 def test_tunings_agree_and_are_deterministic(gq, tuning, engine):
     if engine == 2 and not tensor_tuning_applies(tuning):
         pytest.skip("launch shape the tensor-core kernel does not take")
-    if engine == 1 and tuning.get("split_mode") == 2:
-        pytest.skip("balanced splits are a tensor-core engine plan")
+    if engine == 1 and tuning.get("split_mode", 0) >= 2:
+        pytest.skip("balanced and streamed splits are tensor-core engine plans")
     tuning = dict(tuning, engine=engine)
     rng = np.random.default_rng(99)
     B, C, Hq, Hkv, D = 2, 1500, 24, 8, 128
@@ -344,7 +389,8 @@ def test_invalid_calls_launch_nothing(gq):
     v8 = torch.zeros((1, 16, 2, 64), dtype=torch.bfloat16, device=dev)
     out8 = torch.full((1, 8, 64), 7.0, device=dev)
     for bad in (dict(stages=9), dict(stages=1), dict(rows_per_stage=7), dict(dtile=12),
-                dict(stages=2, early_stages=3), dict(split_mode=3)):
+                dict(stages=2, early_stages=3), dict(split_mode=4),
+                dict(engine=2, split_mode=3, nsplit=5)):
         with pytest.raises(gq.GqaAvError) as e:
             gq.gqa_av_decode_tuned(attn8, v8, None, out8, mode=1, tuning=bad)
         assert e.value.status == 1, bad
@@ -382,12 +428,23 @@ def test_plan_reports_the_launch(gq):
     r = gq.gqa_av_plan(8, 32768, 16, 1, 256, 1, -1)
     assert r["heads_per_cta"] == 16 and r["head_chunk"] == 8
     assert p["early_stages"] == 1
-    t = gq.gqa_av_plan(4, 16384, 24, 8, 128, 0, -1)  # tensor core, 32 tiles: fixed splits
-    assert t["engine"] == 2 and t["split_mode"] == 1 and t["early_stages"] == 1
-    assert t["ctas"] == t["tiles"] * t["nsplit"]
-    u = gq.gqa_av_plan(32, 131072, 64, 8, 128, 0, -1)  # 256 tiles: balanced splits
-    assert u["engine"] == 2 and u["split_mode"] == 2 and u["early_stages"] == 0
-    assert u["ctas"] == u["tiles"] * (u["nsplit"] + 1) and u["combine_ctas"] > 0
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    # Tensor core, 32 tiles (8 a sequence): streamed, two CTAs an SM in groups
+    # of 8, 96-row stages in a 3-stage ring.
+    t = gq.gqa_av_plan(4, 16384, 24, 8, 128, 0, -1)
+    assert t["engine"] == 2 and t["split_mode"] == 3 and t["early_stages"] == 0
+    assert t["ctas"] == 8 * (2 * sms // 8) and t["combine_ctas"] > 0
+    assert t["rows_per_stage"] == 96 and t["stages"] == 3
+    # 256 tiles: streamed, 64-row stages in a 4-stage ring.
+    u = gq.gqa_av_plan(32, 131072, 64, 8, 128, 0, -1)
+    assert u["engine"] == 2 and u["split_mode"] == 3 and u["early_stages"] == 0
+    assert u["ctas"] == 8 * (2 * sms // 8) and u["combine_ctas"] > 0
+    assert u["rows_per_stage"] == 64 and u["stages"] == 4
+    # The other split rules on request.
+    f = gq.gqa_av_plan(4, 16384, 24, 8, 128, 0, -1, dict(split_mode=1))
+    assert f["split_mode"] == 1 and f["early_stages"] == 1 and f["ctas"] == f["tiles"] * f["nsplit"]
+    v = gq.gqa_av_plan(32, 131072, 64, 8, 128, 0, -1, dict(split_mode=2))
+    assert v["split_mode"] == 2 and v["ctas"] == v["tiles"] * (v["nsplit"] + 1)
     with pytest.raises(gq.GqaAvError):
         gq.gqa_av_plan(1, 8192, 32, 8, 128, 0, -1, dict(engine=1, split_mode=2))
     e = gq.gqa_av_plan(1, 8192, 32, 8, 128, 0, -1, dict(stages=3, early_stages=3))

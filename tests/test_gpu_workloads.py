@@ -52,13 +52,14 @@ def _dense_case(name):
     return _REFS[name]
 
 
-@pytest.mark.parametrize("engine", [0, 1, 2], ids=["auto", "fma", "tensor"])
+@pytest.mark.parametrize("engine", [0, 1, 2, 3], ids=["auto", "fma", "tensor", "stream"])
 @pytest.mark.parametrize("name", ["small", "llama", "phi", "mqa"])
 def test_workload_dense(gq, name, engine):
     w, x, ref = _dense_case(name)
     dev = torch.device("cuda")
     attn, v, sl = x["attn"].to(dev), x["v"].to(dev), x["seq_lens"].to(dev)
-    tuning = dict(engine=engine) if engine else None
+    tuning = (dict(engine=2, split_mode=3) if engine == 3 else
+              dict(engine=engine) if engine else None)
 
     def call(out, mode=gq.MODE_AUTO):
         if tuning is None:
@@ -108,8 +109,9 @@ def test_workload_large_full(gq, name):
     gq.gqa_av_device_status()
     tol = TOL * max(1.0, float(out.abs().max()))
     assert float((per - out).abs().max()) <= tol
-    # The other engine on the whole output (the library picks tensor cores here).
-    fma = torch.empty_like(out)
-    gq.gqa_av_decode_tuned(attn, v, sl, fma, tuning=dict(engine=1))
-    gq.gqa_av_device_status()
-    assert float((fma - out).abs().max()) <= tol
+    # The other kernels on the whole output (the library picks tensor cores here).
+    for tun in (dict(engine=1), dict(engine=2, split_mode=3), dict(engine=2, split_mode=2)):
+        other = torch.empty_like(out)
+        gq.gqa_av_decode_tuned(attn, v, sl, other, tuning=tun)
+        gq.gqa_av_device_status()
+        assert float((other - out).abs().max()) <= tol, tun
