@@ -50,6 +50,7 @@ METRIC_QK = ("GQA QK-softmax decode achieved HBM GB/s over compulsory bytes (K r
              "µs/call")
 QK_SOURCES = ["gqa_attention_weighted_gb300/csrc/gqa_qk_kernel.cuh",
               "gqa_attention_weighted_gb300/csrc/gqa_qk_mma.cuh",
+              "gqa_attention_weighted_gb300/csrc/gqa_qk_stream.cuh",
               "gqa_attention_weighted_gb300/csrc/gqa_qk_api.cu",
               "gqa_attention_weighted_gb300/csrc/gqa_av_kernel.cuh"]
 METRIC_ATTN = ("GQA fused decode attention achieved HBM GB/s over compulsory bytes (K and V "
@@ -66,11 +67,18 @@ L2_NOMINAL = 132644864
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["gqa_attention_weighted_gb300/csrc/gqa_av_kernel.cuh",
                   "gqa_attention_weighted_gb300/csrc/gqa_av_mma.cuh",
+                  "gqa_attention_weighted_gb300/csrc/gqa_av_stream.cuh",
                   "gqa_attention_weighted_gb300/csrc/gqa_av_instances.cuh",
                   "gqa_attention_weighted_gb300/csrc/gqa_av_api.cu"]
-ENGINES = {"auto": 0, "fma": 1, "tensor": 2}
-SPLIT_MODES = {"auto": 0, "fixed": 1, "balanced": 2}
+ENGINES = {"auto": 0, "fma": 1, "tensor": 2, "stream": 3}
+SPLIT_MODES = {"auto": 0, "fixed": 1, "balanced": 2, "streamed": 3}
 KERNEL_NAMES = {1: "gqa_av_kernel", 2: "gqa_av_mma_kernel", 3: "gqa_av_generic_kernel"}
+STREAM_KERNEL = "gqa_av_stream_kernel"  # the tensor engine's streamed split rule (split_mode 3)
+
+
+def kernel_name(plan) -> str:
+    """The AV main kernel a plan runs."""
+    return STREAM_KERNEL if plan["split_mode"] == 3 else KERNEL_NAMES[plan["engine"]]
 
 
 def kernel_hash(sources=None) -> str:
@@ -359,7 +367,7 @@ def per_config(gq, dev, stream, peak):
             gbs = cbytes / (st["us_per_call"] * 1e-6) / 1e9
             pl = plans[arm]
             entry[arm] = {**st, "GBps": round(gbs, 2), "frac": round(gbs / peak, 4),
-                          "kernel": KERNEL_NAMES[pl["engine"]], "engine": pl["engine"],
+                          "kernel": kernel_name(pl), "engine": pl["engine"],
                           "split_mode": pl["split_mode"], "nsplit": pl["nsplit"],
                           "ctas": pl["ctas"],
                           "launches_per_call": 2 if pl["combine_ctas"] else 1}
@@ -399,7 +407,9 @@ def run_gpu(args, rank, world, local):
     dev = torch.device("cuda", torch.cuda.current_device())
     mode = {"auto": gq.MODE_AUTO, "gqa": gq.MODE_GQA, "per_head": gq.MODE_PER_HEAD}[args.mode]
     tuning = {}
-    if args.engine != "auto":
+    if args.engine == "stream":  # the tensor engine's streamed split rule
+        tuning["engine"], tuning["split_mode"] = 2, 3
+    elif args.engine != "auto":
         tuning["engine"] = ENGINES[args.engine]
     if args.split_mode != "auto":
         tuning["split_mode"] = SPLIT_MODES[args.split_mode]
@@ -517,7 +527,7 @@ def run_gpu(args, rank, world, local):
                      "peak_kind": f"{peak_kind} hbm_gbs (copy)",
                      "frac_of_8tbs_nominal": round(achieved / 8000.0, 4),
                      "traffic": traffic, "traffic_source": traffic_src,
-                     "kernel": KERNEL_NAMES[plan["engine"]], "kernel_hash": kernel_hash(),
+                     "kernel": kernel_name(plan), "kernel_hash": kernel_hash(),
                      "duration": "average time of one whole call (main kernel and, when the "
                                  "context is split, the split-combine kernel) over the timed "
                                  "region; the main kernel alone is shorter"},
@@ -567,6 +577,11 @@ def run_gpu_qk(args, rank, world, local):
     scale = w.D ** -0.5
 
     engine = ENGINES[args.engine]
+    # The kernel the library picks (include/gqa_qk.h): streamed on shapes with
+    # at least as many tiles as SMs, else the fixed-split tensor-core kernel.
+    qk_heads = w.G if (mode == gq.MODE_GQA or (mode == gq.MODE_AUTO and w.G > 1)) else 1
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    resolved_engine = engine or (3 if w.B * (w.Hq // qk_heads) >= sms and w.B <= 2048 else 2)
 
     def call(st, attn):
         gq.gqa_qk_softmax_decode(st["q"], st["k"], st["seq_lens"], attn, mode=mode, scale=scale,
@@ -660,10 +675,10 @@ def run_gpu_qk(args, rank, world, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "us_per_call": ms_per_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": (f"{w.v_dtype} K x fp32 q split into {w.v_dtype} hi + lo (tcgen05), fp32 "
-                  "accumulate, fp32 softmax" if (engine or 2) == 2 else
+                  "accumulate, fp32 softmax" if resolved_engine >= 2 else
                   f"{w.v_dtype} K widened to fp32, fp32 FMA, fp32 softmax"), "data": "synthetic",
         "config": {**w.describe(), "op": "qk", "mode": args.mode, "resolved_mode": resolved,
-                   "engine": args.engine, "resolved_engine": engine or 2,
+                   "engine": args.engine, "resolved_engine": resolved_engine,
                    "scale": scale, "parallelism": f"replicas{world}" if world > 1 else "single",
                    "compulsory_bytes_per_call": cbytes, "flops_per_call": flops,
                    "l2": f"rotating {n_sets} input sets, {n_sets * set_bytes / 1e6:.0f} MB "
@@ -673,8 +688,9 @@ def run_gpu_qk(args, rank, world, local):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_kind": f"{peak_kind} hbm_gbs (copy)",
-                     "traffic": committed_traffic_qk(w.name, resolved, engine or 2),
-                     "kernel": "gqa_qk_kernel" if engine == 1 else "gqa_qk_mma_kernel",
+                     "traffic": committed_traffic_qk(w.name, resolved, resolved_engine),
+                     "kernel": {1: "gqa_qk_kernel", 2: "gqa_qk_mma_kernel"}.get(
+                         resolved_engine, "gqa_qk_stream_kernel"),
                      "kernel_hash": kernel_hash(QK_SOURCES),
                      "duration": "average time of one whole call (score kernel and the "
                                  "normalise kernel) over the timed region"},
@@ -1093,11 +1109,12 @@ def main():
                     help="one of: " + ", ".join(W.ALIASES))
     ap.add_argument("--mode", choices=["auto", "gqa", "per_head"], default="auto")
     ap.add_argument("--engine", choices=list(ENGINES), default="auto",
-                    help="kernel: the library's choice, the CUDA-core FMA kernel or the "
-                         "tcgen05 tensor-core kernel")
+                    help="kernel: the library's choice, the CUDA-core FMA kernel, the "
+                         "tcgen05 tensor-core kernel, or the streamed tcgen05 kernel")
     ap.add_argument("--split-mode", choices=list(SPLIT_MODES), default="auto",
                     help="context splits: the library's choice, fixed splits of each "
-                         "sequence, or splits balanced over the batch's lengths")
+                         "sequence, splits balanced over the batch's lengths, or the streamed "
+                         "schedule (tensor-core engine)")
     ap.add_argument("--op", choices=["av", "qk", "attn"], default="av",
                     help="av: the AV reduction (the benchmark); qk: the decode score step "
                          "before it; attn: both fused in one pass over K and V")

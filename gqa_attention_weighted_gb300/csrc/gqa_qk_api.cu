@@ -15,6 +15,7 @@
 #include "gqa_qk.h"
 #include "gqa_qk_kernel.cuh"
 #include "gqa_qk_mma.cuh"
+#include "gqa_qk_stream.cuh"
 
 namespace gqa_av {
 namespace {
@@ -65,6 +66,17 @@ QkKernel pick(int gc) {
 }
 
 template <typename Tag>
+QkKernel pick_stream(int nb) {
+  switch (nb) {
+    case 1: return gqa_qk_stream_kernel<Tag, 1>;
+    case 2: return gqa_qk_stream_kernel<Tag, 2>;
+    case 3: return gqa_qk_stream_kernel<Tag, 3>;
+    case 4: return gqa_qk_stream_kernel<Tag, 4>;
+    default: return nullptr;
+  }
+}
+
+template <typename Tag>
 QkKernel pick_mma(int nb) {
   switch (nb) {
     case 1: return gqa_qk_mma_kernel<Tag, 1>;
@@ -75,10 +87,14 @@ QkKernel pick_mma(int nb) {
   }
 }
 
-constexpr int kQkEngineFma = 1, kQkEngineTensor = 2;
+// Engines: the CUDA-core FMA kernel, the tcgen05 kernel with fixed splits,
+// and the streamed tcgen05 kernel (the default where it applies).
+constexpr int kQkEngineFma = 1, kQkEngineTensor = 2, kQkEngineStream = 3;
 
 struct QkPlan {
   int engine, npad, b_off, tmem_cols, threads;
+  int split_units, lens_off;  // streamed kernel
+  size_t whole_off;           // streamed kernel: byte offset of the whole-tile pairs
   int mode, heads, hgroups, gc, nc, rs, R, stages, parts, rows_per_split, nsplit, tiles;
   int smem, q_off, red_off, bar_off, stage_bytes;
   int norm_rows, norm_ctas_per_b;
@@ -104,10 +120,30 @@ int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int k_dtype, int mode
          QkPlan* p) {
   int rc = check_args(B, Cmax, Hq, Hkv, D, k_dtype, mode);
   if (rc) return rc;
-  if (engine < 0 || engine > kQkEngineTensor)
-    return qfail(GQA_AV_ERR_INVALID, "engine=%d must be 0 (auto), 1 (FMA) or 2 (tensor)", engine);
-  // The tensor-core kernel takes every shape the limits allow; it is the default.
-  p->engine = engine ? engine : kQkEngineTensor;
+  if (engine < 0 || engine > kQkEngineStream)
+    return qfail(GQA_AV_ERR_INVALID,
+                 "engine=%d must be 0 (auto), 1 (FMA), 2 (tensor, fixed splits) or 3 (streamed)",
+                 engine);
+  // The streamed tensor-core kernel is the default on shapes with at least as
+  // many tiles (sequences x head groups) as SMs (measured faster there: the
+  // large batch 2.69 vs 2.90 ms); on fewer tiles the fixed-split kernel was
+  // measured faster (Llama-size 20.8 vs 22.6 us, Phi-style 35.5 vs 37.9 us,
+  // the 4x-L2 traffic shape 153 vs 169 us). It keeps the lengths in shared
+  // memory (at most kStreamMaxB sequences).
+  if (engine == kQkEngineStream && B > kStreamMaxB)
+    return qfail(GQA_AV_ERR_UNSUPPORTED, "the streamed kernel takes at most %d sequences",
+                 kStreamMaxB);
+  {
+    const int G0 = Hq / Hkv;
+    const int heads0 = (mode == GQA_AV_MODE_GQA || (mode == GQA_AV_MODE_AUTO && G0 > 1)) ? G0 : 1;
+    int sms0 = 0;
+    cudaError_t e0 = cudaDeviceGetAttribute(&sms0, cudaDevAttrMultiProcessorCount, dev);
+    if (e0 != cudaSuccess) return qfail_cuda(e0, "cudaDeviceGetAttribute");
+    const bool many_tiles = static_cast<long long>(B) * (Hq / heads0) >= sms0;
+    p->engine = engine ? engine
+                       : (B <= kStreamMaxB && many_tiles ? kQkEngineStream : kQkEngineTensor);
+  }
+  const bool auto_stream = engine == 0 && p->engine == kQkEngineStream;
   const int G = Hq / Hkv;
   p->mode = mode == GQA_AV_MODE_AUTO ? (G > 1 ? GQA_AV_MODE_GQA : GQA_AV_MODE_PER_HEAD) : mode;
   p->heads = p->mode == GQA_AV_MODE_GQA ? G : 1;
@@ -124,14 +160,14 @@ int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int k_dtype, int mode
   p->gc = p->heads / p->nc;
   p->rs = kQkConsumerThreads / p->nc;
   p->parts = D / 64;
-  const bool tensor = p->engine == kQkEngineTensor;
+  const bool tensor = p->engine == kQkEngineTensor || p->engine == kQkEngineStream;
   if (tensor) {
     // 128 context rows (the MMA's M) a stage; N = 2 x heads padded to 16.
     p->R = kQkMmaRows;
     p->npad = (p->heads + 15) / 16 * 16;
     p->tmem_cols = 32;
     while (p->tmem_cols < 4 * p->npad) p->tmem_cols *= 2;
-    p->threads = kQkMmaThreads;
+    p->threads = p->engine == kQkEngineStream ? kQkStreamThreads : kQkMmaThreads;
   } else {
     // One K row per consumer thread and stage, at most 64 KiB a stage, a
     // multiple of 32 rows so a warp is busy or idle as a whole.
@@ -149,6 +185,61 @@ int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int k_dtype, int mode
   const int optin = static_cast<int>(prop.sharedMemPerBlockOptin);
 
   p->tiles = p->hgroups * B;
+  if (p->engine == kQkEngineStream) {
+    // Two CTAs an SM where two fit (registers and shared memory; one at
+    // D = 256, whose 64 KiB stages need the room), in groups of one CTA per
+    // head group, each with as many 128-row stages in flight as its share of
+    // shared memory holds.
+    QkKernel kfn = k_dtype == GQA_AV_BF16 ? pick_stream<Bf16Tag>(p->npad / 16)
+                                          : pick_stream<Fp16Tag>(p->npad / 16);
+    if (!kfn) return qfail(GQA_AV_ERR_UNSUPPORTED, "no score kernel for this head count");
+    cudaError_t e2 = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    if (e2 == cudaSuccess)  // all of the SM's unified memory as shared memory, so two CTAs fit
+      e2 = cudaFuncSetAttribute(kfn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e2 != cudaSuccess) return qfail_cuda(e2, "cudaFuncSetAttribute");
+    for (int per_sm = D <= 128 ? 2 : 1; per_sm >= 1; --per_sm) {
+      const int budget =
+          std::min(optin, static_cast<int>(prop.sharedMemPerMultiprocessor) / per_sm - 1024);
+      // As many stages as the CTA's share of shared memory holds (2 to 8).
+      for (p->stages = kMaxStages; p->stages >= 2; --p->stages) {
+        p->b_off = p->stages * p->stage_bytes;
+        p->red_off = p->b_off + 2 * 2 * p->npad * D * 2;
+        p->bar_off = p->red_off + kMmaAccWarps * p->npad * 8;
+        p->lens_off = p->bar_off + (2 * kMaxStages + 10) * 8 + 32;
+        p->q_off = 0;
+        p->smem = p->lens_off + (B + 1) * 4 + 1024;
+        if (p->smem <= budget || p->stages == 2) break;
+      }
+      int occ = 0;
+      e2 = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kfn, p->threads, p->smem);
+      if (e2 != cudaSuccess) return qfail_cuda(e2, "occupancy query");
+      if (occ >= per_sm || per_sm == 1) {
+        p->split_units = p->hgroups * std::max(1, sms * per_sm / p->hgroups);
+        break;
+      }
+    }
+    p->rows_per_split = p->R;
+    p->nsplit = 1;
+    if (p->smem > optin && auto_stream) {
+      // Too large a query operand to double-buffer next to two stages (64
+      // heads at D = 256): the fixed-split kernel, which keeps one.
+      p->engine = kQkEngineTensor;
+      p->threads = kQkMmaThreads;
+      goto fixed_splits;
+    }
+    if (p->smem > optin)
+      return qfail(GQA_AV_ERR_UNSUPPORTED, "plan needs %d B of shared memory (limit %d)", p->smem,
+                   optin);
+    // Partial pairs: two slots a CTA; then one slot per tile held whole.
+    p->whole_off = static_cast<size_t>(2) * p->split_units * p->heads * sizeof(float2);
+    p->ws_bytes = p->whole_off + static_cast<size_t>(p->tiles) * p->heads * sizeof(float2);
+    p->norm_rows = std::max(1, kQkNormBatch * kQkNormThreads / Hq);
+    p->norm_ctas_per_b = (Cmax + p->norm_rows - 1) / p->norm_rows;
+    if (static_cast<long long>(B) * p->norm_ctas_per_b > 0x7fffffffLL)
+      return qfail(GQA_AV_ERR_UNSUPPORTED, "normalise grid too large");
+    return GQA_AV_OK;
+  }
+fixed_splits:
   // FMA kernel: one CTA per SM on few-tile shapes. Tensor-core kernel: on
   // short streams with D <= 128 (at most 2048 rows a CTA at two CTAs per SM),
   // about two CTAs per SM with a ring of about 96 KiB; otherwise, like the FMA
@@ -320,7 +411,7 @@ extern "C" int gqa_qk_softmax_decode_tuned(const float* q, const void* k_cache,
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return qfail_cuda(e, "cudaGetDevice");
-  QkPlan pl;
+  QkPlan pl{};
   if ((rc = plan(dev, B, Cmax, Hq, Hkv, D, k_dtype, mode, engine, &pl))) return rc;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   Ws ws;
@@ -342,9 +433,15 @@ extern "C" int gqa_qk_softmax_decode_tuned(const float* q, const void* k_cache,
   p.timeout_ns = kQkTimeoutNs;
   p.b_off = pl.b_off;
   p.tmem_cols = static_cast<uint32_t>(pl.tmem_cols);
+  p.split_units = pl.split_units;
+  p.lens_off = static_cast<uint32_t>(pl.lens_off);
+  p.stats_whole = reinterpret_cast<float2*>(static_cast<char*>(ws.base) + kQkHeaderBytes +
+                                            pl.whole_off);
 
   QkKernel k;
-  if (pl.engine == kQkEngineTensor)
+  if (pl.engine == kQkEngineStream)
+    k = k_dtype == GQA_AV_BF16 ? pick_stream<Bf16Tag>(pl.npad / 16) : pick_stream<Fp16Tag>(pl.npad / 16);
+  else if (pl.engine == kQkEngineTensor)
     k = k_dtype == GQA_AV_BF16 ? pick_mma<Bf16Tag>(pl.npad / 16) : pick_mma<Fp16Tag>(pl.npad / 16);
   else
     k = k_dtype == GQA_AV_BF16 ? pick<Bf16Tag>(pl.gc) : pick<Fp16Tag>(pl.gc);
@@ -352,8 +449,10 @@ extern "C" int gqa_qk_softmax_decode_tuned(const float* q, const void* k_cache,
   e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
   if (e != cudaSuccess) return qfail_cuda(e, "cudaFuncSetAttribute");
   void* args1[] = {&p};
-  e = launch_pdl(reinterpret_cast<const void*>(k), dim3(pl.tiles * pl.nsplit), dim3(pl.threads),
-                 pl.smem, stream, args1);
+  const unsigned grid1 = pl.engine == kQkEngineStream ? static_cast<unsigned>(pl.split_units)
+                                                      : static_cast<unsigned>(pl.tiles * pl.nsplit);
+  e = launch_pdl(reinterpret_cast<const void*>(k), dim3(grid1), dim3(pl.threads), pl.smem, stream,
+                 args1);
   if (e != cudaSuccess) return qfail_cuda(e, "score kernel launch");
 
   QkNormParams n;
@@ -363,8 +462,12 @@ extern "C" int gqa_qk_softmax_decode_tuned(const float* q, const void* k_cache,
   n.B = B; n.Cmax = Cmax; n.Hq = Hq; n.heads = pl.heads; n.hgroups = pl.hgroups;
   n.rows_per_split = pl.rows_per_split; n.nsplit = pl.nsplit;
   n.rows_per_cta = pl.norm_rows; n.ctas_per_b = pl.norm_ctas_per_b;
+  n.split_units = pl.split_units;
+  n.stats_whole = p.stats_whole;
   void* args2[] = {&n};
-  e = launch_pdl(reinterpret_cast<const void*>(gqa_qk_normalize_kernel),
+  e = launch_pdl(pl.engine == kQkEngineStream
+                     ? reinterpret_cast<const void*>(gqa_qk_stream_normalize)
+                     : reinterpret_cast<const void*>(gqa_qk_normalize_kernel),
                  dim3(B * pl.norm_ctas_per_b), dim3(kQkNormThreads), 0, stream, args2);
   if (e != cudaSuccess) return qfail_cuda(e, "normalise kernel launch");
   return GQA_AV_OK;

@@ -58,9 +58,14 @@ struct alignas(64) QkParams {
   uint32_t stage_bytes;         // R * D * 2
   uint32_t q_off, red_off, bar_off;  // shared-memory offsets from the 1024-aligned base
   long long timeout_ns;
-  // Tensor-core kernel only.
+  // Tensor-core kernels only.
   uint32_t b_off;               // shared-memory offset of the B (query hi / lo) operand
   uint32_t tmem_cols;           // tensor-memory columns allocated (power of 2 >= 4 x Npad)
+  // Streamed kernel only: CTAs (groups of hgroups), lengths in shared memory,
+  // the (max, sum) of each tile one CTA held whole [B][hgroups][heads].
+  int split_units;
+  uint32_t lens_off;
+  float2* stats_whole;
 };
 
 struct QkNormParams {
@@ -70,6 +75,8 @@ struct QkNormParams {
   int B, Cmax, Hq, heads, hgroups, rows_per_split, nsplit;
   int rows_per_cta;             // context rows each CTA rewrites
   int ctas_per_b;
+  int split_units;              // streamed kernel: its CTAs
+  const float2* stats_whole;    // streamed kernel: as QkParams::stats_whole
 };
 
 // Merge of two (max, sum of exp(x - max)) pairs.

@@ -26,7 +26,7 @@
  *
  * Numerics. K is widened exactly (bf16/fp16 -> fp32). The CUDA-core FMA
  * kernel (engine 1) forms the products and sums over d in fp32. The tcgen05
- * tensor-core kernel (engine 2, the default) splits each fp32 query value
+ * tensor-core kernels (engines 2 and 3, the defaults) split each fp32 query value
  * into two 16-bit values of K's type, hi = round(q) and lo = round(q - hi),
  * so the query keeps about 16 (bf16) or 22 (fp16) significant bits; K x hi
  * and K x lo are exact in fp32 and accumulated over d in fp32 in tensor
@@ -42,7 +42,8 @@
  *
  * Execution: asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  * default stream), no host synchronisation. The call keeps its own
- * per-device workspace (per-split softmax pairs and a status word), grown on
+ * per-device workspace (per-split or per-segment softmax pairs and a status
+ * word), grown on
  * demand with cudaMalloc outside stream capture; calls that may overlap on the
  * GPU must not be issued concurrently. Errors: a status code from gqa_av.h;
  * on error nothing is launched and gqa_qk_last_error() holds a message.
@@ -63,10 +64,14 @@ int gqa_qk_softmax_decode(const float *q, const void *k_cache, const int32_t *se
                           float scale, int mode, void *stream);
 
 /* The same with the kernel chosen: engine 0 lets the library pick (the
- * tensor-core kernel), 1 forces the CUDA-core FMA kernel, 2 the tcgen05
- * tensor-core kernel (K rows as the A operand in place, the queries split
- * into 16-bit hi and lo halves as B). Both give results within the stated
- * tolerance. */
+ * streamed tensor-core kernel on shapes with at least as many tiles --
+ * sequences x head groups -- as SMs and at most 2048 sequences, else the
+ * fixed-split one), 1 forces the CUDA-core FMA kernel, 2 the tcgen05 tensor-core kernel
+ * with fixed context splits (K rows as the A operand in place, the queries
+ * split into 16-bit hi and lo halves as B), 3 the streamed tcgen05 kernel
+ * (the same products; persistent CTAs, two an SM where they fit, each taking
+ * an equal run of its head group's 128-row stages across sequences; at most
+ * 2048 sequences). All give results within the stated tolerance. */
 int gqa_qk_softmax_decode_tuned(const float *q, const void *k_cache, const int32_t *seq_lens,
                                 float *attn, int B, int Cmax, int Hq, int Hkv, int D,
                                 int k_dtype, float scale, int mode, int engine, void *stream);

@@ -61,8 +61,8 @@ def check(got, ref, lens, what):
 SWEEP = [(g, d) for g in (1, 2, 3, 4, 8, 16, 32, 64) for d in (64, 128, 256)] + [(5, 256), (12, 128), (24, 64)]
 
 
-ENGINES = [0, 1, 2]
-ENGINE_IDS = ["auto", "fma", "tensor"]
+ENGINES = [0, 1, 2, 3]
+ENGINE_IDS = ["auto", "fma", "tensor", "stream"]
 
 
 @pytest.mark.parametrize("engine", ENGINES, ids=ENGINE_IDS)
@@ -77,11 +77,19 @@ def test_score_step_shape_sweep(gq, G, D, engine):
         scale = D ** -0.5
         ref = gqa_qk.gqa_qk_softmax(q.numpy(), bits(k), kd, sl.numpy(), scale)
         for mode in (0, 1):
+            if engine == 3 and mode == 1 and G == 64 and D == 256:
+                # 64 heads at D = 256: the streamed kernel's double-buffered
+                # queries and two 64 KiB stages exceed shared memory; auto
+                # takes the fixed-split kernel there (checked with engine 0).
+                with pytest.raises(gq.GqaAvError) as e:
+                    run_qk(gq, q, k, sl, mode, engine=engine)
+                assert e.value.status == 2 and "shared memory" in str(e.value)
+                continue
             got = run_qk(gq, q, k, sl, mode, engine=engine)
             check(got, ref, lens, f"G={G} D={D} {kd} mode={mode} engine={engine}")
 
 
-@pytest.mark.parametrize("engine", [1, 2], ids=["fma", "tensor"])
+@pytest.mark.parametrize("engine", [1, 2, 3], ids=["fma", "tensor", "stream"])
 @pytest.mark.parametrize("L", [0, 1, 2, 31, 32, 33, 127, 128, 129, 255, 256, 257, 1000, 4095, 4096])
 def test_score_step_lengths(gq, L, engine):
     rng = np.random.default_rng(L + 3)
@@ -92,7 +100,7 @@ def test_score_step_lengths(gq, L, engine):
     check(run_qk(gq, q, k, sl, engine=engine), ref, lens, f"L={L} engine={engine}")
 
 
-@pytest.mark.parametrize("engine", [1, 2], ids=["fma", "tensor"])
+@pytest.mark.parametrize("engine", [1, 2, 3], ids=["fma", "tensor", "stream"])
 def test_score_step_null_lengths_clamping_scale_and_determinism(gq, engine):
     rng = np.random.default_rng(7)
     B, C, Hq, Hkv, D = 3, 300, 8, 2, 64
@@ -112,7 +120,7 @@ def test_score_step_null_lengths_clamping_scale_and_determinism(gq, engine):
     check(run_qk(gq, q, k, None, 0, 0.3, engine=engine), full, None, "per-head")
 
 
-@pytest.mark.parametrize("engine", [1, 2], ids=["fma", "tensor"])
+@pytest.mark.parametrize("engine", [1, 2, 3], ids=["fma", "tensor", "stream"])
 @pytest.mark.parametrize("name", ["small", "llama", "phi", "mqa"])
 def test_score_step_workload_shapes(gq, name, engine):
     """The AV workloads' shapes, with K drawn like V, and the chained call:
@@ -154,3 +162,30 @@ def test_score_step_errors_launch_nothing(gq):
     assert e.value.status == 2
     torch.cuda.synchronize()
     assert torch.all(attn == SENTINEL)
+
+
+# The streamed kernel over batches past one and several warps of lengths (its
+# first stage is found by a warp scan over the lengths), empty sequences, one
+# long sequence among short ones, and fewer stages than CTAs.
+@pytest.mark.parametrize("B,kind", [(33, "mix"), (70, "mix"), (40, "one_long"), (5, "all_empty"),
+                                    (3, "short")])
+def test_score_step_streamed_over_the_batch(gq, B, kind):
+    rng = np.random.default_rng(B)
+    C, Hq, Hkv, D = 700, 16, 4, 64
+    if kind == "one_long":
+        lens = [3] * B
+        lens[B // 2] = C
+    elif kind == "all_empty":
+        lens = [0] * B
+    elif kind == "short":
+        lens = [1, 0, 5]
+    else:
+        lens = list(rng.integers(0, C + 1, size=B))
+        lens[3] = 0
+        lens[7 % B] = C
+    q, k, sl = qk_case(rng, B, C, Hq, Hkv, D, "bf16", lens)
+    ref = gqa_qk.gqa_qk_softmax(q.numpy(), bits(k), "bf16", sl.numpy(), D ** -0.5)
+    for mode in (0, 1):
+        a = run_qk(gq, q, k, sl, mode, engine=3)
+        check(a, ref, lens, f"B={B} {kind} mode={mode}")
+        assert np.array_equal(run_qk(gq, q, k, sl, mode, engine=3), a), "not reproducible"
