@@ -51,6 +51,8 @@ __host__ __device__ constexpr int consumer_warps(int gc) { return gc >= 12 ? 8 :
 __host__ __device__ constexpr int cta_threads(int gc) { return 32 * (consumer_warps(gc) + 1); }
 constexpr int kMaxStages = 8;
 constexpr int kCombineThreads = 128;
+// Partials a combine thread loads at once.
+constexpr int kCombineBatch = 8;
 
 // Device status word bits.
 constexpr unsigned kErrFullWait = 1u;
@@ -333,7 +335,7 @@ __device__ __forceinline__ void add4(float4& s, const float4 x) {
 template <bool kGlobal>
 __device__ __forceinline__ void sum_strided(float4& s, const float4* src, size_t stride, int lo,
                                             int hi) {
-  constexpr int kBatch = 8;
+  constexpr int kBatch = kCombineBatch;
   for (int i0 = lo; i0 < hi; i0 += kBatch) {
     float4 x[kBatch];
 #pragma unroll
