@@ -247,7 +247,10 @@ fixed_splits:
   // faster in its regime).
   const long long tile_rows = static_cast<long long>(p->tiles) * Cmax;
   const bool short_tc = tensor && D <= 128 && tile_rows <= 2048LL * 2 * sms;
-  long long want = short_tc ? (2LL * sms + p->tiles - 1) / p->tiles
+  // Short streams: at most two CTAs per SM in all, so that every split is
+  // resident from the start (rounding up made a 32-tile ragged batch 320 CTAs
+  // for 304 slots, and the 16 that waited for a slot added a second wave).
+  long long want = short_tc ? std::max(1, 2 * sms / p->tiles)
                    : p->tiles < sms ? std::max(1, sms / p->tiles)
                                     : (2LL * sms + p->tiles - 1) / p->tiles;
   want = std::max<long long>(1, std::min<long long>(want, (Cmax + p->R - 1) / p->R));

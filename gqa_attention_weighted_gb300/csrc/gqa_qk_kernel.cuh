@@ -20,7 +20,8 @@
 // head for its split.
 //
 // gqa_qk_normalize_kernel (launched next, programmatic dependent launch):
-// combines the splits' (max, sum) pairs of each (b, q_h) in split order and
+// combines the splits' (max, sum) pairs of each (b, q_h) (M the largest max,
+// S the sum of each split's sum rescaled to M, both in a fixed order) and
 // rewrites attn[b, c, :] = exp(s - M) / S for the in-range rows. Entries at
 // c >= L_b are never written. Results are bitwise reproducible for a fixed
 // launch shape.
@@ -86,6 +87,31 @@ __device__ __forceinline__ void lse_merge(float& m, float& l, float m2, float l2
   const float b = m2 == -INFINITY ? 0.0f : l2 * __expf(m2 - mn);
   m = mn;
   l = a + b;
+}
+
+// The (max, sum of exp(x - max)) of the pairs held by a warp's lanes: the
+// maximum first, then every lane's sum rescaled to it and added up, each by a
+// fixed butterfly (so bitwise reproducible). One exponential a lane, against
+// one a level for a butterfly of pair merges.
+__device__ __forceinline__ float2 warp_lse(float m, float l) {
+  float M = m;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float s = m == -INFINITY ? 0.0f : l * __expf(m - M);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return make_float2(M, s);
+}
+
+// The same over `n` pairs in memory, in index order.
+__device__ __forceinline__ float2 lse_of(const float2* v, int n, int stride) {
+  float M = -INFINITY, S = 0.0f;
+  for (int i = 0; i < n; ++i) M = fmaxf(M, v[(size_t)i * stride].x);
+  for (int i = 0; i < n; ++i) {
+    const float2 x = v[(size_t)i * stride];
+    if (x.x != -INFINITY) S += x.y * __expf(x.x - M);
+  }
+  return make_float2(M, S);
 }
 
 // ---------------------------------------------------------------------------
@@ -280,11 +306,98 @@ __global__ void __launch_bounds__(kQkThreads, 1) gqa_qk_kernel(const __grid_cons
 }
 
 // ---------------------------------------------------------------------------
+// The normalise step of one CTA (sequence b, rows [c0, c1)), shared by the
+// fixed-split and streamed score kernels: every head of b has `nseg` (max,
+// sum) pairs, pair (h, i) at slot(h / heads, i)[h % heads] (the heads of one
+// slot contiguous). Three steps, with one round of global loads before the
+// first:
+//   1. the block's scores into registers (rows_per_cta * Hq is at most
+//      kQkNormBatch * kQkNormThreads: one batch of loads a thread), and every
+//      pair into shared memory (a slot's heads are adjacent addresses), all
+//      loads in flight together;
+//   2. per head M = max_i m_i, then S = sum_i l_i exp(m_i - M), with `tph`
+//      threads a head (a power of two up to 32) taking segments part, part +
+//      tph, ... and fixed butterflies over them;
+//   3. attn = exp(s - M) / S over the block's rows.
+// ---------------------------------------------------------------------------
+template <typename Slot>
+__device__ __forceinline__ void qk_normalize_rows(float* attn_b, int Hq, int heads, int nseg,
+                                                  int c0, int c1, Slot slot) {
+  __shared__ float2 ms[kQkMaxHeads * 32];   // (M, 1 / S) per head, Hq <= 2048
+  __shared__ float2 pairs[kQkNormMaxPairs];
+  const int tid = threadIdx.x;
+  const int n = (c1 - c0) * Hq;
+  float* row0 = attn_b + (size_t)c0 * Hq;
+  float x[kQkNormBatch];
+#pragma unroll
+  for (int u = 0; u < kQkNormBatch; ++u) {
+    const int i = tid + u * kQkNormThreads;
+    x[u] = i < n ? __ldcg(row0 + i) : 0.0f;
+  }
+  const int per_k = nseg * heads;
+  const int npairs = Hq * nseg;
+  const bool staged = npairs <= kQkNormMaxPairs;
+  if (staged) {
+    for (int i0 = tid; i0 < npairs; i0 += kQkNormBatch * kQkNormThreads) {
+      float2 v[kQkNormBatch];
+#pragma unroll
+      for (int u = 0; u < kQkNormBatch; ++u) {
+        const int i = i0 + u * kQkNormThreads;
+        if (i < npairs) {
+          const int k = i / per_k, r = i - k * per_k;
+          const int seg = r / heads;
+          v[u] = __ldcg(slot(k, seg) + (r - seg * heads));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kQkNormBatch; ++u) {
+        const int i = i0 + u * kQkNormThreads;
+        if (i < npairs) pairs[i] = v[u];
+      }
+    }
+  }
+  __syncthreads();
+  auto pair = [&](int h, int seg) {
+    const int k = h / heads, hh = h - k * heads;
+    return staged ? pairs[(k * nseg + seg) * heads + hh] : __ldcg(slot(k, seg) + hh);
+  };
+  int tph = 1;
+  while (tph < 32 && 2 * tph * Hq <= kQkNormThreads) tph *= 2;
+  const int part = tid & (tph - 1);
+  // The loop's trip count is the same for every thread, so whole warps take
+  // the shuffles; threads past Hq carry (-inf, 0).
+  for (int hb = 0; hb < Hq; hb += kQkNormThreads / tph) {
+    const int h = hb + tid / tph;
+    const bool valid = h < Hq;
+    float M = -INFINITY;
+    if (valid)
+      for (int i = part; i < nseg; i += tph) M = fmaxf(M, pair(h, i).x);
+    for (int o = tph >> 1; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float S = 0.0f;
+    if (valid)
+      for (int i = part; i < nseg; i += tph) {
+        const float2 v = pair(h, i);
+        if (v.x != -INFINITY) S += v.y * __expf(v.x - M);
+      }
+    for (int o = tph >> 1; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+    if (valid && part == 0) ms[h] = make_float2(M, 1.0f / S);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int u = 0; u < kQkNormBatch; ++u) {
+    const int i = tid + u * kQkNormThreads;
+    if (i < n) {
+      const float2 v = ms[i % Hq];
+      row0[i] = expf(x[u] - v.x) * v.y;
+    }
+  }
+}
+
 // CTA (b, block of rows): the (max, sum) of every head of b from the splits
-// of its tiles, in split order, then exp(s - M) / S over the block's rows.
+// of its tiles (pairs [tile = hg * B + b][split][heads]), then exp(s - M) / S
+// over the block's rows.
 __global__ void __launch_bounds__(kQkNormThreads)
 gqa_qk_normalize_kernel(const __grid_constant__ QkNormParams p) {
-  __shared__ float2 ms[kQkMaxHeads * 32];  // (M, 1 / S) per head, heads <= Hq <= 2048
   const int b = blockIdx.x / p.ctas_per_b;
   const int blk = blockIdx.x - b * p.ctas_per_b;
   const int L = clamped_len(p.seq_lens, b, p.Cmax);
@@ -294,68 +407,10 @@ gqa_qk_normalize_kernel(const __grid_constant__ QkNormParams p) {
   const int c0 = blk * p.rows_per_cta;
   const int c1 = min(c0 + p.rows_per_cta, L);
   if (c0 >= c1) return;
-  // Every (head, split) pair of b in one round of loads into shared memory
-  // (when they fit), then one warp per head merges its splits: lanes take
-  // splits s, s + 32, ... in split order, then a fixed butterfly.
-  __shared__ float2 pairs[kQkNormMaxPairs];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int npairs = p.Hq * nsplit_b;
-  const bool staged = npairs <= kQkNormMaxPairs;
-  auto pair_at = [&](int h, int s) {
-    const int hg = h / p.heads, hh = h - hg * p.heads;
-    return p.stats + ((size_t)(hg * p.B + b) * p.nsplit + s) * p.heads + hh;
-  };
-  if (staged) {
-    for (int i0 = threadIdx.x; i0 < npairs; i0 += kQkNormBatch * kQkNormThreads) {
-      float2 v[kQkNormBatch];
-#pragma unroll
-      for (int u = 0; u < kQkNormBatch; ++u) {
-        const int i = i0 + u * kQkNormThreads;
-        if (i < npairs) v[u] = __ldcg(pair_at(i / nsplit_b, i % nsplit_b));
-      }
-#pragma unroll
-      for (int u = 0; u < kQkNormBatch; ++u) {
-        const int i = i0 + u * kQkNormThreads;
-        if (i < npairs) pairs[i] = v[u];
-      }
-    }
-    __syncthreads();
-  }
-  for (int h = warp; h < p.Hq; h += kQkNormThreads / 32) {
-    float M = -INFINITY, S = 0.0f;
-    for (int s = lane; s < nsplit_b; s += 32) {
-      const float2 v = staged ? pairs[h * nsplit_b + s] : __ldcg(pair_at(h, s));
-      lse_merge(M, S, v.x, v.y);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
-      const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
-      lse_merge(M, S, m2, s2);
-    }
-    if (lane == 0) ms[h] = make_float2(M, 1.0f / S);
-  }
-  __syncthreads();
-  // The block's rows are contiguous: each thread loads its (at most
-  // kQkNormBatch) scores together, then rewrites them.
-  const int n = (c1 - c0) * p.Hq;
-  float* row0 = p.attn + ((size_t)b * p.Cmax + c0) * p.Hq;
-  for (int i0 = threadIdx.x; i0 < n; i0 += kQkNormBatch * kQkNormThreads) {
-    float x[kQkNormBatch];
-#pragma unroll
-    for (int u = 0; u < kQkNormBatch; ++u) {
-      const int i = i0 + u * kQkNormThreads;
-      x[u] = i < n ? __ldcg(row0 + i) : 0.0f;
-    }
-#pragma unroll
-    for (int u = 0; u < kQkNormBatch; ++u) {
-      const int i = i0 + u * kQkNormThreads;
-      if (i < n) {
-        const float2 v = ms[i % p.Hq];
-        row0[i] = expf(x[u] - v.x) * v.y;
-      }
-    }
-  }
+  qk_normalize_rows(p.attn + (size_t)b * p.Cmax * p.Hq, p.Hq, p.heads, nsplit_b, c0, c1,
+                    [&](int hg, int s) {
+                      return p.stats + ((size_t)(hg * p.B + b) * p.nsplit + s) * p.heads;
+                    });
 }
 
 }  // namespace gqa_av

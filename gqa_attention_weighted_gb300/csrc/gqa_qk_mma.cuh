@@ -132,6 +132,22 @@ __global__ void __launch_bounds__(kQkMmaThreads, 1)
   grid_dependency_wait();
   grid_launch_dependents();
 
+  // The first stages do not depend on the length: the producer issues them
+  // before its load of seq_lens (measured: the load delayed the first copy
+  // by about 0.8 us).
+  auto issue = [&](int stage, int c0) {
+    if (lane == 0) {
+      const uint32_t full = full0 + 8 * stage;
+      mbar_arrive_expect_tx(full, p.stage_bytes);
+      const uint32_t dst = base_s + (uint32_t)stage * p.stage_bytes;
+      for (int part = 0; part < p.parts; ++part)
+        tma_load_4d(dst + (uint32_t)part * kQkMmaRows * 128, &p.k_map, 64 * part, kv_h, c0, b,
+                    full, policy);
+    }
+  };
+  if (warp == producer_warp)
+    for (int it = 0; it < pre; ++it) issue(it, c_begin + it * kQkMmaRows);
+
   const int L = clamped_len(p.seq_lens, b, p.Cmax);
   const int nsplit_b = L > 0 ? (L + p.rows_per_split - 1) / p.rows_per_split : 1;
   const int c_end = min(c_begin + p.rows_per_split, L);
@@ -140,17 +156,6 @@ __global__ void __launch_bounds__(kQkMmaThreads, 1)
 
   if (warp == producer_warp) {
     // ----------------------------------------------------------------- producer
-    auto issue = [&](int stage, int c0) {
-      if (lane == 0) {
-        const uint32_t full = full0 + 8 * stage;
-        mbar_arrive_expect_tx(full, p.stage_bytes);
-        const uint32_t dst = base_s + (uint32_t)stage * p.stage_bytes;
-        for (int part = 0; part < p.parts; ++part)
-          tma_load_4d(dst + (uint32_t)part * kQkMmaRows * 128, &p.k_map, 64 * part, kv_h, c0, b,
-                      full, policy);
-      }
-    };
-    for (int it = 0; it < pre; ++it) issue(it, c_begin + it * kQkMmaRows);
     bool ok = true;
     int issued = pre;
     for (int it = pre; it < n_iters; ++it) {
@@ -301,28 +306,18 @@ __global__ void __launch_bounds__(kQkMmaThreads, 1)
     }
   }
 
-  // One (max, sum) per head for the split: over each warp's lanes, then over
-  // the four warps in warp order.
+  // One (max, sum) per head of the group (not the padding up to N) for the
+  // split: over each warp's lanes, then over the four warps in warp order.
 #pragma unroll
   for (int n = 0; n < N; ++n) {
-    float mm = mx[n], ll = sm[n];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, mm, o);
-      const float l2 = __shfl_xor_sync(0xffffffffu, ll, o);
-      lse_merge(mm, ll, m2, l2);
+    if (n < p.heads) {
+      const float2 r = warp_lse(mx[n], sm[n]);
+      if (lane == 0) red[(size_t)warp * N + n] = r;
     }
-    if (lane == 0) red[(size_t)warp * N + n] = make_float2(mm, ll);
   }
   named_sync(1, 32 * kMmaAccWarps);
-  if (tid < p.heads && ok && n_iters > 0) {
-    float mm = -INFINITY, ll = 0.0f;
-    for (int w = 0; w < kMmaAccWarps; ++w) {
-      const float2 v = red[(size_t)w * N + tid];
-      lse_merge(mm, ll, v.x, v.y);
-    }
-    p.stats[((size_t)tile * p.nsplit + split) * p.heads + tid] = make_float2(mm, ll);
-  }
+  if (tid < p.heads && ok && n_iters > 0)
+    p.stats[((size_t)tile * p.nsplit + split) * p.heads + tid] = lse_of(red + tid, kMmaAccWarps, N);
   tc_fence_before();
   mma_team_sync();
 }

@@ -18,7 +18,7 @@
 // end the CTA writes the segment's (max, sum of exp) per head: for a segment
 // that is its whole tile to the tile's own slot, for a cut one to slot 2u
 // (the CTA's first segment) or 2u + 1 (its last). gqa_qk_stream_normalize
-// merges a tile's pairs in group order and rewrites the scores, so the
+// merges a tile's pairs in a fixed order and rewrites the scores, so the
 // result is bitwise reproducible.
 //
 // Per stage of 128 context rows the CTA computes
@@ -348,29 +348,19 @@ __global__ void __launch_bounds__(kQkStreamThreads, 1)
 #pragma unroll
       for (int n = 0; n < N; ++n) {
         if (n < p.heads) {  // the group's heads only (N pads them to 16)
-          float mm = mx[n], ll = sm[n];
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, mm, o);
-            const float l2 = __shfl_xor_sync(0xffffffffu, ll, o);
-            lse_merge(mm, ll, m2, l2);
-          }
-          if (lane == 0) red[(size_t)warp * N + n] = make_float2(mm, ll);
+          const float2 r = warp_lse(mx[n], sm[n]);
+          if (lane == 0) red[(size_t)warp * N + n] = r;
         }
         mx[n] = -INFINITY;
         sm[n] = 0.0f;
       }
       named_sync(1, 32 * kMmaAccWarps);
       if (tid < p.heads) {
-        float mm = -INFINITY, ll = 0.0f;
-        for (int w = 0; w < kMmaAccWarps; ++w) {
-          const float2 v = red[(size_t)w * N + tid];
-          lse_merge(mm, ll, v.x, v.y);
-        }
         const bool whole = seg_j0 == 0 && tile_end;
         float2* dst = whole ? p.stats_whole + ((size_t)cur.b * K + hg) * p.heads
                             : p.stats + (size_t)(2 * u + (first_segment ? 0 : 1)) * p.heads;
-        if (!*abort_flag) dst[tid] = make_float2(mm, ll);
+        const float2 r = lse_of(red + tid, kMmaAccWarps, N);
+        if (!*abort_flag) dst[tid] = r;
       }
       named_sync(1, 32 * kMmaAccWarps);  // red is reused by the next segment
       first_segment = false;
@@ -384,12 +374,11 @@ __global__ void __launch_bounds__(kQkStreamThreads, 1)
 
 // ---------------------------------------------------------------------------
 // CTA (b, block of rows): the (max, sum) of every head of b, merged over the
-// segments of its tile in group order (the tile's own slot when one CTA held
-// it whole), then exp(s - M) / S over the block's rows.
+// segments of its tile (the tile's own slot when one CTA held it whole), then
+// exp(s - M) / S over the block's rows.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kQkNormThreads)
     gqa_qk_stream_normalize(const __grid_constant__ QkNormParams p) {
-  __shared__ float2 ms[kQkMaxHeads * 32];  // (M, 1 / S) per head, heads <= Hq <= 2048
   __shared__ long long span[2];            // stages of a column in all, and before b
   const int b = blockIdx.x / p.ctas_per_b;
   const int blk = blockIdx.x - b * p.ctas_per_b;
@@ -417,68 +406,15 @@ __global__ void __launch_bounds__(kQkNormThreads)
   const int c0 = blk * p.rows_per_cta;
   const int c1 = min(c0 + p.rows_per_cta, L);
   if (c0 >= c1) return;
-  // Every (head, segment) pair of b in one round of loads into shared
-  // memory, then one warp per head merges its segments: lanes take segments
-  // g0 + lane, g0 + lane + 32, ... in order, then a fixed butterfly.
-  __shared__ float2 pairs[kQkNormMaxPairs];
+  // Segment i of head group k: the tile's own slot when one CTA held it
+  // whole, else slot 2 (g K + k) of group g = g0 + i (2 (g0 K + k) + 1 for
+  // the first when the tile does not start g0's range).
   const int nseg = g0 == g1 ? 1 : g1 - g0 + 1;
-  const int npairs = p.Hq * nseg;
-  const bool staged = npairs <= kQkNormMaxPairs;
-  auto pair_at = [&](int h, int i) {
-    const int k = h / p.heads, hh = h - k * p.heads;
-    if (g0 == g1) return p.stats_whole + ((size_t)b * K + k) * p.heads + hh;
-    const int g = g0 + i;
-    return p.stats + (size_t)(2 * (g * K + k) + (i == 0 ? adj : 0)) * p.heads + hh;
-  };
-  if (staged) {
-    for (int i0 = threadIdx.x; i0 < npairs; i0 += kQkNormBatch * kQkNormThreads) {
-      float2 v[kQkNormBatch];
-#pragma unroll
-      for (int t = 0; t < kQkNormBatch; ++t) {
-        const int i = i0 + t * kQkNormThreads;
-        if (i < npairs) v[t] = __ldcg(pair_at(i / nseg, i - (i / nseg) * nseg));
-      }
-#pragma unroll
-      for (int t = 0; t < kQkNormBatch; ++t) {
-        const int i = i0 + t * kQkNormThreads;
-        if (i < npairs) pairs[i] = v[t];
-      }
-    }
-    __syncthreads();
-  }
-  for (int h = warp; h < p.Hq; h += kQkNormThreads / 32) {
-    float M = -INFINITY, S = 0.0f;
-    for (int i = lane; i < nseg; i += 32) {
-      const float2 v = staged ? pairs[h * nseg + i] : __ldcg(pair_at(h, i));
-      lse_merge(M, S, v.x, v.y);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, M, o);
-      const float s2 = __shfl_xor_sync(0xffffffffu, S, o);
-      lse_merge(M, S, m2, s2);
-    }
-    if (lane == 0) ms[h] = make_float2(M, 1.0f / S);
-  }
-  __syncthreads();
-  const int n = (c1 - c0) * p.Hq;
-  float* row0 = p.attn + ((size_t)b * p.Cmax + c0) * p.Hq;
-  for (int i0 = threadIdx.x; i0 < n; i0 += kQkNormBatch * kQkNormThreads) {
-    float x[kQkNormBatch];
-#pragma unroll
-    for (int v = 0; v < kQkNormBatch; ++v) {
-      const int i = i0 + v * kQkNormThreads;
-      x[v] = i < n ? __ldcg(row0 + i) : 0.0f;
-    }
-#pragma unroll
-    for (int v = 0; v < kQkNormBatch; ++v) {
-      const int i = i0 + v * kQkNormThreads;
-      if (i < n) {
-        const float2 w = ms[i % p.Hq];
-        row0[i] = expf(x[v] - w.x) * w.y;
-      }
-    }
-  }
+  qk_normalize_rows(p.attn + (size_t)b * p.Cmax * p.Hq, p.Hq, p.heads, nseg, c0, c1,
+                    [&](int k, int i) {
+                      if (g0 == g1) return p.stats_whole + ((size_t)b * K + k) * p.heads;
+                      return p.stats + (size_t)(2 * ((g0 + i) * K + k) + (i == 0 ? adj : 0)) * p.heads;
+                    });
 }
 
 }  // namespace gqa_av
