@@ -581,7 +581,9 @@ def run_gpu_qk(args, rank, world, local):
     # at least as many tiles as SMs, else the fixed-split tensor-core kernel.
     qk_heads = w.G if (mode == gq.MODE_GQA or (mode == gq.MODE_AUTO and w.G > 1)) else 1
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    resolved_engine = engine or (3 if w.B * (w.Hq // qk_heads) >= sms and w.B <= 2048 else 2)
+    qk_tiles = w.B * (w.Hq // qk_heads)
+    short_few = qk_tiles < sms and w.D <= 128 and qk_tiles * w.Cmax <= 2048 * 2 * sms
+    resolved_engine = engine or (3 if w.B <= 2048 and not short_few else 2)
 
     def call(st, attn):
         gq.gqa_qk_softmax_decode(st["q"], st["k"], st["seq_lens"], attn, mode=mode, scale=scale,

@@ -116,6 +116,39 @@ int check_args(int B, int Cmax, int Hq, int Hkv, int D, int k_dtype, int mode) {
   return GQA_AV_OK;
 }
 
+// CTAs of `threads` threads and `smem` bytes of dynamic shared memory that
+// one SM holds by its shared memory, registers and threads (registers are
+// given out per warp in units of 256).
+int resident_ctas(const void* fn, int threads, int smem, const cudaDeviceProp& prop) {
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return 0;
+  const int warps = (threads + 31) / 32;
+  const long long regs_cta = (static_cast<long long>(fa.numRegs) * 32 + 255) / 256 * 256 * warps;
+  const long long smem_cta =
+      static_cast<long long>(smem) + fa.sharedSizeBytes + prop.reservedSharedMemPerBlock;
+  long long n = prop.maxThreadsPerMultiProcessor / (32LL * warps);
+  if (regs_cta > 0) n = std::min(n, prop.regsPerMultiprocessor / regs_cta);
+  if (smem_cta > 0) n = std::min<long long>(n, static_cast<long long>(prop.sharedMemPerMultiprocessor) / smem_cta);
+  return static_cast<int>(n);
+}
+
+// Normalise launch: a CTA rewrites `norm_rows` rows of one sequence, in
+// batches of qk_norm_rows_per_batch(Hq) rows (the next batch's loads in flight
+// while the current one is written). One batch a CTA where that makes about
+// kQkNormCtasPerSm x 2 CTAs an SM or fewer (the latency-bound short calls);
+// on longer calls as many batches a CTA (up to kQkNormMaxIters) as keep the
+// grid near that size, so the pair loads and merges of a CTA are paid once
+// for many rows (one batch a CTA took 93 us to rewrite the 79 MB of scores
+// of a 32-sequence batch: CTA launches and their per-CTA merges bound it).
+void norm_layout(QkPlan* p, int B, int Cmax, int Hq, int sms) {
+  const int base = qk_norm_rows_per_batch(Hq);
+  const long long blocks = static_cast<long long>(B) * ((Cmax + base - 1) / base);
+  const long long target = 2LL * kQkNormCtasPerSm * sms;
+  const long long iters = std::min<long long>(kQkNormMaxIters, std::max<long long>(1, (blocks + target - 1) / target));
+  p->norm_rows = base * static_cast<int>(iters);
+  p->norm_ctas_per_b = (Cmax + p->norm_rows - 1) / p->norm_rows;
+}
+
 int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int k_dtype, int mode, int engine,
          QkPlan* p) {
   int rc = check_args(B, Cmax, Hq, Hkv, D, k_dtype, mode);
@@ -124,12 +157,14 @@ int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int k_dtype, int mode
     return qfail(GQA_AV_ERR_INVALID,
                  "engine=%d must be 0 (auto), 1 (FMA), 2 (tensor, fixed splits) or 3 (streamed)",
                  engine);
-  // The streamed tensor-core kernel is the default on shapes with at least as
-  // many tiles (sequences x head groups) as SMs (measured faster there: the
-  // large batch 2.69 vs 2.90 ms); on fewer tiles the fixed-split kernel was
-  // measured faster (Llama-size 20.8 vs 22.6 us, Phi-style 35.5 vs 37.9 us,
-  // the 4x-L2 traffic shape 153 vs 169 us). It keeps the lengths in shared
-  // memory (at most kStreamMaxB sequences).
+  // The streamed tensor-core kernel is the default except on short streams
+  // with fewer tiles (sequences x head groups) than SMs, where the
+  // fixed-split kernel runs about two CTAs an SM in one wave (D <= 128 and at
+  // most 2048 x 2 x SMs tile rows). Measured on GB300, us per call, fixed vs
+  // streamed: Llama-size 12.8 vs 14.7 and Phi-style 26.1 vs 27.3 (short);
+  // MQA-style 40.6 vs 39.9 (D = 256), the 4x-L2 traffic shape 123 vs 98, its
+  // 32-sequence ragged twin 235 vs 157. The streamed kernel keeps the lengths
+  // in shared memory (at most kStreamMaxB sequences).
   if (engine == kQkEngineStream && B > kStreamMaxB)
     return qfail(GQA_AV_ERR_UNSUPPORTED, "the streamed kernel takes at most %d sequences",
                  kStreamMaxB);
@@ -139,9 +174,10 @@ int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int k_dtype, int mode
     int sms0 = 0;
     cudaError_t e0 = cudaDeviceGetAttribute(&sms0, cudaDevAttrMultiProcessorCount, dev);
     if (e0 != cudaSuccess) return qfail_cuda(e0, "cudaDeviceGetAttribute");
-    const bool many_tiles = static_cast<long long>(B) * (Hq / heads0) >= sms0;
+    const long long tiles0 = static_cast<long long>(B) * (Hq / heads0);
+    const bool short_few = tiles0 < sms0 && D <= 128 && tiles0 * Cmax <= 2048LL * 2 * sms0;
     p->engine = engine ? engine
-                       : (B <= kStreamMaxB && many_tiles ? kQkEngineStream : kQkEngineTensor);
+                       : (B <= kStreamMaxB && !short_few ? kQkEngineStream : kQkEngineTensor);
   }
   const bool auto_stream = engine == 0 && p->engine == kQkEngineStream;
   const int G = Hq / Hkv;
@@ -193,9 +229,8 @@ int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int k_dtype, int mode
     QkKernel kfn = k_dtype == GQA_AV_BF16 ? pick_stream<Bf16Tag>(p->npad / 16)
                                           : pick_stream<Fp16Tag>(p->npad / 16);
     if (!kfn) return qfail(GQA_AV_ERR_UNSUPPORTED, "no score kernel for this head count");
-    cudaError_t e2 = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-    if (e2 == cudaSuccess)  // all of the SM's unified memory as shared memory, so two CTAs fit
-      e2 = cudaFuncSetAttribute(kfn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    // All of the SM's unified memory as shared memory, so two CTAs fit.
+    cudaError_t e2 = cudaFuncSetAttribute(kfn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e2 != cudaSuccess) return qfail_cuda(e2, "cudaFuncSetAttribute");
     for (int per_sm = D <= 128 ? 2 : 1; per_sm >= 1; --per_sm) {
       const int budget =
@@ -210,9 +245,20 @@ int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int k_dtype, int mode
         p->smem = p->lens_off + (B + 1) * 4 + 1024;
         if (p->smem <= budget || p->stages == 2) break;
       }
+      // CTAs an SM: the occupancy query, or where it gives fewer, what the
+      // SM's shared memory, registers and threads hold. (For this kernel the
+      // query answered one CTA an SM at every shared-memory size, where two
+      // of 84 KB ran side by side and 20 % faster. The CTAs do not wait on
+      // one another, so a count that were too high would only make a second
+      // wave.)
       int occ = 0;
+      e2 = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                std::min(p->smem, optin));
+      if (e2 != cudaSuccess) return qfail_cuda(e2, "cudaFuncSetAttribute");
       e2 = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kfn, p->threads, p->smem);
       if (e2 != cudaSuccess) return qfail_cuda(e2, "occupancy query");
+      if (occ < per_sm)
+        occ = std::max(occ, resident_ctas(reinterpret_cast<const void*>(kfn), p->threads, p->smem, prop));
       if (occ >= per_sm || per_sm == 1) {
         p->split_units = p->hgroups * std::max(1, sms * per_sm / p->hgroups);
         break;
@@ -233,8 +279,7 @@ int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int k_dtype, int mode
     // Partial pairs: two slots a CTA; then one slot per tile held whole.
     p->whole_off = static_cast<size_t>(2) * p->split_units * p->heads * sizeof(float2);
     p->ws_bytes = p->whole_off + static_cast<size_t>(p->tiles) * p->heads * sizeof(float2);
-    p->norm_rows = std::max(1, kQkNormBatch * kQkNormThreads / Hq);
-    p->norm_ctas_per_b = (Cmax + p->norm_rows - 1) / p->norm_rows;
+    norm_layout(p, B, Cmax, Hq, sms);
     if (static_cast<long long>(B) * p->norm_ctas_per_b > 0x7fffffffLL)
       return qfail(GQA_AV_ERR_UNSUPPORTED, "normalise grid too large");
     return GQA_AV_OK;
@@ -290,8 +335,7 @@ fixed_splits:
 
   // Normalise: about kQkNormBatch scores a thread, so each thread has one
   // round of loads in flight.
-  p->norm_rows = std::max(1, kQkNormBatch * kQkNormThreads / Hq);
-  p->norm_ctas_per_b = (Cmax + p->norm_rows - 1) / p->norm_rows;
+  norm_layout(p, B, Cmax, Hq, sms);
   if (static_cast<long long>(B) * p->norm_ctas_per_b > 0x7fffffffLL)
     return qfail(GQA_AV_ERR_UNSUPPORTED, "normalise grid too large");
   return GQA_AV_OK;

@@ -27,6 +27,8 @@
 // launch shape.
 #pragma once
 
+#include <type_traits>
+
 #include "gqa_av_kernel.cuh"
 
 namespace gqa_av {
@@ -37,6 +39,20 @@ constexpr int kQkThreads = kQkConsumerThreads + 32;  // + the producer warp
 constexpr int kQkNormThreads = 256;
 constexpr int kQkNormBatch = 8;          // scores each normalise thread loads at once
 constexpr int kQkNormMaxPairs = 3072;     // (head, split) pairs staged in shared memory
+constexpr int kQkNormCtasPerSm = 5;       // normalise CTAs resident an SM (their static shared memory)
+constexpr int kQkNormMaxIters = 64;       // batches of scores a normalise CTA rewrites, at most
+// Floats a normalise load moves: 4 when Hq % 4 == 0 (every row then starts on
+// a 16-byte boundary), else 1; loads a thread has in flight per batch.
+__host__ __device__ constexpr int qk_norm_vec(int Hq) { return Hq % 4 == 0 ? 4 : 1; }
+__host__ __device__ constexpr int qk_norm_loads(int vec) { return vec == 4 ? 4 : 8; }
+// Rows a normalise CTA rewrites per batch. With Hq / vec <= kQkNormThreads
+// vectors a row, a thread keeps one column of vectors (fixed heads) over
+// kQkNormThreads / (Hq / vec) rows a pass; wider rows go element by element.
+__host__ __device__ constexpr int qk_norm_rows_per_batch(int Hq) {
+  return Hq / qk_norm_vec(Hq) <= kQkNormThreads
+             ? qk_norm_loads(qk_norm_vec(Hq)) * (kQkNormThreads / (Hq / qk_norm_vec(Hq)))
+             : (qk_norm_loads(qk_norm_vec(Hq)) * qk_norm_vec(Hq) * kQkNormThreads + Hq - 1) / Hq;
+}
 constexpr int kQkMaxHeads = 64;
 
 struct alignas(64) QkParams {
@@ -311,29 +327,54 @@ __global__ void __launch_bounds__(kQkThreads, 1) gqa_qk_kernel(const __grid_cons
 // sum) pairs, pair (h, i) at slot(h / heads, i)[h % heads] (the heads of one
 // slot contiguous). Three steps, with one round of global loads before the
 // first:
-//   1. the block's scores into registers (rows_per_cta * Hq is at most
-//      kQkNormBatch * kQkNormThreads: one batch of loads a thread), and every
+//   1. the first batch of the block's scores into registers (a batch is
+//      qk_norm_rows_per_batch(Hq) rows, a few loads a thread), and every
 //      pair into shared memory (a slot's heads are adjacent addresses), all
 //      loads in flight together;
 //   2. per head M = max_i m_i, then S = sum_i l_i exp(m_i - M), with `tph`
 //      threads a head (a power of two up to 32) taking segments part, part +
 //      tph, ... and fixed butterflies over them;
-//   3. attn = exp(s - M) / S over the block's rows.
+//   3. attn = exp(s - M) / S, batch after batch, the next batch's loads
+//      issued before the current one is written.
 // ---------------------------------------------------------------------------
-template <typename Slot>
+template <int VEC, typename Slot>
 __device__ __forceinline__ void qk_normalize_rows(float* attn_b, int Hq, int heads, int nseg,
-                                                  int c0, int c1, Slot slot) {
-  __shared__ float2 ms[kQkMaxHeads * 32];   // (M, 1 / S) per head, Hq <= 2048
-  __shared__ float2 pairs[kQkNormMaxPairs];
+                                                  int c0, int c1, Slot slot, float2* ms,
+                                                  float2* pairs) {
+  // VEC floats a load, kLoads loads a thread a batch. Rows of at most
+  // kQkNormThreads vectors: thread t takes vector column t % cols of rows
+  // t / cols, t / cols + rpp, ... (rpp rows a pass), so its heads, and their
+  // (M, 1 / S), are the same for every row it writes. Wider rows: element
+  // index base + (t + u kQkNormThreads) VEC of the block.
+  constexpr int kLoads = qk_norm_loads(VEC);
+  using Vec = typename std::conditional<VEC == 4, float4, float>::type;
   const int tid = threadIdx.x;
-  const int n = (c1 - c0) * Hq;
+  const int rows = c1 - c0;
+  const int n = rows * Hq;
   float* row0 = attn_b + (size_t)c0 * Hq;
-  float x[kQkNormBatch];
+  const int cols = Hq / VEC;
+  const bool by_col = cols <= kQkNormThreads;
+  const int rpp = by_col ? kQkNormThreads / cols : 0;
+  const int my_col = by_col ? tid % cols : 0;
+  const int my_row = by_col ? tid / cols : 0;
+  const bool active = by_col && my_row < rpp;
+  const int rpb = kLoads * rpp;              // rows a batch (by column)
+  constexpr int kChunk = kLoads * VEC * kQkNormThreads;  // elements a batch (wide rows)
+  auto load = [&](Vec (&x)[kLoads], int base) {  // base: first row, or first element
 #pragma unroll
-  for (int u = 0; u < kQkNormBatch; ++u) {
-    const int i = tid + u * kQkNormThreads;
-    x[u] = i < n ? __ldcg(row0 + i) : 0.0f;
-  }
+    for (int u = 0; u < kLoads; ++u) {
+      if (by_col) {
+        const int r = base + u * rpp + my_row;
+        if (active && r < rows)
+          x[u] = __ldcg(reinterpret_cast<const Vec*>(row0 + (size_t)r * Hq + my_col * VEC));
+      } else {
+        const int i = base + (tid + u * kQkNormThreads) * VEC;
+        if (i < n) x[u] = __ldcg(reinterpret_cast<const Vec*>(row0 + i));
+      }
+    }
+  };
+  Vec x[kLoads];
+  load(x, 0);
   const int per_k = nseg * heads;
   const int npairs = Hq * nseg;
   const bool staged = npairs <= kQkNormMaxPairs;
@@ -383,12 +424,53 @@ __device__ __forceinline__ void qk_normalize_rows(float* attn_b, int Hq, int hea
     if (valid && part == 0) ms[h] = make_float2(M, 1.0f / S);
   }
   __syncthreads();
+  // exp(s - M) / S. The fast exponential's relative error (a few 1e-7 plus
+  // |s - M| x 6e-8) stays far inside the step's 1e-4 relative tolerance.
+  auto prob = [](float s, float2 w) { return __expf(s - w.x) * w.y; };
+  auto put = [&](float* dst, const Vec& v, const float2* w) {
+    if constexpr (VEC == 4)
+      *reinterpret_cast<float4*>(dst) =
+          make_float4(prob(v.x, w[0]), prob(v.y, w[1]), prob(v.z, w[2]), prob(v.w, w[3]));
+    else
+      *dst = prob(v, w[0]);
+  };
+  if (by_col) {
+    float2 w[VEC];
 #pragma unroll
-  for (int u = 0; u < kQkNormBatch; ++u) {
-    const int i = tid + u * kQkNormThreads;
-    if (i < n) {
-      const float2 v = ms[i % Hq];
-      row0[i] = expf(x[u] - v.x) * v.y;
+    for (int e = 0; e < VEC; ++e) w[e] = active ? ms[my_col * VEC + e] : make_float2(0.f, 0.f);
+    for (int r0 = 0; r0 < rows; r0 += rpb) {
+      Vec y[kLoads];
+      const bool more = r0 + rpb < rows;
+      if (more) load(y, r0 + rpb);
+#pragma unroll
+      for (int u = 0; u < kLoads; ++u) {
+        const int r = r0 + u * rpp + my_row;
+        if (active && r < rows) put(row0 + (size_t)r * Hq + my_col * VEC, x[u], w);
+      }
+      if (more) {
+#pragma unroll
+        for (int u = 0; u < kLoads; ++u) x[u] = y[u];
+      }
+    }
+  } else {
+    for (int base = 0; base < n; base += kChunk) {
+      Vec y[kLoads];
+      const bool more = base + kChunk < n;
+      if (more) load(y, base + kChunk);
+#pragma unroll
+      for (int u = 0; u < kLoads; ++u) {
+        const int i = base + (tid + u * kQkNormThreads) * VEC;
+        if (i < n) {
+          float2 w[VEC];
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) w[e] = ms[(i + e) % Hq];
+          put(row0 + i, x[u], w);
+        }
+      }
+      if (more) {
+#pragma unroll
+        for (int u = 0; u < kLoads; ++u) x[u] = y[u];
+      }
     }
   }
 }
@@ -407,10 +489,16 @@ gqa_qk_normalize_kernel(const __grid_constant__ QkNormParams p) {
   const int c0 = blk * p.rows_per_cta;
   const int c1 = min(c0 + p.rows_per_cta, L);
   if (c0 >= c1) return;
-  qk_normalize_rows(p.attn + (size_t)b * p.Cmax * p.Hq, p.Hq, p.heads, nsplit_b, c0, c1,
-                    [&](int hg, int s) {
-                      return p.stats + ((size_t)(hg * p.B + b) * p.nsplit + s) * p.heads;
-                    });
+  __shared__ float2 ms[kQkMaxHeads * 32];  // (M, 1 / S) per head, Hq <= 2048
+  __shared__ float2 pairs[kQkNormMaxPairs];
+  auto slot = [&](int hg, int s) {
+    return p.stats + ((size_t)(hg * p.B + b) * p.nsplit + s) * p.heads;
+  };
+  float* attn_b = p.attn + (size_t)b * p.Cmax * p.Hq;
+  if (qk_norm_vec(p.Hq) == 4)
+    qk_normalize_rows<4>(attn_b, p.Hq, p.heads, nsplit_b, c0, c1, slot, ms, pairs);
+  else
+    qk_normalize_rows<1>(attn_b, p.Hq, p.heads, nsplit_b, c0, c1, slot, ms, pairs);
 }
 
 }  // namespace gqa_av

@@ -410,11 +410,17 @@ __global__ void __launch_bounds__(kQkNormThreads)
   // whole, else slot 2 (g K + k) of group g = g0 + i (2 (g0 K + k) + 1 for
   // the first when the tile does not start g0's range).
   const int nseg = g0 == g1 ? 1 : g1 - g0 + 1;
-  qk_normalize_rows(p.attn + (size_t)b * p.Cmax * p.Hq, p.Hq, p.heads, nseg, c0, c1,
-                    [&](int k, int i) {
-                      if (g0 == g1) return p.stats_whole + ((size_t)b * K + k) * p.heads;
-                      return p.stats + (size_t)(2 * ((g0 + i) * K + k) + (i == 0 ? adj : 0)) * p.heads;
-                    });
+  __shared__ float2 ms[kQkMaxHeads * 32];  // (M, 1 / S) per head, Hq <= 2048
+  __shared__ float2 pairs[kQkNormMaxPairs];
+  auto slot = [&](int k, int i) {
+    if (g0 == g1) return p.stats_whole + ((size_t)b * K + k) * p.heads;
+    return p.stats + (size_t)(2 * ((g0 + i) * K + k) + (i == 0 ? adj : 0)) * p.heads;
+  };
+  float* attn_b = p.attn + (size_t)b * p.Cmax * p.Hq;
+  if (qk_norm_vec(p.Hq) == 4)
+    qk_normalize_rows<4>(attn_b, p.Hq, p.heads, nseg, c0, c1, slot, ms, pairs);
+  else
+    qk_normalize_rows<1>(attn_b, p.Hq, p.heads, nseg, c0, c1, slot, ms, pairs);
 }
 
 }  // namespace gqa_av

@@ -64,9 +64,10 @@ int gqa_qk_softmax_decode(const float *q, const void *k_cache, const int32_t *se
                           float scale, int mode, void *stream);
 
 /* The same with the kernel chosen: engine 0 lets the library pick (the
- * streamed tensor-core kernel on shapes with at least as many tiles --
- * sequences x head groups -- as SMs and at most 2048 sequences, else the
- * fixed-split one), 1 forces the CUDA-core FMA kernel, 2 the tcgen05 tensor-core kernel
+ * streamed tensor-core kernel for at most 2048 sequences, except on short
+ * streams -- fewer tiles (sequences x head groups) than SMs, D <= 128 and at
+ * most 2 x 2048 x SMs rows over all tiles -- and on larger batches, where it
+ * takes the fixed-split one), 1 forces the CUDA-core FMA kernel, 2 the tcgen05 tensor-core kernel
  * with fixed context splits (K rows as the A operand in place, the queries
  * split into 16-bit hi and lo halves as B), 3 the streamed tcgen05 kernel
  * (the same products; persistent CTAs, two an SM where they fit, each taking

@@ -189,3 +189,24 @@ def test_score_step_streamed_over_the_batch(gq, B, kind):
         a = run_qk(gq, q, k, sl, mode, engine=3)
         check(a, ref, lens, f"B={B} {kind} mode={mode}")
         assert np.array_equal(run_qk(gq, q, k, sl, mode, engine=3), a), "not reproducible"
+
+
+# Calls long enough that each normalise CTA rewrites its rows in several
+# batches (the grid is capped near ten CTAs an SM on these), with 16-byte
+# loads (Hq % 4 == 0) and with 4-byte loads (Hq = 6), ragged lengths with
+# empty and full sequences, on both score kernels and their normalise steps.
+@pytest.mark.parametrize("engine", [2, 3], ids=["tensor", "stream"])
+@pytest.mark.parametrize("B,C,Hq,Hkv", [(64, 16384, 8, 1), (48, 16384, 6, 1)], ids=["vec4", "scalar"])
+def test_score_step_normalise_in_batches(gq, B, C, Hq, Hkv, engine):
+    D = 64
+    rng = np.random.default_rng(B + Hq)
+    lens = rng.integers(0, C + 1, size=B)
+    lens[0], lens[1], lens[2] = 0, C, 1
+    q = torch.from_numpy(rng.standard_normal((B, Hq, D), dtype=np.float32))
+    k = torch.from_numpy(rng.standard_normal((B, C, Hkv, D), dtype=np.float32)).to(torch.bfloat16)
+    for b in range(B):
+        k[b, int(lens[b]):] = float("nan")
+    sl = torch.tensor(lens, dtype=torch.int32)
+    ref = gqa_qk.gqa_qk_softmax(q.numpy(), bits(k), "bf16", sl.numpy(), D ** -0.5)
+    got = run_qk(gq, q, k, sl, engine=engine)
+    check(got, ref, lens, f"B={B} Hq={Hq} engine={engine}")
