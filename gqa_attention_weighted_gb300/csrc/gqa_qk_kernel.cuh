@@ -398,8 +398,8 @@ __device__ __forceinline__ void qk_normalize_rows(float* attn_b, int Hq, int hea
     }
   }
   __syncthreads();
-  auto pair = [&](int h, int seg) {
-    const int k = h / heads, hh = h - k * heads;
+  // Pair (h, seg) with k = h / heads and hh = h % heads worked out once a head.
+  auto pair = [&](int k, int hh, int seg) {
     return staged ? pairs[(k * nseg + seg) * heads + hh] : __ldcg(slot(k, seg) + hh);
   };
   int tph = 1;
@@ -410,18 +410,19 @@ __device__ __forceinline__ void qk_normalize_rows(float* attn_b, int Hq, int hea
   for (int hb = 0; hb < Hq; hb += kQkNormThreads / tph) {
     const int h = hb + tid / tph;
     const bool valid = h < Hq;
+    const int k = h / heads, hh = h - k * heads;
     float M = -INFINITY;
     if (valid)
-      for (int i = part; i < nseg; i += tph) M = fmaxf(M, pair(h, i).x);
+      for (int i = part; i < nseg; i += tph) M = fmaxf(M, pair(k, hh, i).x);
     for (int o = tph >> 1; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float S = 0.0f;
     if (valid)
       for (int i = part; i < nseg; i += tph) {
-        const float2 v = pair(h, i);
+        const float2 v = pair(k, hh, i);
         if (v.x != -INFINITY) S += v.y * __expf(v.x - M);
       }
     for (int o = tph >> 1; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
-    if (valid && part == 0) ms[h] = make_float2(M, 1.0f / S);
+    if (valid && part == 0) ms[h] = make_float2(M, __frcp_rn(S));
   }
   __syncthreads();
   // exp(s - M) / S. The fast exponential's relative error (a few 1e-7 plus

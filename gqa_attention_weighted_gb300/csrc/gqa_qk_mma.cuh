@@ -60,6 +60,84 @@ __device__ __forceinline__ void split_query(Fp16Tag, float a, float b, uint32_t&
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
+// The queries of `heads` consecutive heads (row n at q_rows + n * 8 * nkc)
+// -> the B operand's hi and lo rows, element (n, k) at ((n / 8) * nkc + k / 8)
+// * 128 + (n % 8) * 16 + (k % 8) * 2; rows n >= heads are zero. A thread takes
+// items t = first, first + stride, ... (item t: row t % N, 8 columns from
+// 8 (t / N)) and issues the loads of BATCH items before converting any, so
+// the operand costs about one round of global loads per batch (one item a
+// round made the first MMA of an MQA-shaped call wait 4 us for its queries).
+template <typename Tag, int N, int BATCH>
+__device__ __forceinline__ void convert_queries(const float* q_rows, int heads, int nkc,
+                                                uint8_t* bst, uint32_t b_half, int first,
+                                                int stride) {
+  const int items = N * nkc;
+  for (int t0 = first; t0 < items; t0 += BATCH * stride) {
+    float4 x[BATCH][2];
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const int t = t0 + u * stride;
+      const int n = t % N, kc = t / N;
+      if (t < items && n < heads) {
+        const float4* src = reinterpret_cast<const float4*>(q_rows + (size_t)n * nkc * 8 + kc * 8);
+        x[u][0] = src[0];
+        x[u][1] = src[1];
+      } else {
+        x[u][0] = x[u][1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const int t = t0 + u * stride;
+      if (t < items) {
+        const int n = t % N, kc = t / N;
+        uint32_t hi[4], lo[4];
+        split_query(Tag{}, x[u][0].x, x[u][0].y, hi[0], lo[0]);
+        split_query(Tag{}, x[u][0].z, x[u][0].w, hi[1], lo[1]);
+        split_query(Tag{}, x[u][1].x, x[u][1].y, hi[2], lo[2]);
+        split_query(Tag{}, x[u][1].z, x[u][1].w, hi[3], lo[3]);
+        const size_t off = (size_t)((n >> 3) * nkc + kc) * 128 + (n & 7) * 16;
+        *reinterpret_cast<uint4*>(bst + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(bst + b_half + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+    }
+  }
+}
+
+// The (max, sum of exp(x - max)) over a warp's lanes of each of the first
+// `heads` of N running pairs, four heads at a time so that their shuffles
+// overlap; lane 0 writes head n's pair to red[n]. Deterministic (fixed
+// butterflies): the maximum first, then each lane's sum rescaled to it.
+template <int N>
+__device__ __forceinline__ void warp_lse_heads(const float (&mx)[N], const float (&sm)[N],
+                                               int heads, float2* red) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int n0 = 0; n0 < N; n0 += 4) {
+    if (n0 < heads) {
+      float M[4], S[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) M[i] = mx[n0 + i];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) M[i] = fmaxf(M[i], __shfl_xor_sync(0xffffffffu, M[i], o));
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        S[i] = mx[n0 + i] == -INFINITY ? 0.0f : sm[n0 + i] * __expf(mx[n0 + i] - M[i]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) S[i] += __shfl_xor_sync(0xffffffffu, S[i], o);
+      if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (n0 + i < heads) red[n0 + i] = make_float2(M[i], S[i]);
+      }
+    }
+  }
+}
+
 // Shared memory (offsets from a 1024-byte-aligned base):
 //   [K ring: stages x D/64 parts x 128 rows x 128 B]   (stage_bytes each)
 //   [B: 2 Npad rows x D columns, 16-bit, core-matrix layout]   at b_off
@@ -232,28 +310,8 @@ __global__ void __launch_bounds__(kQkMmaThreads, 1)
   // The group's queries -> B hi / lo (element (n, k) at ((n / 8) * nkc + k / 8)
   // * 128 + (n % 8) * 16 + (k % 8) * 2; heads past the group are zero).
   {
-    uint8_t* bst = smem + p.b_off;
-    const int items = N * nkc;
-    for (int t = tid; t < items; t += 32 * kMmaAccWarps) {
-      const int n = t % N, kc = t / N;
-      float w[8];
-      if (n < p.heads) {
-        const float4* src =
-            reinterpret_cast<const float4*>(p.q + ((size_t)b * p.Hq + h0 + n) * p.D + kc * 8);
-        const float4 x = src[0], y = src[1];
-        w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
-        w[4] = y.x; w[5] = y.y; w[6] = y.z; w[7] = y.w;
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) w[e] = 0.0f;
-      }
-      uint32_t hi[4], lo[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) split_query(Tag{}, w[2 * q], w[2 * q + 1], hi[q], lo[q]);
-      const size_t off = (size_t)((n >> 3) * nkc + kc) * 128 + (n & 7) * 16;
-      *reinterpret_cast<uint4*>(bst + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(bst + b_half + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    }
+    convert_queries<Tag, N, 4>(p.q + ((size_t)b * p.Hq + h0) * p.D, p.heads, nkc, smem + p.b_off,
+                               b_half, tid, 32 * kMmaAccWarps);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     if (lane == 0) mbar_arrive(qready);
@@ -308,13 +366,7 @@ __global__ void __launch_bounds__(kQkMmaThreads, 1)
 
   // One (max, sum) per head of the group (not the padding up to N) for the
   // split: over each warp's lanes, then over the four warps in warp order.
-#pragma unroll
-  for (int n = 0; n < N; ++n) {
-    if (n < p.heads) {
-      const float2 r = warp_lse(mx[n], sm[n]);
-      if (lane == 0) red[(size_t)warp * N + n] = r;
-    }
-  }
+  warp_lse_heads<N>(mx, sm, p.heads, red + (size_t)warp * N);
   named_sync(1, 32 * kMmaAccWarps);
   if (tid < p.heads && ok && n_iters > 0)
     p.stats[((size_t)tile * p.nsplit + split) * p.heads + tid] = lse_of(red + tid, kMmaAccWarps, N);

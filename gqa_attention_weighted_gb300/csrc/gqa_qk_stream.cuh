@@ -189,28 +189,8 @@ __global__ void __launch_bounds__(kQkStreamThreads, 1)
           if (lane == 0) atomicOr(p.status, kErrMmaWait);
           break;
         }
-        uint8_t* bst = smem + p.b_off + (size_t)buf * 2 * b_half;
-        const int items = N * nkc;
-        for (int t = lane; t < items; t += 32) {
-          const int n = t % N, kc = t / N;
-          float w[8];
-          if (n < p.heads) {
-            const float4* src = reinterpret_cast<const float4*>(
-                p.q + ((size_t)cur.b * p.Hq + h0 + n) * p.D + kc * 8);
-            const float4 x = src[0], y = src[1];
-            w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
-            w[4] = y.x; w[5] = y.y; w[6] = y.z; w[7] = y.w;
-          } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) w[i] = 0.0f;
-          }
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) split_query(Tag{}, w[2 * q], w[2 * q + 1], hi[q], lo[q]);
-          const size_t off = (size_t)((n >> 3) * nkc + kc) * 128 + (n & 7) * 16;
-          *reinterpret_cast<uint4*>(bst + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(bst + b_half + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
+        convert_queries<Tag, N, 8>(p.q + ((size_t)cur.b * p.Hq + h0) * p.D, p.heads, nkc,
+                                   smem + p.b_off + (size_t)buf * 2 * b_half, b_half, lane, 32);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) mbar_arrive(qready0 + 8 * buf);
@@ -345,12 +325,9 @@ __global__ void __launch_bounds__(kQkStreamThreads, 1)
       // End of a segment: one (max, sum) per head, over each warp's lanes and
       // then over the four warps in warp order, to the tile's slot (whole) or
       // the CTA's (cut).
+      warp_lse_heads<N>(mx, sm, p.heads, red + (size_t)warp * N);  // the group's heads only
 #pragma unroll
       for (int n = 0; n < N; ++n) {
-        if (n < p.heads) {  // the group's heads only (N pads them to 16)
-          const float2 r = warp_lse(mx[n], sm[n]);
-          if (lane == 0) red[(size_t)warp * N + n] = r;
-        }
         mx[n] = -INFINITY;
         sm[n] = 0.0f;
       }
