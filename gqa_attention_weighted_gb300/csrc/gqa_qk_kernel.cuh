@@ -41,6 +41,7 @@ constexpr int kQkNormBatch = 8;          // scores each normalise thread loads a
 constexpr int kQkNormMaxPairs = 3072;     // (head, split) pairs staged in shared memory
 constexpr int kQkNormCtasPerSm = 5;       // normalise CTAs resident an SM (their static shared memory)
 constexpr int kQkNormMaxIters = 64;       // batches of scores a normalise CTA rewrites, at most
+constexpr int kQkNormFastSeg = 32;        // pairs a head a thread merges on its own, at most
 // Floats a normalise load moves: 4 when Hq % 4 == 0 (every row then starts on
 // a 16-byte boundary), else 1; loads a thread has in flight per batch.
 __host__ __device__ constexpr int qk_norm_vec(int Hq) { return Hq % 4 == 0 ? 4 : 1; }
@@ -325,15 +326,18 @@ __global__ void __launch_bounds__(kQkThreads, 1) gqa_qk_kernel(const __grid_cons
 // The normalise step of one CTA (sequence b, rows [c0, c1)), shared by the
 // fixed-split and streamed score kernels: every head of b has `nseg` (max,
 // sum) pairs, pair (h, i) at slot(h / heads, i)[h % heads] (the heads of one
-// slot contiguous). Three steps, with one round of global loads before the
-// first:
-//   1. the first batch of the block's scores into registers (a batch is
-//      qk_norm_rows_per_batch(Hq) rows, a few loads a thread), and every
+// slot contiguous). The routine waits for the score kernel (programmatic
+// dependent launch) after working out what needs no results of it, then:
+//   1. loads the first batch of the block's scores into registers (a batch
+//      is qk_norm_rows_per_batch(Hq) rows, a few loads a thread) and every
 //      pair into shared memory (a slot's heads are adjacent addresses), all
-//      loads in flight together;
-//   2. per head M = max_i m_i, then S = sum_i l_i exp(m_i - M), with `tph`
-//      threads a head (a power of two up to 32) taking segments part, part +
-//      tph, ... and fixed butterflies over them;
+//      in flight together;
+//   2. per head M = max_i m_i, then S = sum_i l_i exp(m_i - M): with at most
+//      kQkNormFastSeg segments by the head's own thread in segment order,
+//      else with `tph` threads a head (a power of two up to 32) taking
+//      segments part, part + tph, ... and fixed butterflies over them (each
+//      dependent step of a merge costs about 0.2 us, so few segments go
+//      without the butterflies);
 //   3. attn = exp(s - M) / S, batch after batch, the next batch's loads
 //      issued before the current one is written.
 // ---------------------------------------------------------------------------
@@ -373,12 +377,38 @@ __device__ __forceinline__ void qk_normalize_rows(float* attn_b, int Hq, int hea
       }
     }
   };
-  Vec x[kLoads];
-  load(x, 0);
+  // Pair i of the staging order (i = (k * nseg + seg) * heads + hh) comes
+  // from slot(k, seg)[hh]. When all pairs fit one batch of loads (the usual
+  // case), each thread works out the addresses of its pairs before the
+  // dependency wait, so the loads issue as soon as it returns.
   const int per_k = nseg * heads;
   const int npairs = Hq * nseg;
   const bool staged = npairs <= kQkNormMaxPairs;
-  if (staged) {
+  const bool one_batch = npairs <= kQkNormBatch * kQkNormThreads;
+  const float2* src[kQkNormBatch];
+#pragma unroll
+  for (int u = 0; u < kQkNormBatch; ++u) {
+    const int i = tid + u * kQkNormThreads;
+    src[u] = nullptr;
+    if (one_batch && i < npairs) {
+      const int k = i / per_k, r = i - k * per_k;
+      const int seg = r / heads;
+      src[u] = slot(k, seg) + (r - seg * heads);
+    }
+  }
+  grid_dependency_wait();  // scores and pairs of the score kernel are visible
+  grid_launch_dependents();
+  Vec x[kLoads];
+  load(x, 0);
+  if (one_batch) {
+    float2 v[kQkNormBatch];
+#pragma unroll
+    for (int u = 0; u < kQkNormBatch; ++u)
+      if (src[u]) v[u] = __ldcg(src[u]);
+#pragma unroll
+    for (int u = 0; u < kQkNormBatch; ++u)
+      if (src[u]) pairs[tid + u * kQkNormThreads] = v[u];
+  } else if (staged) {
     for (int i0 = tid; i0 < npairs; i0 += kQkNormBatch * kQkNormThreads) {
       float2 v[kQkNormBatch];
 #pragma unroll
@@ -402,27 +432,45 @@ __device__ __forceinline__ void qk_normalize_rows(float* attn_b, int Hq, int hea
   auto pair = [&](int k, int hh, int seg) {
     return staged ? pairs[(k * nseg + seg) * heads + hh] : __ldcg(slot(k, seg) + hh);
   };
-  int tph = 1;
-  while (tph < 32 && 2 * tph * Hq <= kQkNormThreads) tph *= 2;
-  const int part = tid & (tph - 1);
-  // The loop's trip count is the same for every thread, so whole warps take
-  // the shuffles; threads past Hq carry (-inf, 0).
-  for (int hb = 0; hb < Hq; hb += kQkNormThreads / tph) {
-    const int h = hb + tid / tph;
-    const bool valid = h < Hq;
-    const int k = h / heads, hh = h - k * heads;
-    float M = -INFINITY;
-    if (valid)
-      for (int i = part; i < nseg; i += tph) M = fmaxf(M, pair(k, hh, i).x);
-    for (int o = tph >> 1; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float S = 0.0f;
-    if (valid)
-      for (int i = part; i < nseg; i += tph) {
-        const float2 v = pair(k, hh, i);
-        if (v.x != -INFINITY) S += v.y * __expf(v.x - M);
+  if (staged && nseg <= kQkNormFastSeg && Hq <= kQkNormThreads) {
+    // Few segments (the usual case): thread h < Hq merges head h's pairs from
+    // shared memory in segment order; no shuffles.
+    if (tid < Hq) {
+      const int k = tid / heads, hh = tid - k * heads;
+      const float2* v = pairs + (size_t)k * per_k + hh;
+      float M = -INFINITY, S = 0.0f;
+#pragma unroll 8
+      for (int i = 0; i < nseg; ++i) M = fmaxf(M, v[i * heads].x);
+#pragma unroll 8
+      for (int i = 0; i < nseg; ++i) {
+        const float2 w = v[i * heads];
+        if (w.x != -INFINITY) S += w.y * __expf(w.x - M);
       }
-    for (int o = tph >> 1; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
-    if (valid && part == 0) ms[h] = make_float2(M, __frcp_rn(S));
+      ms[tid] = make_float2(M, __frcp_rn(S));
+    }
+  } else {
+    int tph = 1;
+    while (tph < 32 && 2 * tph * Hq <= kQkNormThreads) tph *= 2;
+    const int part = tid & (tph - 1);
+    // The loop's trip count is the same for every thread, so whole warps take
+    // the shuffles; threads past Hq carry (-inf, 0).
+    for (int hb = 0; hb < Hq; hb += kQkNormThreads / tph) {
+      const int h = hb + tid / tph;
+      const bool valid = h < Hq;
+      const int k = h / heads, hh = h - k * heads;
+      float M = -INFINITY;
+      if (valid)
+        for (int i = part; i < nseg; i += tph) M = fmaxf(M, pair(k, hh, i).x);
+      for (int o = tph >> 1; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      float S = 0.0f;
+      if (valid)
+        for (int i = part; i < nseg; i += tph) {
+          const float2 v = pair(k, hh, i);
+          if (v.x != -INFINITY) S += v.y * __expf(v.x - M);
+        }
+      for (int o = tph >> 1; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+      if (valid && part == 0) ms[h] = make_float2(M, __frcp_rn(S));
+    }
   }
   __syncthreads();
   // exp(s - M) / S. The fast exponential's relative error (a few 1e-7 plus
@@ -485,8 +533,7 @@ gqa_qk_normalize_kernel(const __grid_constant__ QkNormParams p) {
   const int blk = blockIdx.x - b * p.ctas_per_b;
   const int L = clamped_len(p.seq_lens, b, p.Cmax);
   const int nsplit_b = L > 0 ? (L + p.rows_per_split - 1) / p.rows_per_split : 1;
-  grid_dependency_wait();   // scores and per-split pairs of the score kernel are visible
-  grid_launch_dependents();
+  // A block past the length has nothing to do (and nothing to wait for).
   const int c0 = blk * p.rows_per_cta;
   const int c1 = min(c0 + p.rows_per_cta, L);
   if (c0 >= c1) return;

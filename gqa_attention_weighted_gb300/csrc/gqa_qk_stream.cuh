@@ -378,8 +378,7 @@ __global__ void __launch_bounds__(kQkNormThreads)
   const int Ug = static_cast<int>(T < Ug0 ? T : Ug0);
   const int g0 = stream_owner(T, P, Ug), g1 = stream_owner(T, P + nb - 1, Ug);
   const int adj = stream_first(T, g0, Ug) == P ? 0 : 1;
-  grid_dependency_wait();  // scores and pairs of the score kernel are visible
-  grid_launch_dependents();
+  // A block past the length has nothing to do (and nothing to wait for).
   const int c0 = blk * p.rows_per_cta;
   const int c1 = min(c0 + p.rows_per_cta, L);
   if (c0 >= c1) return;

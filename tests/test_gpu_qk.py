@@ -210,3 +210,20 @@ def test_score_step_normalise_in_batches(gq, B, C, Hq, Hkv, engine):
     ref = gqa_qk.gqa_qk_softmax(q.numpy(), bits(k), "bf16", sl.numpy(), D ** -0.5)
     got = run_qk(gq, q, k, sl, engine=engine)
     check(got, ref, lens, f"B={B} Hq={Hq} engine={engine}")
+
+
+# One sequence over many splits or groups: more than 32 (max, sum) pairs a
+# head, so the normalise step merges them with the shared-memory path
+# (Hq = 8: 1024 pairs staged) or reads them from global memory (Hq = 32:
+# 4096 pairs, past the staging buffer), on both score kernels.
+@pytest.mark.parametrize("engine", [2, 3], ids=["tensor", "stream"])
+@pytest.mark.parametrize("Hq", [8, 32])
+@pytest.mark.parametrize("L", [16384, 9001])
+def test_score_step_many_segments(gq, Hq, L, engine):
+    C, Hkv, D = 16384, 1, 64
+    rng = np.random.default_rng(Hq + L)
+    q, k, sl = qk_case(rng, 1, C, Hq, Hkv, D, "bf16", [L])
+    ref = gqa_qk.gqa_qk_softmax(q.numpy(), bits(k), "bf16", sl.numpy(), D ** -0.5)
+    got = run_qk(gq, q, k, sl, engine=engine)
+    check(got, ref, [L], f"Hq={Hq} L={L} engine={engine}")
+    assert np.array_equal(run_qk(gq, q, k, sl, engine=engine), got), "not reproducible"
