@@ -307,18 +307,12 @@ __global__ void __launch_bounds__(kQkStreamThreads, 1)
           if (n < p.heads)
             __stcg(reinterpret_cast<float4*>(dst + n), make_float4(s[n], s[n + 1], s[n + 2], s[n + 3]));
       }
+      if (!vec4) {
 #pragma unroll
-      for (int n = 0; n < N; ++n) {
-        if (n < p.heads) {
-          if (!vec4) dst[n] = s[n];
-          if (s[n] > mx[n]) {
-            sm[n] = (mx[n] == -INFINITY ? 0.0f : sm[n] * __expf(mx[n] - s[n])) + 1.0f;
-            mx[n] = s[n];
-          } else {
-            sm[n] += __expf(s[n] - mx[n]);
-          }
-        }
+        for (int n = 0; n < N; ++n)
+          if (n < p.heads) dst[n] = s[n];
       }
+      online_lse_update<N>(mx, sm, s, p.heads);
     }
     const bool tile_end = cur.j == cur.n - 1;
     if (tile_end || it == n_iters - 1) {
