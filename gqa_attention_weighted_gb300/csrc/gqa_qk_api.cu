@@ -133,17 +133,21 @@ int resident_ctas(const void* fn, int threads, int smem, const cudaDeviceProp& p
 }
 
 // Normalise launch: a CTA rewrites `norm_rows` rows of one sequence, in
-// batches of qk_norm_rows_per_batch(Hq) rows (the next batch's loads in flight
-// while the current one is written). One batch a CTA where that makes about
-// kQkNormCtasPerSm x 2 CTAs an SM or fewer (the latency-bound short calls);
-// on longer calls as many batches a CTA (up to kQkNormMaxIters) as keep the
-// grid near that size, so the pair loads and merges of a CTA are paid once
-// for many rows (one batch a CTA took 93 us to rewrite the 79 MB of scores
-// of a 32-sequence batch: CTA launches and their per-CTA merges bound it).
+// batches of qk_norm_rows_per_batch(Hq) rows (the next batch's loads in
+// flight while the current one is written). One batch a CTA where that
+// makes one wave (kQkNormCtasPerSm an SM) or less: the latency-bound short
+// calls; on longer calls as many batches a CTA (up to kQkNormMaxIters) as
+// keep the grid near one wave, so the pair loads and merges of a CTA are paid
+// once for many rows. Measured on GB300 (us per call of the score step, grid
+// of about 10 / 4 / 2 / 1 CTAs an SM): MQA-style 30.7 / 29.8 / 31.9 / 35.8,
+// the 32-sequence ragged batch 142.9 / 140.6 / 156.6 / 188.9; with one batch
+// a CTA the ragged batch's 79 MB of scores took 93 us to rewrite. At most 8
+// batches a CTA (against 64 / 32 / 16): the large ragged batch 1276 us (1334
+// / 1296 / 1281), whose long blocks past a sequence's length left CTAs idle.
 void norm_layout(QkPlan* p, int B, int Cmax, int Hq, int sms) {
   const int base = qk_norm_rows_per_batch(Hq);
   const long long blocks = static_cast<long long>(B) * ((Cmax + base - 1) / base);
-  const long long target = 2LL * kQkNormCtasPerSm * sms;
+  const long long target = 1LL * kQkNormCtasPerSm * sms;
   const long long iters = std::min<long long>(kQkNormMaxIters, std::max<long long>(1, (blocks + target - 1) / target));
   p->norm_rows = base * static_cast<int>(iters);
   p->norm_ctas_per_b = (Cmax + p->norm_rows - 1) / p->norm_rows;

@@ -39,8 +39,8 @@ constexpr int kQkThreads = kQkConsumerThreads + 32;  // + the producer warp
 constexpr int kQkNormThreads = 256;
 constexpr int kQkNormBatch = 8;          // scores each normalise thread loads at once
 constexpr int kQkNormMaxPairs = 3072;     // (head, split) pairs staged in shared memory
-constexpr int kQkNormCtasPerSm = 5;       // normalise CTAs resident an SM (their static shared memory)
-constexpr int kQkNormMaxIters = 64;       // batches of scores a normalise CTA rewrites, at most
+constexpr int kQkNormCtasPerSm = 4;       // normalise CTAs resident an SM (their registers)
+constexpr int kQkNormMaxIters = 8;        // batches of scores a normalise CTA rewrites, at most
 constexpr int kQkNormFastSeg = 32;        // pairs a head a thread merges on its own, at most
 // Floats a normalise load moves: 4 when Hq % 4 == 0 (every row then starts on
 // a 16-byte boundary), else 1; loads a thread has in flight per batch.
