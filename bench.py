@@ -942,9 +942,12 @@ def oracle_baseline_qk(w, x, scale, seconds):
 
 def run_e2e(gq, w, x, call, dev, args, world):
     """Same call with host inputs, through the public API: every step copies
-    the inputs from pinned host memory (split over `args.e2e_streams` copy
-    streams, whose copy engines run side by side), makes the call once they
-    have landed, and copies out back to pinned host memory."""
+    from pinned host memory what the call reads -- rows c < L_b of attn and V
+    (contiguous for each sequence; rows past a length are never read, as for
+    a serving engine's cache) and the lengths -- split over `args.e2e_streams`
+    copy streams, makes the call once they have landed, and copies out back to
+    pinned host memory. The result is checked bitwise against the same call on
+    the device-resident inputs."""
     host = {}
     for k, t in x.items():
         h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
@@ -955,16 +958,23 @@ def run_e2e(gq, w, x, call, dev, args, world):
     out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
     copiers = [torch.cuda.Stream(device=dev) for _ in range(max(1, args.e2e_streams))]
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_host.numel() * 4
     steps = max(1, min(args.e2e_steps, args.steps))
-    # Chunks of at most 1 GiB, dealt to the copy streams in turn.
+    lens = [max(0, min(int(v), w.Cmax)) for v in x["seq_lens"].cpu().tolist()]
+    # Copies of at most 1 GiB, dealt to the copy streams in turn: the rows
+    # each sequence reads of the [B, Cmax, ...] tensors, the rest whole.
     chunks = []
     for k, h in host.items():
-        hf, df = h.view(-1), dbuf[k].view(-1)
-        per = max(1, (1 << 30) // h.element_size())
-        for i in range(0, hf.numel(), per):
-            chunks.append((df[i:i + per], hf[i:i + per]))
+        if h.dim() >= 2 and h.shape[0] == w.B and h.shape[1] == w.Cmax and not args.paged:
+            pieces = [(dbuf[k][b, :L].reshape(-1), h[b, :L].reshape(-1))
+                      for b, L in enumerate(lens) if L > 0]
+        else:
+            pieces = [(dbuf[k].view(-1), h.view(-1))]
+        for df, hf in pieces:
+            per = max(1, (1 << 30) // hf.element_size())
+            for i in range(0, hf.numel(), per):
+                chunks.append((df[i:i + per], hf[i:i + per]))
+    h2d = sum(src.numel() * src.element_size() for _, src in chunks)
 
     def step():
         ready = torch.cuda.Event()
@@ -994,11 +1004,18 @@ def run_e2e(gq, w, x, call, dev, args, world):
     end.synchronize()
     barrier(world)
     ms = max_over_ranks(start.elapsed_time(end), world) / steps
+    ref = torch.empty_like(out)
+    with torch.cuda.stream(stream):
+        call(x, ref)
+    stream.synchronize()
+    if not torch.equal(out_host, ref.cpu()):
+        raise RuntimeError("e2e: the call on the copied inputs differs from the device-resident call")
     cbytes = W.compulsory_bytes(w, x["seq_lens"].cpu().tolist())
     return {"value": round(cbytes * world / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
             "ms_per_step": ms, "steps": steps, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "copy_streams": len(copiers),
-            "h2d_GBps": round(h2d / (ms * 1e-3) / 1e9, 2)}
+            "copies_per_step": len(chunks), "h2d_GBps": round(h2d / (ms * 1e-3) / 1e9, 2),
+            "checked": "bitwise against the device-resident call"}
 
 
 # --------------------------------------------------------- oracle timings
