@@ -638,18 +638,23 @@ def run_gpu_qk(args, rank, world, local):
     achieved = cbytes / (ms_per_step * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
 
-    # End to end: pinned H2D of q, K and seq_lens, the call, D2H of attn.
+    # End to end: pinned H2D of q, K rows c < L_b and seq_lens, the call, D2H
+    # of the attn rows it wrote (rows c < L_b).
     host = {k: t.cpu().pin_memory() for k, t in x.items()}
     dbuf = {k: torch.empty_like(t) for k, t in x.items()}
     attn_d = torch.zeros((w.B, w.Cmax, w.Hq), dtype=torch.float32, device=dev)
     attn_h = torch.empty_like(attn_d, device="cpu").pin_memory()
     e_steps = max(1, min(args.e2e_steps, args.steps))
+    e_lens = [max(0, min(int(v), w.Cmax)) for v in lens]
+    ins = in_range_copies([(dbuf[k], host[k]) for k in host], w, e_lens)
+    outs_back = in_range_copies([(attn_h, attn_d)], w, e_lens)
     with torch.cuda.stream(stream):
         def step():
-            for k in host:
-                dbuf[k].copy_(host[k], non_blocking=True)
+            for d, h in ins:
+                d.copy_(h, non_blocking=True)
             call(dbuf, attn_d)
-            attn_h.copy_(attn_d, non_blocking=True)
+            for h, d in outs_back:
+                h.copy_(d, non_blocking=True)
         for _ in range(3):
             step()
         stream.synchronize()
@@ -665,8 +670,8 @@ def run_gpu_qk(args, rank, world, local):
     e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e_steps
     e2e = {"value": round(cbytes * world / (e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
            "ms_per_step": e_ms, "steps": e_steps,
-           "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host.values()),
-           "d2h_bytes_per_step": attn_h.numel() * 4}
+           "h2d_bytes_per_step": sum(h.numel() * h.element_size() for _, h in ins),
+           "d2h_bytes_per_step": sum(d.numel() * d.element_size() for _, d in outs_back)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -784,10 +789,13 @@ def run_gpu_attn(args, rank, world, local):
     out_d = torch.zeros((w.B, w.Hq, w.D), dtype=torch.float32, device=dev)
     out_h = torch.empty_like(out_d, device="cpu").pin_memory()
     e_steps = max(1, min(args.e2e_steps, args.steps))
+    # Only the K and V rows each sequence reads (c < L_b) go to the device.
+    ins = in_range_copies([(dbuf[k], host[k]) for k in host], w,
+                          [max(0, min(int(v), w.Cmax)) for v in lens])
     with torch.cuda.stream(stream):
         def step():
-            for k in host:
-                dbuf[k].copy_(host[k], non_blocking=True)
+            for d, h in ins:
+                d.copy_(h, non_blocking=True)
             call(dbuf, out_d)
             out_h.copy_(out_d, non_blocking=True)
         for _ in range(3):
@@ -805,7 +813,7 @@ def run_gpu_attn(args, rank, world, local):
     e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e_steps
     e2e = {"value": round(cbytes * world / (e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
            "ms_per_step": e_ms, "steps": e_steps,
-           "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host.values()),
+           "h2d_bytes_per_step": sum(h.numel() * h.element_size() for _, h in ins),
            "d2h_bytes_per_step": out_h.numel() * 4}
 
     cpu = None
@@ -940,6 +948,24 @@ def oracle_baseline_qk(w, x, scale, seconds):
                       f"threads over the affinity mask), {t_total:.1f} s"}
 
 
+def in_range_copies(pairs, w, lens):
+    """(dst, src) flat copies of at most 1 GiB for each (dst, src) tensor pair:
+    for the [B, Cmax, ...] tensors, rows c < L_b of each sequence (contiguous
+    per sequence; rows past a length are never read or written), the rest
+    whole (everything whole when `lens` is None)."""
+    out = []
+    for d, h in pairs:
+        if lens is not None and h.dim() >= 2 and h.shape[0] == w.B and h.shape[1] == w.Cmax:
+            pieces = [(d[b, :L].reshape(-1), h[b, :L].reshape(-1)) for b, L in enumerate(lens) if L > 0]
+        else:
+            pieces = [(d.view(-1), h.view(-1))]
+        for df, hf in pieces:
+            per = max(1, (1 << 30) // hf.element_size())
+            for i in range(0, hf.numel(), per):
+                out.append((df[i:i + per], hf[i:i + per]))
+    return out
+
+
 def run_e2e(gq, w, x, call, dev, args, world):
     """Same call with host inputs, through the public API: every step copies
     from pinned host memory what the call reads -- rows c < L_b of attn and V
@@ -963,17 +989,8 @@ def run_e2e(gq, w, x, call, dev, args, world):
     lens = [max(0, min(int(v), w.Cmax)) for v in x["seq_lens"].cpu().tolist()]
     # Copies of at most 1 GiB, dealt to the copy streams in turn: the rows
     # each sequence reads of the [B, Cmax, ...] tensors, the rest whole.
-    chunks = []
-    for k, h in host.items():
-        if h.dim() >= 2 and h.shape[0] == w.B and h.shape[1] == w.Cmax and not args.paged:
-            pieces = [(dbuf[k][b, :L].reshape(-1), h[b, :L].reshape(-1))
-                      for b, L in enumerate(lens) if L > 0]
-        else:
-            pieces = [(dbuf[k].view(-1), h.view(-1))]
-        for df, hf in pieces:
-            per = max(1, (1 << 30) // hf.element_size())
-            for i in range(0, hf.numel(), per):
-                chunks.append((df[i:i + per], hf[i:i + per]))
+    # A paged cache's blocks are copied whole.
+    chunks = in_range_copies([(dbuf[k], host[k]) for k in host], w, None if args.paged else lens)
     h2d = sum(src.numel() * src.element_size() for _, src in chunks)
 
     def step():
