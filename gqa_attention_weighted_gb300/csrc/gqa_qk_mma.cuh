@@ -67,40 +67,55 @@ __device__ __forceinline__ void split_query(Fp16Tag, float a, float b, uint32_t&
 // 8 (t / N)) and issues the loads of BATCH items before converting any, so
 // the operand costs about one round of global loads per batch (one item a
 // round made the first MMA of an MQA-shaped call wait 4 us for its queries).
+// load_queries issues one batch (items t0, t0 + stride, ... into x),
+// store_queries converts and stores it; convert_queries does every batch.
+template <int N, int BATCH>
+__device__ __forceinline__ void load_queries(const float* q_rows, int heads, int nkc, int t0,
+                                             int stride, float4 (&x)[BATCH][2]) {
+  const int items = N * nkc;
+#pragma unroll
+  for (int u = 0; u < BATCH; ++u) {
+    const int t = t0 + u * stride;
+    const int n = t % N, kc = t / N;
+    if (t < items && n < heads) {
+      const float4* src = reinterpret_cast<const float4*>(q_rows + (size_t)n * nkc * 8 + kc * 8);
+      x[u][0] = src[0];
+      x[u][1] = src[1];
+    } else {
+      x[u][0] = x[u][1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+  }
+}
+
+template <typename Tag, int N, int BATCH>
+__device__ __forceinline__ void store_queries(const float4 (&x)[BATCH][2], int nkc, uint8_t* bst,
+                                              uint32_t b_half, int t0, int stride) {
+  const int items = N * nkc;
+#pragma unroll
+  for (int u = 0; u < BATCH; ++u) {
+    const int t = t0 + u * stride;
+    if (t < items) {
+      const int n = t % N, kc = t / N;
+      uint32_t hi[4], lo[4];
+      split_query(Tag{}, x[u][0].x, x[u][0].y, hi[0], lo[0]);
+      split_query(Tag{}, x[u][0].z, x[u][0].w, hi[1], lo[1]);
+      split_query(Tag{}, x[u][1].x, x[u][1].y, hi[2], lo[2]);
+      split_query(Tag{}, x[u][1].z, x[u][1].w, hi[3], lo[3]);
+      const size_t off = (size_t)((n >> 3) * nkc + kc) * 128 + (n & 7) * 16;
+      *reinterpret_cast<uint4*>(bst + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      *reinterpret_cast<uint4*>(bst + b_half + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+  }
+}
+
 template <typename Tag, int N, int BATCH>
 __device__ __forceinline__ void convert_queries(const float* q_rows, int heads, int nkc,
                                                 uint8_t* bst, uint32_t b_half, int first,
                                                 int stride) {
-  const int items = N * nkc;
-  for (int t0 = first; t0 < items; t0 += BATCH * stride) {
+  for (int t0 = first; t0 < N * nkc; t0 += BATCH * stride) {
     float4 x[BATCH][2];
-#pragma unroll
-    for (int u = 0; u < BATCH; ++u) {
-      const int t = t0 + u * stride;
-      const int n = t % N, kc = t / N;
-      if (t < items && n < heads) {
-        const float4* src = reinterpret_cast<const float4*>(q_rows + (size_t)n * nkc * 8 + kc * 8);
-        x[u][0] = src[0];
-        x[u][1] = src[1];
-      } else {
-        x[u][0] = x[u][1] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < BATCH; ++u) {
-      const int t = t0 + u * stride;
-      if (t < items) {
-        const int n = t % N, kc = t / N;
-        uint32_t hi[4], lo[4];
-        split_query(Tag{}, x[u][0].x, x[u][0].y, hi[0], lo[0]);
-        split_query(Tag{}, x[u][0].z, x[u][0].w, hi[1], lo[1]);
-        split_query(Tag{}, x[u][1].x, x[u][1].y, hi[2], lo[2]);
-        split_query(Tag{}, x[u][1].z, x[u][1].w, hi[3], lo[3]);
-        const size_t off = (size_t)((n >> 3) * nkc + kc) * 128 + (n & 7) * 16;
-        *reinterpret_cast<uint4*>(bst + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(bst + b_half + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-      }
-    }
+    load_queries<N, BATCH>(q_rows, heads, nkc, t0, stride, x);
+    store_queries<Tag, N, BATCH>(x, nkc, bst, b_half, t0, stride);
   }
 }
 

@@ -86,7 +86,12 @@ __global__ void __launch_bounds__(kQkStreamThreads, 1)
   const uint32_t qfree0 = smem_addr(bars + 2 * kMaxStages + 6);
   const uint32_t drain = smem_addr(bars + 2 * kMaxStages + 8);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 9);
-  int* range_rec = reinterpret_cast<int*>(bars + 2 * kMaxStages + 10);
+  int* range_rec = reinterpret_cast<int*>(bars + 2 * kMaxStages + 10);  // 8 ints, 0-4 used
+  // The first segment's queries, converted by the accumulator and converter
+  // warps together (N = 16): in the range record's last 8 bytes.
+  const uint32_t q0ready = smem_addr(bars + 2 * kMaxStages + 13);
+  constexpr bool kFirstTogether = N == 16;
+  constexpr int kFirstWarps = kMmaAccWarps + 1;
   int* lens = reinterpret_cast<int*>(smem + p.lens_off);
 
   if (warp == issuer_warp) {
@@ -108,6 +113,7 @@ __global__ void __launch_bounds__(kQkStreamThreads, 1)
       mbar_init(qfree0 + 8 * j, 1);   // a tcgen05.commit after a segment's last MMA
     }
     mbar_init(drain, 1);
+    mbar_init(q0ready, kFirstWarps);  // one arrival per converting warp
     range_rec[4] = 0;  // the accumulators' abort flag
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -144,6 +150,21 @@ __global__ void __launch_bounds__(kQkStreamThreads, 1)
 
   const int nkc = p.D / 8;                        // 16-byte core-matrix columns along K
   const uint32_t b_half = (uint32_t)N * p.D * 2;  // bytes of the hi (or lo) rows of one buffer
+
+  // With at most 16 heads (N = 16, at most 16 x 32 items) the first
+  // segment's queries are converted into buffer 0 by the four accumulator
+  // warps and the converter warp together, in one round of loads: one warp
+  // alone needed two rounds, and on an MQA-shaped call the first MMA waited
+  // about 4 us for them.
+  if (kFirstTogether && n_iters > 0 && warp < kFirstWarps) {
+    float4 x[4][2];
+    const float* q_rows = p.q + ((size_t)rg.b * p.Hq + h0) * p.D;
+    load_queries<N, 4>(q_rows, p.heads, nkc, tid, 32 * kFirstWarps, x);
+    store_queries<Tag, N, 4>(x, nkc, smem + p.b_off, b_half, tid, 32 * kFirstWarps);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) mbar_arrive(q0ready);
+  }
 
   if (warp == producer_warp) {
     // ----------------------------------------------------------------- producer
@@ -183,7 +204,9 @@ __global__ void __launch_bounds__(kQkStreamThreads, 1)
     int e = 0;
     for (int it = 0; it < n_iters; ++it) {
       const bool seg_start = it == 0 || cur.j == 0;
-      if (seg_start) {
+      if (seg_start && kFirstTogether && e == 0) {
+        ++e;  // converted above, with the accumulator warps
+      } else if (seg_start) {
         const int buf = e & 1;
         if (e >= 2 && !mbar_wait(qfree0 + 8 * buf, ((e - 2) >> 1) & 1, p.timeout_ns)) {
           if (lane == 0) atomicOr(p.status, kErrMmaWait);
@@ -212,7 +235,13 @@ __global__ void __launch_bounds__(kQkStreamThreads, 1)
         const bool seg_end = cur.j == cur.n - 1 || it == n_iters - 1;
         if (seg_start) {
           ++e;
-          if (!mbar_poll(qready0 + 8 * (e & 1), (e >> 1) & 1, p.timeout_ns)) {
+          // Segment 0 (converted together) completes q0ready; then buffer 0's
+          // qready first completes for segment 2.
+          const bool first = kFirstTogether && e == 0;
+          const uint32_t bar = first ? q0ready : qready0 + 8 * (e & 1);
+          const uint32_t parity =
+              first ? 0u : (kFirstTogether && (e & 1) == 0 ? ((e >> 1) - 1) & 1 : (e >> 1) & 1);
+          if (!mbar_poll(bar, parity, p.timeout_ns)) {
             atomicOr(p.status, kErrMmaWait);
             break;
           }
