@@ -34,7 +34,8 @@
 //     context row a thread) add hi + lo, scale, write the row's scores and
 //     keep a running (max, sum of exp) per head.
 //
-// Warps: 0-3 accumulate, 4 converts each segment's queries, 5 is the TMA
+// Warps: 0-3 accumulate, 4 converts each segment's queries (with at most 16
+// heads, warps 0-4 convert the first segment's together), 5 is the TMA
 // producer, 6 owns tensor memory and one of its threads issues the MMAs.
 // Every mbarrier wait is bounded; on expiry the CTA sets the device status
 // word, lets its copies and MMAs in flight finish, frees its tensor memory and
