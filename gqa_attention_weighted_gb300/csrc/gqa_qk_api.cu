@@ -90,6 +90,7 @@ QkKernel pick_mma(int nb) {
 // Engines: the CUDA-core FMA kernel, the tcgen05 kernel with fixed splits,
 // and the streamed tcgen05 kernel (the default where it applies).
 constexpr int kQkEngineFma = 1, kQkEngineTensor = 2, kQkEngineStream = 3;
+constexpr int kQkStreamStages = 2;  // K ring depth of the streamed score kernel
 
 struct QkPlan {
   int engine, npad, b_off, tmem_cols, threads;
@@ -228,8 +229,7 @@ int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int k_dtype, int mode
   if (p->engine == kQkEngineStream) {
     // Two CTAs an SM where two fit (registers and shared memory; one at
     // D = 256, whose 64 KiB stages need the room), in groups of one CTA per
-    // head group, each with as many 128-row stages in flight as its share of
-    // shared memory holds.
+    // head group, each with a ring of two 128-row stages.
     QkKernel kfn = k_dtype == GQA_AV_BF16 ? pick_stream<Bf16Tag>(p->npad / 16)
                                           : pick_stream<Fp16Tag>(p->npad / 16);
     if (!kfn) return qfail(GQA_AV_ERR_UNSUPPORTED, "no score kernel for this head count");
@@ -239,8 +239,11 @@ int plan(int dev, int B, int Cmax, int Hq, int Hkv, int D, int k_dtype, int mode
     for (int per_sm = D <= 128 ? 2 : 1; per_sm >= 1; --per_sm) {
       const int budget =
           std::min(optin, static_cast<int>(prop.sharedMemPerMultiprocessor) / per_sm - 1024);
-      // As many stages as the CTA's share of shared memory holds (2 to 8).
-      for (p->stages = kMaxStages; p->stages >= 2; --p->stages) {
+      // Two 128-row stages: at D <= 128 that is what two CTAs' shares of
+      // shared memory hold; at D = 256 a third 64 KB stage left no room for
+      // the normalise kernel's CTAs to start next to the score kernel's, and
+      // measured slower (MQA-style call 27.2 us against 26.0 with two).
+      for (p->stages = kQkStreamStages; p->stages >= 2; --p->stages) {
         p->b_off = p->stages * p->stage_bytes;
         p->red_off = p->b_off + 2 * 2 * p->npad * D * 2;
         p->bar_off = p->red_off + kMmaAccWarps * p->npad * 8;
