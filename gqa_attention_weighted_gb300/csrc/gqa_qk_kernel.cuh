@@ -106,21 +106,8 @@ __device__ __forceinline__ void lse_merge(float& m, float& l, float m2, float l2
   l = a + b;
 }
 
-// The (max, sum of exp(x - max)) of the pairs held by a warp's lanes: the
-// maximum first, then every lane's sum rescaled to it and added up, each by a
-// fixed butterfly (so bitwise reproducible). One exponential a lane, against
-// one a level for a butterfly of pair merges.
-__device__ __forceinline__ float2 warp_lse(float m, float l) {
-  float M = m;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float s = m == -INFINITY ? 0.0f : l * __expf(m - M);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  return make_float2(M, s);
-}
-
-// The same over `n` pairs in memory, in index order.
+// The (max, sum of exp(x - max)) of `n` pairs in memory (stride apart): the
+// maximum first, then every pair's sum rescaled to it, added in index order.
 __device__ __forceinline__ float2 lse_of(const float2* v, int n, int stride) {
   float M = -INFINITY, S = 0.0f;
   for (int i = 0; i < n; ++i) M = fmaxf(M, v[(size_t)i * stride].x);
