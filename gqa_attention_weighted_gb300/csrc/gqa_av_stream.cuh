@@ -69,6 +69,34 @@ struct StreamRange {
   int b, j;
 };
 
+// Sequence b and stage j holding stage s0 of a column: P_b <= s0 < P_b + n_b,
+// P_b the stages of the sequences before b, found by a warp prefix scan in
+// the integer type I. Warp-collective.
+template <typename I>
+__device__ __forceinline__ bool stream_locate(const int* lens, int B, int R, I s0, StreamRange& r) {
+  const int lane = threadIdx.x & 31;
+  I base = 0;  // P of the first sequence of this chunk of 32
+  for (int b0 = 0; b0 < B; b0 += 32) {
+    const int b = b0 + lane;
+    const I n = b < B ? static_cast<I>(stream_stages(lens[b], R)) : I(0);
+    I incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const I t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, n > 0 && s0 >= base + incl - n && s0 < base + incl);
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      r.b = b0 + src;
+      r.j = static_cast<int>(s0 - base - __shfl_sync(0xffffffffu, incl - n, src));
+      return true;
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return false;  // unreachable: s0 < T
+}
+
 // Warp-collective (the producer warp): stores the clamped lengths in `lens`
 // and works out the range of group g of Ug in a column.
 __device__ __forceinline__ StreamRange stream_range(const int32_t* seq_lens, int B, int Cmax,
@@ -81,38 +109,35 @@ __device__ __forceinline__ StreamRange stream_range(const int32_t* seq_lens, int
     T += stream_stages(L, R);
   }
   __syncwarp();  // the warp's lanes read each other's lengths below
+  if (__all_sync(0xffffffffu, T < (1LL << 26))) {
+    // 32 partial sums below 2^26 add up to less than 2^31: one warp reduction.
+    T = __reduce_add_sync(0xffffffffu, static_cast<unsigned>(T));
+  } else {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) T += __shfl_xor_sync(0xffffffffu, T, o);
+    for (int o = 16; o > 0; o >>= 1) T += __shfl_xor_sync(0xffffffffu, T, o);
+  }
   StreamRange r;
   r.b = 0; r.j = 0; r.count = 0;
   // With fewer stages than groups only the first T groups take one each:
   // every CTA that streams has at least one stage (the combine relies on it).
   if (static_cast<long long>(Ug) > T) Ug = static_cast<int>(T);
   if (g >= Ug) return r;
-  const long long s0 = stream_first(T, g, Ug);
-  r.count = static_cast<int>(stream_first(T, g + 1, Ug) - s0);
-  // Sequence b holding stage s0: P_b <= s0 < P_b + n_b, P_b the stages of the
-  // sequences before b, found by a warp prefix scan.
-  long long base = 0;  // P of the first sequence of this chunk of 32
-  for (int b0 = 0; b0 < B; b0 += 32) {
-    const int b = b0 + lane;
-    const int n = b < B ? stream_stages(lens[b], R) : 0;
-    long long incl = n;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    const unsigned hit = __ballot_sync(0xffffffffu, n > 0 && s0 >= base + incl - n && s0 < base + incl);
-    if (hit) {
-      const int src = __ffs(hit) - 1;
-      r.b = b0 + src;
-      r.j = static_cast<int>(s0 - base - __shfl_sync(0xffffffffu, incl - n, src));
-      return r;
-    }
-    base += __shfl_sync(0xffffffffu, incl, 31);
+  bool found;
+  if (T < (1LL << 31) && Ug < (1 << 15)) {
+    // The usual sizes, in 32-bit arithmetic: with T = q Ug + r0,
+    // floor(T g / Ug) = q g + floor(r0 g / Ug), and r0 g < 2^30.
+    const unsigned t = static_cast<unsigned>(T), ug = static_cast<unsigned>(Ug);
+    const unsigned q = t / ug, r0 = t - q * ug;
+    const unsigned s0 = q * g + (r0 * g) / ug;
+    const unsigned s1 = q * (g + 1) + (r0 * (g + 1)) / ug;
+    r.count = static_cast<int>(s1 - s0);
+    found = stream_locate<int>(lens, B, R, static_cast<int>(s0), r);
+  } else {
+    const long long s0 = stream_first(T, g, Ug);
+    r.count = static_cast<int>(stream_first(T, g + 1, Ug) - s0);
+    found = stream_locate<long long>(lens, B, R, s0, r);
   }
-  r.count = 0;  // unreachable: s0 < T
+  if (!found) r.count = 0;  // unreachable: s0 < T
   return r;
 }
 
@@ -211,12 +236,12 @@ __global__ void __launch_bounds__(kMmaMaxThreads, NB == 1 ? 3 : (NB == 2 ? 2 : 1
 
   if (warp == producer_warp) {
     // ----------------------------------------------------------------- producer
-    const int per_row = p.heads / p.avec;
+    const int per_row = p.avec == 4 ? p.heads >> 2 : (p.avec == 2 ? p.heads >> 1 : p.heads);
     bool ok = true;
     int issued = 0;
+    int stage = 0;
+    uint32_t parity = 1;  // of the empty barrier: a fresh slot passes at once
     for (int it = 0; it < n_iters; ++it) {
-      const int stage = it % p.stages;
-      const uint32_t parity = ((it / p.stages) & 1) ^ 1;  // a fresh slot passes at once
       if (it >= p.stages && !mbar_wait(empty0 + 8 * stage, parity, p.timeout_ns)) {
         atomicOr(p.status, kErrEmptyWait);
         ok = false;
@@ -253,6 +278,7 @@ __global__ void __launch_bounds__(kMmaMaxThreads, NB == 1 ? 3 : (NB == 2 ? 2 : 1
       }
       issued = it + 1;
       stream_advance(cur, p.B, p.R, lens);
+      if (++stage == p.stages) { stage = 0; parity ^= 1u; }
     }
     cp_async_wait_all();
     if (!ok) {
@@ -272,9 +298,11 @@ __global__ void __launch_bounds__(kMmaMaxThreads, NB == 1 ? 3 : (NB == 2 ? 2 : 1
     const uint32_t b_sbo = (uint32_t)(p.R / 8) * 128;  // next 8 rows of B
     if (lane == 0) {
       int issued = 0;
+      int stage = 0;
+      uint32_t phase = 0;
       for (int it = 0; it < n_iters; ++it) {
-        const int stage = it % p.stages, j = it & 1;
-        if (!mbar_poll(bready0 + 8 * stage, (it / p.stages) & 1, p.timeout_ns) ||
+        const int j = it & 1;
+        if (!mbar_poll(bready0 + 8 * stage, phase, p.timeout_ns) ||
             (it >= 2 && !mbar_poll(dfree0 + 8 * j, ((it - 2) >> 1) & 1, p.timeout_ns))) {
           atomicOr(p.status, kErrMmaWait);
           break;
@@ -293,6 +321,7 @@ __global__ void __launch_bounds__(kMmaMaxThreads, NB == 1 ? 3 : (NB == 2 ? 2 : 1
         mma_commit(empty0 + 8 * stage);  // V, attn and B slots free once these MMAs are done
         mma_commit(dfull0 + 8 * j);
         issued = it + 1;
+        if (++stage == p.stages) { stage = 0; phase ^= 1u; }
       }
       if (issued > 0) {
         mma_commit(drain);
@@ -314,9 +343,10 @@ __global__ void __launch_bounds__(kMmaMaxThreads, NB == 1 ? 3 : (NB == 2 ? 2 : 1
     const int ctid = tid - 32 * kMmaAccWarps;
     const int nkc = p.R / 8;
     const int items = N * nkc;
+    int stage = 0;
+    uint32_t phase = 0;
     for (int it = 0; it < n_iters; ++it) {
-      const int stage = it % p.stages;
-      if (!mbar_poll(full0 + 8 * stage, (it / p.stages) & 1, p.timeout_ns)) {
+      if (!mbar_poll(full0 + 8 * stage, phase, p.timeout_ns)) {
         atomicOr(p.status, kErrFullWait);
         break;
       }
@@ -354,6 +384,7 @@ __global__ void __launch_bounds__(kMmaMaxThreads, NB == 1 ? 3 : (NB == 2 ? 2 : 1
       __syncwarp();
       if (lane == 0) mbar_arrive(bready0 + 8 * stage);
       stream_advance(cur, p.B, p.R, lens);
+      if (++stage == p.stages) { stage = 0; phase ^= 1u; }
     }
     return;
   }

@@ -171,10 +171,10 @@ __global__ void __launch_bounds__(kQkStreamThreads, 1)
     // ----------------------------------------------------------------- producer
     bool ok = true;
     int issued = 0;
+    int stage = 0;
+    uint32_t parity = 1;  // of the empty barrier: a fresh slot passes at once
     for (int it = 0; it < n_iters; ++it) {
-      const int stage = it % p.stages;
-      if (it >= p.stages &&
-          !mbar_poll(empty0 + 8 * stage, ((it / p.stages) & 1) ^ 1, p.timeout_ns)) {
+      if (it >= p.stages && !mbar_poll(empty0 + 8 * stage, parity, p.timeout_ns)) {
         if (lane == 0) atomicOr(p.status, kErrEmptyWait);
         ok = false;
         break;
@@ -189,6 +189,7 @@ __global__ void __launch_bounds__(kQkStreamThreads, 1)
       }
       issued = it + 1;
       stream_advance(cur, p.B, kQkMmaRows, lens);
+      if (++stage == p.stages) { stage = 0; parity ^= 1u; }
     }
     if (!ok) {
       for (int it = max(0, issued - p.stages); it < issued; ++it)
@@ -230,8 +231,10 @@ __global__ void __launch_bounds__(kQkStreamThreads, 1)
     if (lane == 0) {
       const uint32_t idesc = qk_mma_idesc<Tag>(2 * N);
       int issued = 0, e = -1;
+      int stage = 0;
+      uint32_t phase = 0;
       for (int it = 0; it < n_iters; ++it) {
-        const int stage = it % p.stages, j = it & 1;
+        const int j = it & 1;
         const bool seg_start = it == 0 || cur.j == 0;
         const bool seg_end = cur.j == cur.n - 1 || it == n_iters - 1;
         if (seg_start) {
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(kQkStreamThreads, 1)
             break;
           }
         }
-        if (!mbar_poll(full0 + 8 * stage, (it / p.stages) & 1, p.timeout_ns) ||
+        if (!mbar_poll(full0 + 8 * stage, phase, p.timeout_ns) ||
             (it >= 2 && !mbar_poll(dfree0 + 8 * j, ((it - 2) >> 1) & 1, p.timeout_ns))) {
           atomicOr(p.status, kErrMmaWait);
           break;
@@ -269,6 +272,7 @@ __global__ void __launch_bounds__(kQkStreamThreads, 1)
         if (seg_end) mma_commit(qfree0 + 8 * (e & 1));  // and the segment's queries
         issued = it + 1;
         stream_advance(cur, p.B, kQkMmaRows, lens);
+        if (++stage == p.stages) { stage = 0; phase ^= 1u; }
       }
       if (issued > 0) {
         mma_commit(drain);

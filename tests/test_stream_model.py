@@ -31,14 +31,27 @@ def stages_of(L, R):
     return max(1, -(-L // R))
 
 
+M32 = (1 << 32) - 1
+
+
+def first_stage(T, g, Ug):
+    """floor(T g / Ug), as the producer warp computes it: in unsigned 32-bit
+    arithmetic with T = q Ug + r0 when T < 2^31 and Ug < 2^15, else in 64-bit."""
+    if T < (1 << 31) and Ug < (1 << 15):
+        q = (T & M32) // Ug
+        r0 = (T - q * Ug) & M32
+        return ((q * g) & M32) + ((r0 * g) & M32) // Ug & M32
+    return T * g // Ug
+
+
 def stream_range(lens, R, g, Ug):
     """(count, b, j) of group g in a column, as the producer warp finds them."""
     T = sum(stages_of(L, R) for L in lens)
     Ug = min(Ug, T)
     if g >= Ug:
         return 0, 0, 0
-    s0 = T * g // Ug
-    count = T * (g + 1) // Ug - s0
+    s0, s1 = first_stage(T, g, Ug), first_stage(T, g + 1, Ug)
+    count = s1 - s0
     assert count >= 1
     base = 0
     for b, L in enumerate(lens):  # the warp scan, one sequence at a time
@@ -164,3 +177,20 @@ def test_more_ctas_than_stages():
     # Fewer stages than CTAs: most CTAs have none; each stage still once.
     check([5, 0, 17], 16, 1, 152)
     check([0], 64, 1, 304)
+
+
+def test_first_stage_32bit_path():
+    # The 32-bit path is floor(T g / Ug) exactly, with nothing wrapping, up to
+    # its bounds (T < 2^31, Ug < 2^15, g <= Ug); the 64-bit path takes the rest.
+    rng = random.Random(11)
+    cases = [((1 << 31) - 1, (1 << 15) - 1), ((1 << 31) - 1, 1), (1, 1), (12345, 304)]
+    for _ in range(20000):
+        Ug = rng.choice([1, 2, 3, 7, 19, 38, 152, 304, 4096, (1 << 15) - 1, rng.randint(1, (1 << 15) - 1)])
+        T = rng.choice([Ug, Ug + 1, rng.randint(Ug, (1 << 31) - 1), (1 << 31) - 1 - rng.randint(0, 99)])
+        cases.append((max(T, Ug), Ug))
+    for T, Ug in cases:
+        for g in {0, 1, Ug // 2, Ug - 1, Ug, rng.randint(0, Ug)}:
+            q, r0 = T // Ug, T % Ug
+            assert q * g < (1 << 32) and r0 * g < (1 << 30) + (1 << 15)
+            assert first_stage(T, g, Ug) == T * g // Ug, (T, g, Ug)
+    assert first_stage(1 << 40, 5, 7) == (1 << 40) * 5 // 7
