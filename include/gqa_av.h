@@ -104,27 +104,40 @@ int gqa_av_decode_per_head(const float *attn, const void *v_cache, const int32_t
 
 /*
  * Launch-shape overrides for sweeps and tests. A field <= 0 keeps the
- * library's choice. nsplit: context splits per tile (of a full-length
- * sequence; with balanced splits, see split_mode, the CTAs the batch's
- * context is spread over are tiles x nsplit); dtile: output columns
- * per CTA (a multiple of 8 dividing D, <= 256); rows_per_stage: V rows per
- * pipeline stage (8..256); stages: pipeline depth (2..8); early_stages:
- * stages each CTA issues before it has read its sequence length (1..stages;
- * the library issues one, since rows past a length are read for nothing and
- * the first stage lands later behind the others; with balanced splits none
- * are, though the value is still checked against stages); engine: 0 lets the library
- * pick, 1 forces the CUDA-core packed-FMA kernel, 2 the tcgen05 tensor-core
- * kernel (head groups of <= 64 heads and D >= 64 with D <= 128 or
- * D % 128 == 0; the library picks it wherever it applies unless dtile is
- * set, and with it dtile must be min(D, 128) or unset; rows_per_stage must
- * then be a multiple of 16); split_mode: 1 fixed splits (split s of each
- * sequence covers rows [s, s + 1) x rows_per_split, and splits past a
- * sequence's length have no work), 2 balanced splits (tensor-core engine
- * only: every CTA reads all lengths and the batch's context rows are cut into
- * equal splits of whole stages, each sequence getting splits in proportion
- * to its length), 0 lets the library pick (balanced for the tensor-core
- * engine on shapes with at least as many tiles as SMs, else fixed). Results
- * stay within the stated tolerance for every choice, and are bitwise
+ * library's choice.
+ *   nsplit: context splits per tile (of a full-length sequence); with
+ *     balanced splits the batch's context is spread over tiles x nsplit
+ *     CTAs; with streamed splits it is the CTAs per SM (1..4, default 2).
+ *   dtile: output columns per CTA (a multiple of 8 dividing D, <= 256).
+ *   rows_per_stage: V rows per pipeline stage (8..256).
+ *   stages: pipeline depth (2..8).
+ *   early_stages: stages each CTA issues before it has read its sequence
+ *     length (1..stages). With fixed splits the library issues one: rows past
+ *     a length are read for nothing and the first stage lands later behind
+ *     the others. Balanced and streamed splits issue none (a CTA finds its
+ *     range from the lengths), though the value is still checked against
+ *     stages.
+ *   engine: 0 lets the library pick, 1 forces the CUDA-core packed-FMA
+ *     kernel, 2 the tcgen05 tensor-core kernel (head groups of <= 64 heads
+ *     and D >= 64 with D <= 128 or D % 128 == 0; dtile must then be
+ *     min(D, 128) or unset and rows_per_stage a multiple of 16). The library
+ *     picks the tensor-core kernel where it applies and the CTA has 8 or more
+ *     heads or the call streams 2^18 tile rows or more (there the FMA kernel
+ *     is bound by its own arithmetic issue), else the FMA kernel (short calls
+ *     with few heads are latency-bound); setting dtile selects the FMA kernel.
+ *   split_mode: 1 fixed splits (split s of each sequence covers rows
+ *     [s, s + 1) x rows_per_split, and splits past a sequence's length have
+ *     no work); 2 balanced splits (tensor-core engine only: every CTA reads
+ *     all lengths and the batch's context rows are cut into equal splits of
+ *     whole stages); 3 streamed splits (tensor-core engine only, contiguous V,
+ *     B <= 2048: persistent CTAs, nsplit CTAs an SM, each take an equal run
+ *     of one column of the call's stage list across sequence boundaries);
+ *     0 lets the library pick: fixed for the FMA kernel; streamed for the
+ *     tensor-core kernel, except where streaming does not apply (paged V,
+ *     B > 2048) or nsplit or early_stages is set, where it takes balanced
+ *     splits on shapes with at least as many tiles as SMs and fixed splits on
+ *     the others.
+ * Results stay within the stated tolerance for every choice, and are bitwise
  * reproducible for a fixed choice and fixed lengths. Tunings apply to the TMA
  * kernels only: a call that would run the generic kernel (D % 8 != 0 or a
  * pointer not 16-byte aligned) with any field set returns
@@ -171,12 +184,15 @@ typedef struct gqa_av_plan_info {
     int early_stages;    /* stages issued before the sequence length is read (0: none) */
     int engine;          /* 1 CUDA-core packed FMA, 2 tcgen05 tensor cores, 3 generic
                             (D % 8 != 0; a call with misaligned pointers also runs it) */
-    int split_mode;      /* 1 fixed splits, 2 balanced over the batch's lengths */
-    int nsplit;          /* context splits per tile (of a full-length sequence) */
+    int split_mode;      /* 1 fixed, 2 balanced over the batch's lengths, 3 streamed */
+    int nsplit;          /* context splits per tile (of a full-length sequence);
+                            streamed: CTAs per SM */
     int combine_ctas;    /* CTAs of the split-combine kernel (0: not launched) */
     int rows_per_split;  /* of a full-length sequence */
     int tiles;           /* (head groups) x B x (D / dtile) */
-    int ctas;            /* tiles x nsplit; tiles x (nsplit + 1) with balanced splits */
+    int ctas;            /* tiles x nsplit; tiles x (nsplit + 1) with balanced splits;
+                            streamed: (head groups x D / dtile) x the groups that fit
+                            nsplit CTAs on every SM */
     int threads_per_cta;
     int smem_bytes;
     int ctas_per_sm;     /* occupancy of this kernel at this shared-memory size */
